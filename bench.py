@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the OSCAR INT2 KV-cache decode step on GB300.
+
+Workload: one Qwen3-8B-shaped attention layer (32 query / 8 KV heads, head_dim 128) at 100,000 tokens
+of context = 64 BF16 sink + 99,680 INT2 history (paged, shuffled page table, partial last page) + 256
+BF16 recent, batch 1, group 128, clip 0.9, covariance-aligned rotations computed on the GPU from
+synthetic anisotropic calibration samples.  One step = append the new token (demoting the oldest
+recent token into the INT2 history) + decode attention over the whole pool.  Steps rotate over
+several layer buffers whose total size exceeds the L2 cache, so every step reads its KV from HBM.
+
+Metric: KV tokens/s (tokens of context attended per second, one layer, all heads), with the history
+kernel's achieved HBM bandwidth against the measured peak.  Synthetic data (seeded); no weights.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes as C
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L_CTX, HQ, HKV, D, GROUP, CLIP = 100_000, 32, 8, 128, 128, 0.9
+SINK, RECENT, PAGE = 64, 256, 64
+CALIB_T = 4096
+METRIC = "INT2-KV decode attn: KV tokens/s, HBM GB/s as frac of GB300 peak; demote tok/s"
+WORKLOAD = "qwen3-8b-layer decode, 100k context (64 sink + 99,680 INT2 history + 256 recent), batch 1"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8, help="rotating layer buffers (working set > L2)")
+    ap.add_argument("--e2e-steps", type=int, default=2000)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------------
+# Oracle CPU baseline (the only place besides --impl reference that runs oracle/): one decode step
+# of KV head 0 (its 4 query heads), i.e. 1/8 of the layer's step, repeated within a time budget.
+def cpu_baseline_child(budget_s: float) -> dict:
+    import numpy as np
+    import synth
+    from oracle import pool as opool
+    from oracle import rotation as orot
+    ch = synth.outlier_channels(7, 1, D, 4)
+    K = synth.outlier_kv(8, L_CTX + 64, 1, D, ch)
+    V = synth.outlier_kv(9, L_CTX + 64, 1, D, ch)
+    q = synth.outlier_q(10, 1, HQ // HKV, 1, D, ch)
+    R = orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(11, D)))[None]
+    hist = L_CTX - SINK - RECENT
+    pages = -(-hist // PAGE) + 2
+    O = opool.Pool(1, HQ // HKV, 1, D, GROUP, pages, pages, R, R, [CLIP], [CLIP])
+    O.page_table[0] = synth.shuffled_pages(12, pages)
+    O.prefill(0, K[:L_CTX], V[:L_CTX])
+    n, t_total, ctx = 0, 0.0, 0
+    while t_total < budget_s and n < 64:
+        t0 = time.perf_counter()
+        O.append(K[L_CTX + n][None], V[L_CTX + n][None])
+        O.decode(q)
+        t_total += time.perf_counter() - t0
+        ctx += L_CTX + n + 1
+        n += 1
+    # KV tokens/s of the full layer: this sample did 1/8 of each step's work
+    return {"value": ctx / t_total / HKV, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} decode steps of KV head 0 (4 of 32 query heads, 1/8 of the layer) at 100k context, "
+                      "append with demotion + float64 attention; value scaled to the full layer",
+            "seconds": round(t_total, 3)}
+
+
+def run_cpu_baseline(budget_s: float) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--cpu-seconds",
+                        str(budget_s)], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float) -> dict:
+        """Summarise the samples taken between wall-clock times t0 and t1 (the timed region)."""
+        import datetime
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if not (t0 <= ts <= t1):
+                    continue
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_from_profiles(kernel_src: str):
+    """DRAM bytes per launch of the history kernel from the committed ncu summary, if the kernel's
+    source has not changed since that capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "hist_partial_decode100k.md")
+    if not os.path.exists(path):
+        return None
+    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(path):
+        if ":" in line and line.startswith("- "):
+            k, v = line[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------------------------
+def setup_layers(n_layers: int, extra_tokens: int, seed: int = 2024):
+    import torch
+    import numpy as np
+    import bit_rotated_kv_02_gb300 as ok
+    import synth
+    dev = torch.device("cuda")
+    G = HQ // HKV
+    # covariance-aligned rotations from synthetic calibration samples (one set shared by the layers)
+    ch = synth.outlier_channels(seed, HKV, D, 4)
+    Rk, Rv = [], []
+    for h in range(HKV):
+        chh = ch[h:h + 1]
+        Qc = synth.calib_samples(seed + 10 + h, CALIB_T, G, D, chh, heads_per_channel_set=G)
+        KVc = synth.calib_samples(seed + 50 + h, CALIB_T, 2, D, chh, heads_per_channel_set=2)
+        tq = torch.from_numpy(Qc.view(np.int16)).view(torch.bfloat16).to(dev)
+        tk = torch.from_numpy(np.ascontiguousarray(KVc[:, 0]).view(np.int16)).view(torch.bfloat16).to(dev)
+        tv = torch.from_numpy(np.ascontiguousarray(KVc[:, 1]).view(np.int16)).view(torch.bfloat16).to(dev)
+        Rk.append(ok.oscar_make_rotation(ok.oscar_calib_covariance_k(tq), ok.ROT_COVARIANCE)[1])
+        Rv.append(ok.oscar_make_rotation(ok.oscar_calib_covariance_v(tq, tk, tv), ok.ROT_COVARIANCE)[1])
+    Rk, Rv = torch.stack(Rk), torch.stack(Rv)
+    clip = torch.full((HKV,), CLIP, dtype=torch.float32)
+    hist = L_CTX - SINK - RECENT
+    pages = -(-(hist + extra_tokens) // PAGE) + 1
+    gen = torch.Generator(device=dev)
+    chan = torch.from_numpy(ch.astype(np.int64)).to(dev)
+    layers = []
+    for l in range(n_layers):
+        gen.manual_seed(seed + 1000 + l)
+        P = ok.Pool(1, HQ, HKV, GROUP, pages, pages, Rk, Rv, clip, clip)
+        P.set_page_table(torch.randperm(pages, generator=gen, device=dev).to(torch.int32)[None])
+        for which in range(2):
+            x = torch.randn((L_CTX, HKV, D), generator=gen, device=dev)
+            x.scatter_(2, chan[None].expand(L_CTX, -1, -1), x.gather(2, chan[None].expand(L_CTX, -1, -1)) * 20)
+            if which == 0:
+                kx = x.to(torch.bfloat16)
+            else:
+                vx = x.to(torch.bfloat16)
+        ok.oscar_prefill_pool(P, 0, kx, vx)
+        del kx, vx
+        layers.append(P)
+    torch.cuda.synchronize()
+    for P in layers:
+        assert P.err() == 0
+    return layers
+
+
+def main():
+    args = parse()
+    if args.cpu_baseline_child:
+        print(json.dumps(cpu_baseline_child(args.cpu_seconds)))
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            cpu = cpu_baseline_child(args.cpu_seconds)
+            val = cpu["value"]
+            print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "KV tokens/s",
+                              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": 1000.0 * L_CTX / val if val else None, "higher_is_better": True,
+                              "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                              "config": {"workload": WORKLOAD + " (oracle sample: KV head 0)"},
+                              "cpu_baseline": cpu,
+                              "e2e": {"value": val, "unit": "KV tokens/s", "h2d_bytes_per_step": 0,
+                                      "d2h_bytes_per_step": 0}}))
+        return
+
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    import bit_rotated_kv_02_gb300 as ok
+    from bit_rotated_kv_02_gb300 import _lib
+    lib = ok.lib()
+
+    NL = args.layers
+    total = args.warmup + args.steps + args.e2e_steps
+    per_layer = -(-total // NL)
+    layers = setup_layers(NL, per_layer + 8)
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77 + rank)
+    NQ = 64
+    qs = (torch.randn((NQ, 1, HQ, D), generator=gen, device=dev) * 3).to(torch.bfloat16)
+    kn = (torch.randn((NQ, 1, HKV, D), generator=gen, device=dev) * 3).to(torch.bfloat16)
+    vn = (torch.randn((NQ, 1, HKV, D), generator=gen, device=dev) * 3).to(torch.bfloat16)
+    outs = [torch.empty((1, HQ, D), dtype=torch.float32, device=dev) for _ in range(NL)]
+    ws_bytes = ok.oscar_decode_workspace_size(layers[0], 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+    scale = 1.0 / math.sqrt(D)
+    appended = [0] * NL
+
+    def step(i, ev=None):
+        l = i % NL
+        P = layers[l]
+        if ev is not None:
+            lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
+            lib.oscar_profile_events(1, C.c_void_p(ev[2].cuda_event), C.c_void_p(ev[3].cuda_event))
+        j = i % NQ
+        st = lib.oscar_append_kv(P.ref, C.c_void_p(kn[j].data_ptr()), C.c_void_p(vn[j].data_ptr()), sp)
+        st |= lib.oscar_decode_attention(P.ref, C.c_void_p(qs[j].data_ptr()), C.c_void_p(outs[l].data_ptr()),
+                                         scale, 0, C.c_void_p(ws.data_ptr()), ws_bytes, sp)
+        if st:
+            raise RuntimeError(lib.oscar_last_error_string().decode())
+        appended[l] += 1
+        return L_CTX + appended[l]      # tokens attended in this step
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or "0"
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tokens = 0
+    wall0 = time.time()
+    t_start.record()
+    for i in range(args.steps):
+        tokens += step(args.warmup + i, evs[i])
+    t_stop.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop(wall0, time.time())
+    ms = t_start.elapsed_time(t_stop)
+    hist_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dem_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    for P in layers:
+        if P.err() != 0:
+            raise RuntimeError(f"device error flags {P.err():#x}")
+
+    # end to end through the public API: pinned host inputs copied in, result copied out, every step
+    hq = torch.empty((1, HQ, D), dtype=torch.bfloat16).pin_memory()
+    hk = torch.empty((1, HKV, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((1, HKV, D), dtype=torch.bfloat16).pin_memory()
+    hq.copy_(qs[0].cpu()); hk.copy_(kn[0].cpu()); hv.copy_(vn[0].cpu())
+    hout = torch.empty((1, HQ, D), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(kn[0]), torch.empty_like(vn[0])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_tokens = 0
+    base = args.warmup + args.steps
+    e0.record()
+    for i in range(args.e2e_steps):
+        l = (base + i) % NL
+        dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+        ok.oscar_append_kv(layers[l], dk, dv)
+        ok.oscar_decode_attention(layers[l], dq, out=outs[l], num_splits=0, ws=ws)
+        hout.copy_(outs[l], non_blocking=True)
+        appended[l] += 1
+        e2e_tokens += L_CTX + appended[l]
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # algorithmic bytes of the history kernel per launch (codes + scale/zero + page table + q)
+    hist_tokens_avg = (tokens / args.steps) - SINK - RECENT
+    hist_bytes = hist_tokens_avg * HKV * 2 * (D // 4 + 4 * (D // GROUP)) + 4 * math.ceil(hist_tokens_avg / PAGE) \
+        + HQ * D * 2
+    bf16_bytes = (SINK + RECENT) * HKV * 2 * D * 2
+    step_bytes = hist_bytes + bf16_bytes + HQ * D * 4 + HKV * 2 * D * 2 * 3 + HKV * 2 * (D // 4 + 4)
+    hist_mean_ms = statistics.mean(hist_ms)
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    achieved = hist_bytes / (hist_mean_ms * 1e-3) / 1e9
+    value = world * tokens / (ms * 1e-3)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        rec = {
+            "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int2-kv/f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D,
+                       "group_size": GROUP, "clip": CLIP, "page_tokens": PAGE, "rotation": "covariance (GPU calib)",
+                       "l2": f"{NL} rotating layer buffers ({NL * step_bytes / 1e6:.0f} MB > L2)",
+                       "parallelism": f"replicas x{world}"},
+            "decode_steps_per_s": world * args.steps / (ms * 1e-3),
+            "bytes_per_step": step_bytes,
+            "step_gbs": step_bytes * args.steps / (ms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "hist_partial_kernel", "achieved": achieved, "peak": peak,
+                         "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic_from_profiles(os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc",
+                                                                       "decode.cu")),
+                         "algorithmic_bytes_per_launch": hist_bytes, "mean_launch_us": hist_mean_ms * 1e3},
+            "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
+                       statistics.mean(dem_ms) * 1e3, "note": "append+demote kernel, 1 token x 8 KV heads x K/V per launch"},
+            "e2e": {"value": world * e2e_tokens / (e2e_ms * 1e-3), "unit": "KV tokens/s",
+                    "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
+                    "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
+            "gpu_launches": args.steps * 4,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(rec))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+"""Python binding of liboscar.so — the GB300 (sm_103a) OSCAR INT2 KV-cache hot path.
+
+The functions below carry the C ABI's names (include/oscar.h) and only marshal arguments: torch
+tensors provide device memory and streams, every computation runs in the library's CUDA kernels.
+If liboscar.so has not been built the first call raises; there is no fallback implementation.
+
+Three-segment pool "BF16 sink (64 tokens) | INT2 history | BF16 recent (256 tokens)", rotation
+R = U · Hadamard · bit-reversal, 4 two-bit codes per byte ("超越TurboQuant！OSCAR：面向真实服务的2-bit
+KV Cache量化", section "OSCAR 的设计").
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import torch
+
+from . import _lib
+from ._lib import OscarError
+
+HEAD_DIM, PAGE, SINK, RECENT = 128, 64, 64, 256
+ROT_HAAR, ROT_COVARIANCE = 0, 1
+DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS = 1, 2, 4
+
+__all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
+           "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_demote", "oscar_append_kv",
+           "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events", "lib"]
+PROFILE_HISTORY, PROFILE_DEMOTE = 0, 1
+
+
+def lib() -> C.CDLL:
+    return _lib.load()
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    if stream is None:
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev(t, dtype, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def oscar_version() -> str:
+    return lib().oscar_version().decode()
+
+
+def oscar_make_rotation(M: torch.Tensor, mode: int, stream=None):
+    """R = U·H·P from a d x d fp64 device matrix M (Gaussian draws for ROT_HAAR, covariance for
+    ROT_COVARIANCE).  Returns (R64 fp64, R32 fp32).  Synchronous."""
+    _dev(M, torch.float64, "M")
+    d = M.shape[0]
+    R64 = torch.empty((d, d), dtype=torch.float64, device=M.device)
+    R32 = torch.empty((d, d), dtype=torch.float32, device=M.device)
+    ws = torch.empty(lib().oscar_make_rotation_workspace_size(d), dtype=torch.uint8, device=M.device)
+    _lib.check(lib().oscar_make_rotation(d, mode, _p(M), _p(R64), _p(R32), _p(ws), ws.numel(), _s(stream)),
+               "oscar_make_rotation")
+    return R64, R32
+
+
+def oscar_calib_covariance_k(Q: torch.Tensor, stream=None) -> torch.Tensor:
+    """C = sum_h Q_h^T Q_h for bf16 Q [T][heads][d]; fp64 [d][d]."""
+    _dev(Q, torch.bfloat16, "Q")
+    T, H, d = Q.shape
+    C_ = torch.empty((d, d), dtype=torch.float64, device=Q.device)
+    _lib.check(lib().oscar_calib_covariance_k(T, H, d, _p(Q), _p(C_), _s(stream)), "oscar_calib_covariance_k")
+    return C_
+
+
+def oscar_calib_covariance_v(Q, K, V, softmax_scale=None, stream=None) -> torch.Tensor:
+    """C = sum_h (S_h V)^T (S_h V), S_h = causal softmax(Q_h K^T * scale); Q [T][heads][d], K, V [T][d] bf16."""
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _dev(t, torch.bfloat16, n)
+    T, H, d = Q.shape
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    C_ = torch.empty((d, d), dtype=torch.float64, device=Q.device)
+    ws = torch.empty(lib().oscar_calib_covariance_v_workspace_size(T, H, d), dtype=torch.uint8, device=Q.device)
+    _lib.check(lib().oscar_calib_covariance_v(T, H, d, _p(Q), _p(K), _p(V), scale, _p(C_), _p(ws), ws.numel(),
+                                              _s(stream)), "oscar_calib_covariance_v")
+    return C_
+
+
+def oscar_quantize_kv(x, R32, clip, group_size, codes=None, scale=None, zero=None, stats=None, stream=None):
+    """Bulk rotate/clip/quantize/pack: x bf16 [N][Hkv][128] -> (codes u8 [N][Hkv][32], scale, zero bf16 [N][Hkv][ng])."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(R32, torch.float32, "R32")
+    _dev(clip, torch.float32, "clip")
+    N, Hkv, d = x.shape
+    ng = d // group_size
+    codes = torch.empty((N, Hkv, d // 4), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scale = torch.empty((N, Hkv, ng), dtype=torch.bfloat16, device=x.device) if scale is None else scale
+    zero = torch.empty((N, Hkv, ng), dtype=torch.bfloat16, device=x.device) if zero is None else zero
+    _lib.check(lib().oscar_quantize_kv(N, Hkv, d, group_size, _p(x), _p(R32), _p(clip), _p(codes), _p(scale),
+                                       _p(zero), _p(stats), _s(stream)), "oscar_quantize_kv")
+    return codes, scale, zero
+
+
+class Pool:
+    """Device storage of one layer's three-segment pool plus its C struct (see include/oscar.h)."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, group_size, num_pages, max_pages, R_k, R_v, clip_k, clip_v,
+                 device="cuda", head_dim=HEAD_DIM):
+        dev = torch.device(device)
+        self.B, self.Hq, self.Hkv, self.d, self.g = batch, num_q_heads, num_kv_heads, head_dim, group_size
+        self.ng = head_dim // group_size
+        self.num_pages, self.max_pages = num_pages, max_pages
+        bf = torch.bfloat16
+        z = lambda *shape, dt: torch.zeros(shape, dtype=dt, device=dev)
+        self.sink_k, self.sink_v = z(batch, num_kv_heads, SINK, head_dim, dt=bf), z(batch, num_kv_heads, SINK, head_dim, dt=bf)
+        self.recent_k = z(batch, num_kv_heads, RECENT, head_dim, dt=bf)
+        self.recent_v = z(batch, num_kv_heads, RECENT, head_dim, dt=bf)
+        self.codes_k = z(num_pages, num_kv_heads, PAGE, head_dim // 4, dt=torch.uint8)
+        self.codes_v = z(num_pages, num_kv_heads, PAGE, head_dim // 4, dt=torch.uint8)
+        self.scale_k, self.zero_k = z(num_pages, num_kv_heads, PAGE, self.ng, dt=bf), z(num_pages, num_kv_heads, PAGE, self.ng, dt=bf)
+        self.scale_v, self.zero_v = z(num_pages, num_kv_heads, PAGE, self.ng, dt=bf), z(num_pages, num_kv_heads, PAGE, self.ng, dt=bf)
+        self.page_table = torch.full((batch, max(max_pages, 1)), -1, dtype=torch.int32, device=dev)
+        self.sink_len, self.hist_len = z(batch, dt=torch.int32), z(batch, dt=torch.int32)
+        self.recent_start, self.recent_len = z(batch, dt=torch.int32), z(batch, dt=torch.int32)
+        self.R_k = _dev(R_k.to(dev, torch.float32).contiguous(), torch.float32, "R_k")
+        self.R_v = _dev(R_v.to(dev, torch.float32).contiguous(), torch.float32, "R_v")
+        self.clip_k = clip_k.to(dev, torch.float32).contiguous()
+        self.clip_v = clip_v.to(dev, torch.float32).contiguous()
+        self.err_word = z(1, dt=torch.int32)
+        self.sync = z(batch, dt=torch.int32)
+        self.struct = _lib.oscar_pool(
+            batch, num_q_heads, num_kv_heads, head_dim, group_size, num_pages, max_pages,
+            *(t.data_ptr() for t in (self.sink_k, self.sink_v, self.recent_k, self.recent_v, self.codes_k,
+                                     self.codes_v, self.scale_k, self.zero_k, self.scale_v, self.zero_v,
+                                     self.page_table, self.sink_len, self.hist_len, self.recent_start,
+                                     self.recent_len, self.R_k, self.R_v, self.clip_k, self.clip_v, self.err_word,
+                                     self.sync)))
+
+    @property
+    def ref(self):
+        return C.byref(self.struct)
+
+    def set_page_table(self, pt):
+        self.page_table.copy_(torch.as_tensor(pt, dtype=torch.int32).reshape(self.page_table.shape))
+
+    def err(self) -> int:
+        return int(self.err_word.item()) & 0xffffffff
+
+    def counters(self):
+        return {k: getattr(self, k).cpu().numpy().copy() for k in ("sink_len", "hist_len", "recent_start", "recent_len")}
+
+
+def oscar_prefill_pool(pool: Pool, seq: int, k, v, stats=None, stream=None):
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v")
+    _lib.check(lib().oscar_prefill_pool(pool.ref, seq, k.shape[0], _p(k), _p(v), _p(stats), _s(stream)),
+               "oscar_prefill_pool")
+
+
+def oscar_demote(pool: Pool, mask=None, stream=None):
+    if mask is not None:
+        _dev(mask, torch.int32, "mask")
+    _lib.check(lib().oscar_demote(pool.ref, _p(mask), _s(stream)), "oscar_demote")
+
+
+def oscar_append_kv(pool: Pool, k_new, v_new, stream=None):
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _lib.check(lib().oscar_append_kv(pool.ref, _p(k_new), _p(v_new), _s(stream)), "oscar_append_kv")
+
+
+def oscar_decode_workspace_size(pool: Pool, num_splits: int = 0) -> int:
+    n = C.c_size_t(0)
+    _lib.check(lib().oscar_decode_workspace_size(pool.ref, num_splits, C.byref(n)), "oscar_decode_workspace_size")
+    return n.value
+
+
+def oscar_decode_attention(pool: Pool, q, out=None, softmax_scale=None, num_splits=0, ws=None, stream=None):
+    """fp32 out [B][Hq][128] of bf16 q [B][Hq][128] over the pool."""
+    _dev(q, torch.bfloat16, "q")
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    if ws is None:
+        ws = torch.empty(oscar_decode_workspace_size(pool, num_splits), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(pool.d) if softmax_scale is None else float(softmax_scale)
+    _lib.check(lib().oscar_decode_attention(pool.ref, _p(q), _p(out), scale, num_splits, _p(ws), ws.numel(),
+                                            _s(stream)), "oscar_decode_attention")
+    return out
+
+
+def oscar_profile_events(which: int, start=None, stop=None):
+    """Arm the timing hook: the next launch of kernel kind `which` on this thread records torch.cuda.Event
+    `start` before and `stop` after that kernel (on the call's stream)."""
+    sp = None if start is None else C.c_void_p(start.cuda_event)
+    ep = None if stop is None else C.c_void_p(stop.cuda_event)
+    _lib.check(lib().oscar_profile_events(which, sp, ep), "oscar_profile_events")

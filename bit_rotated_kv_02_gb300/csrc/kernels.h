@@ -1,0 +1,51 @@
+// Launchers shared between the API layer and the kernel translation units (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "oscar_internal.cuh"
+
+namespace oscar {
+
+// Per-thread profiling events armed by oscar_profile_events (api.cu); launchers record them around the
+// kernel of the matching kind and disarm.
+struct ProfileSlot {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+ProfileSlot &profile_slot(int which);
+inline void profile_begin(int which, cudaStream_t s) {
+  ProfileSlot &p = profile_slot(which);
+  if (p.start) cudaEventRecord(p.start, s);
+}
+inline void profile_end(int which, cudaStream_t s) {
+  ProfileSlot &p = profile_slot(which);
+  if (p.stop) cudaEventRecord(p.stop, s);
+  p.start = p.stop = nullptr;
+}
+
+// quantize.cu
+cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
+                          const uint16_t *v_new, cudaStream_t s);
+cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride, const float *R32,
+                                 const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
+                                 const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s);
+cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
+                           cudaStream_t s);
+
+// decode.cu
+constexpr int PART_STRIDE = D + 4;  // one partial: o[128], m, l, pad
+size_t decode_ws_bytes(const PoolArgs &p, int splits);
+cudaError_t launch_decode(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, int splits, float *ws,
+                          cudaStream_t s);
+
+// rotation.cu
+size_t rotation_ws_bytes(int d);
+cudaError_t launch_make_rotation(int d, int mode, const double *M, double *R64, float *R32, void *ws,
+                                 cudaStream_t s);
+cudaError_t launch_cov_k(int64_t T, int heads, int d, const uint16_t *Q, double *C, cudaStream_t s);
+size_t cov_v_ws_bytes(int64_t T, int d);
+cudaError_t launch_cov_v(int64_t T, int heads, int d, const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                         double scale, double *C, void *ws, cudaStream_t s);
+
+}  // namespace oscar

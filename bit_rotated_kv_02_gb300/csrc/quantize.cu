@@ -1,0 +1,211 @@
+// Demotion, append and prefill kernels of the three-segment pool.
+//
+// "超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化", section "OSCAR 的设计": a new token is
+// first written into the recent window; as decoding advances the oldest recent token is rotated,
+// clipped, quantized and packed by a fused kernel and demoted into the INT2 history; sink and
+// recent stay BF16.
+#include "oscar_internal.cuh"
+#include "kernels.h"
+
+namespace oscar {
+
+// ---------------------------------------------------------------------------------------------
+// Demote (and optionally append): grid (Hkv, B), 64 threads.  Warp 0 handles K, warp 1 handles V
+// of KV head blockIdx.x of sequence blockIdx.y.  Every CTA reads the sequence's counters before
+// any CTA of that sequence can change them: the last CTA to arrive (arrival counter pool.sync[b])
+// updates the counters and returns the arrival counter to zero.
+// mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
+// mode 2: as mode 0, then append k_new/v_new.
+__global__ void __launch_bounds__(64) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
+                                                           const uint16_t *k_new, const uint16_t *v_new) {
+  __shared__ float xs[2][D];
+  __shared__ int s_ok;
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
+  const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
+  bool demote = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
+  int page = -1;
+  if (demote) {
+    const int pidx = hl / PAGE;
+    if (pidx >= p.max_pages) {
+      demote = false;
+      if (threadIdx.x == 0) atomicOr(p.err, OSCAR_DEVERR_HISTORY_FULL);
+    } else {
+      page = p.page_table[(size_t)b * p.max_pages + pidx];
+      if (page < 0 || page >= p.num_pages) {
+        demote = false;
+        if (threadIdx.x == 0) atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
+      }
+    }
+  }
+  if (!counters_ok && threadIdx.x == 0) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
+  // A demotion that cannot be stored leaves the whole sequence unchanged (no append either).
+  const bool blocked = counters_ok && !demote && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
+  if (demote) {
+    const uint16_t *src = (warp == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D;
+    load_vec_to_smem(src, xs[warp]);
+    const float *R = (warp == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
+    const float clip = (warp == 0 ? p.clip_k : p.clip_v)[kvh];
+    const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
+    QuantStats st{0, 0, 0};
+    rotate_quantize_warp(xs[warp], R, clip, p.g, (warp == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
+                         (warp == 0 ? p.scale_k : p.scale_v) + row * p.ng,
+                         (warp == 0 ? p.zero_k : p.zero_v) + row * p.ng, st);
+  }
+  __syncthreads();  // the demoted slot is read before the append may overwrite it
+  const bool append = mode == 2 && counters_ok && !blocked;
+  int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
+  if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
+  if (append) {
+    uint16_t *dk, *dv;
+    if (nslen < SINK && nhl == 0 && nrl == 0) {
+      const size_t o = (((size_t)b * p.Hkv + kvh) * SINK + nslen) * D;
+      dk = p.sink_k + o; dv = p.sink_v + o;
+      nslen += 1;
+    } else {
+      const size_t o = (((size_t)b * p.Hkv + kvh) * RECENT + (nrs + nrl) % RECENT) * D;
+      dk = p.recent_k + o; dv = p.recent_v + o;
+      nrl += 1;
+    }
+    const size_t so = ((size_t)b * p.Hkv + kvh) * D;
+    if (warp == 0) reinterpret_cast<uint2 *>(dk)[lane] = reinterpret_cast<const uint2 *>(k_new + so)[lane];
+    else reinterpret_cast<uint2 *>(dv)[lane] = reinterpret_cast<const uint2 *>(v_new + so)[lane];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int arrived = atomicAdd(p.sync + b, 1);
+    s_ok = arrived == p.Hkv - 1;
+  }
+  __syncthreads();
+  if (s_ok && threadIdx.x == 0) {
+    __threadfence();
+    if (counters_ok && !blocked) {
+      p.sink_len[b] = nslen;
+      p.hist_len[b] = nhl;
+      p.recent_start[b] = nrs;
+      p.recent_len[b] = nrl;
+    }
+    p.sync[b] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Rotate/quantize rows of one KV head with R staged in shared memory.  grid (ceil(n/ROWS), Hkv),
+// 256 threads (8 warps), each warp loops over rows.  Output addressing: contiguous
+// [n][Hkv][...] (pt == nullptr) or paged through one page-table row (pt != nullptr, row t goes to
+// page pt[t/64], slot t%64).
+constexpr int QROWS = 64;
+
+__global__ void __launch_bounds__(256) quantize_rows_kernel(int64_t n, int Hkv, int g, const uint16_t *x,
+                                                           int64_t x_row_stride, const float *R32, const float *clip,
+                                                           uint8_t *codes, uint16_t *scale, uint16_t *zero,
+                                                           const int32_t *pt, int num_pages, uint32_t *err,
+                                                           uint32_t *stats) {
+  extern __shared__ float4 smem4[];
+  float *Rs = reinterpret_cast<float *>(smem4);
+  float *xs_all = Rs + D * D;
+  const int kvh = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const float *Rg = R32 + (size_t)kvh * D * D;
+  for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) smem4[i] = reinterpret_cast<const float4 *>(Rg)[i];
+  __syncthreads();
+  float *xs = xs_all + warp * D;
+  const float c = clip[kvh];
+  const int ng = D / g;
+  QuantStats st{0, 0, 0};
+  const int64_t r0 = (int64_t)blockIdx.x * QROWS;
+  for (int64_t r = r0 + warp; r < r0 + QROWS && r < n; r += 8) {
+    size_t orow;
+    if (pt == nullptr) {
+      orow = (size_t)r * Hkv + kvh;
+    } else {
+      const int page = pt[r / PAGE];
+      if (page < 0 || page >= num_pages) {
+        if ((threadIdx.x & 31) == 0) atomicOr(err, OSCAR_DEVERR_PAGE_INDEX);
+        continue;
+      }
+      orow = ((size_t)page * Hkv + kvh) * PAGE + (r % PAGE);
+    }
+    load_vec_to_smem(x + (size_t)r * x_row_stride + (size_t)kvh * D, xs);
+    rotate_quantize_warp(xs, Rs, c, g, codes + orow * (D / 4), scale + orow * ng, zero + orow * ng, st);
+    __syncwarp();
+  }
+  flush_stats(stats, st);
+}
+
+// Copy token rows [t0, t0+n) of x [L][Hkv][D] into dst [Hkv][cap][D] rows [0, n) of one sequence.
+__global__ void copy_rows_kernel(const uint16_t *x, int64_t t0, int n, int Hkv, uint16_t *dst, int cap) {
+  const int kvh = blockIdx.y;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n * (D / 8); i += gridDim.x * blockDim.x) {
+    const int t = i / (D / 8), c = i % (D / 8);
+    reinterpret_cast<uint4 *>(dst + ((size_t)kvh * cap + t) * D)[c] =
+        reinterpret_cast<const uint4 *>(x + ((size_t)(t0 + t) * Hkv + kvh) * D)[c];
+  }
+}
+
+__global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl) {
+  p.sink_len[b] = slen;
+  p.hist_len[b] = hl;
+  p.recent_start[b] = 0;
+  p.recent_len[b] = rl;
+}
+
+// ---- launchers ------------------------------------------------------------------------------
+cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
+                          const uint16_t *v_new, cudaStream_t s) {
+  profile_begin(OSCAR_PROFILE_DEMOTE, s);
+  demote_append_kernel<<<dim3(p.Hkv, p.B), 64, 0, s>>>(p, mask, mode, k_new, v_new);
+  profile_end(OSCAR_PROFILE_DEMOTE, s);
+  return cudaGetLastError();
+}
+
+static size_t quant_smem_bytes() { return (size_t)D * D * 4 + 8 * D * 4; }
+
+cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride, const float *R32,
+                                 const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
+                                 const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const size_t smem = quant_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(quantize_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)((n + QROWS - 1) / QROWS), Hkv);
+  quantize_rows_kernel<<<grid, 256, smem, s>>>(n, Hkv, g, x, x_row_stride, R32, clip, codes, scale, zero, pt,
+                                               num_pages, err, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
+                           cudaStream_t s) {
+  const int ns = (int)(L < SINK ? L : SINK);
+  const int64_t rest = L - ns;
+  const int nr = (int)(rest < RECENT ? rest : RECENT);
+  const int64_t nh = L - ns - nr;
+  const int64_t stride = (int64_t)p.Hkv * D;
+  cudaError_t e;
+  if (ns > 0) {
+    copy_rows_kernel<<<dim3(8, p.Hkv), 256, 0, s>>>(k, 0, ns, p.Hkv, p.sink_k + (size_t)b * p.Hkv * SINK * D, SINK);
+    copy_rows_kernel<<<dim3(8, p.Hkv), 256, 0, s>>>(v, 0, ns, p.Hkv, p.sink_v + (size_t)b * p.Hkv * SINK * D, SINK);
+  }
+  if (nr > 0) {
+    copy_rows_kernel<<<dim3(16, p.Hkv), 256, 0, s>>>(k, ns + nh, nr, p.Hkv,
+                                                     p.recent_k + (size_t)b * p.Hkv * RECENT * D, RECENT);
+    copy_rows_kernel<<<dim3(16, p.Hkv), 256, 0, s>>>(v, ns + nh, nr, p.Hkv,
+                                                     p.recent_v + (size_t)b * p.Hkv * RECENT * D, RECENT);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (nh > 0) {
+    const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
+    e = launch_quantize_rows(nh, p.Hkv, p.g, k + (size_t)ns * stride, stride, p.R_k, p.clip_k, p.codes_k, p.scale_k,
+                             p.zero_k, pt, p.num_pages, p.err, stats, s);
+    if (e != cudaSuccess) return e;
+    e = launch_quantize_rows(nh, p.Hkv, p.g, v + (size_t)ns * stride, stride, p.R_v, p.clip_v, p.codes_v, p.scale_v,
+                             p.zero_v, pt, p.num_pages, p.err, stats, s);
+    if (e != cudaSuccess) return e;
+  }
+  set_counters_kernel<<<1, 1, 0, s>>>(p, b, ns, (int)nh, nr);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

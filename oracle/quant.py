@@ -88,6 +88,22 @@ def rotate_exact(x_bits: np.ndarray, R32: np.ndarray) -> np.ndarray:
     return out
 
 
+def rotate_exact_many(x_bits: np.ndarray, R32: np.ndarray) -> np.ndarray:
+    """Same result as rotate_exact, for many rows: a float64 product y = x @ R32 has error at most
+    gamma_128 * (|x| @ |R32|) (gamma_n = n u / (1 - n u), u = 2^-53, any summation order); where the
+    interval y -/+ that bound rounds to one float32 at both ends, that float32 is the correctly rounded
+    value; every other element is recomputed by rotate_exact's fsum path."""
+    X = bf16_bits_to_f64(np.atleast_2d(x_bits))
+    R = np.asarray(R32, dtype=F32).astype(np.float64)
+    y = X @ R
+    bound = (np.abs(X) @ np.abs(R)) * (1.5e-14 * (1 + 1e-10)) + 1e-300
+    lo, hi = (y - bound).astype(F32), (y + bound).astype(F32)
+    out = hi.copy()
+    for r, j in zip(*np.nonzero(lo != hi)):
+        out[r, j] = round_sum_to_f32((X[r] * R[:, j]).tolist())
+    return out
+
+
 # ---- clip + asymmetric INT2 quantizer ------------------------------------
 
 def quantize_group(xh: np.ndarray, clip: float) -> tuple[np.ndarray, np.uint16, np.uint16]:
@@ -126,6 +142,32 @@ def quantize_rotated(xh: np.ndarray, clip: float, group: int):
             sl = slice(gi * group, (gi + 1) * group)
             codes[r, sl], scale[r, gi], zero[r, gi] = quantize_group(xh[r, sl], clip)
     return codes, scale, zero
+
+
+def quantize_rotated_many(xh: np.ndarray, clip: float, group: int):
+    """quantize_rotated with the same float32 operations applied to all groups at once."""
+    xh = np.atleast_2d(np.asarray(xh, F32))
+    n, d = xh.shape
+    ng = d // group
+    xg = xh.reshape(n, ng, group)
+    c = F32(clip)
+    mn, mx = xg.min(axis=2), xg.max(axis=2)
+    lo = (c * mn).astype(F32)
+    hi = (c * mx).astype(F32)
+    s32 = ((hi - lo).astype(F32) / F32(3.0)).astype(F32)
+    scale_bits, zero_bits = f32_to_bf16_bits(s32), f32_to_bf16_bits(lo)
+    scale, zero = bf16_bits_to_f32(scale_bits), bf16_bits_to_f32(zero_bits)
+    valid = (scale != 0) & np.isfinite(scale)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = ((xg - zero[:, :, None]).astype(F32) / scale[:, :, None]).astype(F32)
+        codes = np.clip(np.rint(t), 0, 3)
+    codes = np.where(valid[:, :, None], codes, 0).astype(np.uint8).reshape(n, d)
+    return codes, scale_bits.reshape(n, ng), zero_bits.reshape(n, ng)
+
+
+def quantize_vectors_many(x_bits: np.ndarray, R32: np.ndarray, clip: float, group: int):
+    codes, scale, zero = quantize_rotated_many(rotate_exact_many(x_bits, R32), clip, group)
+    return pack_codes(codes), scale, zero
 
 
 def pack_codes(codes: np.ndarray) -> np.ndarray:

@@ -1,0 +1,73 @@
+"""Shared test plumbing: numpy <-> torch bf16 bit conversion, pool construction for both sides,
+and the parity checks the tests apply (bit-exact bytes; attention within the stated tolerance)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import pool as opool
+from oracle import quant as oquant
+from oracle import rotation as orot
+import synth
+
+# Attention tolerance: max-abs 2e-3 and relative-L2 1e-3 against the float64 oracle.
+ATOL, RTOL_L2 = 2e-3, 1e-3
+
+
+def to_dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_rotations(seed: int, Hkv: int, d: int = 128):
+    """Per-head float32 rotations R32 = fp32(U·H·P) with Haar U, from the oracle (kernel test inputs)."""
+    return np.stack([orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(seed + h, d))) for h in range(Hkv)])
+
+
+def make_pools(B, Hq, Hkv, g, pages_per_seq, seed, clip_k=None, clip_v=None, extra_pages=0):
+    """(oracle Pool, device Pool) with identical rotations, clips and shuffled page tables."""
+    import bit_rotated_kv_02_gb300 as ok
+    Rk = oracle_rotations(seed, Hkv)
+    Rv = oracle_rotations(seed + 1000, Hkv)
+    clip_k = np.full(Hkv, 0.9, np.float32) if clip_k is None else np.asarray(clip_k, np.float32)
+    clip_v = np.full(Hkv, 0.9, np.float32) if clip_v is None else np.asarray(clip_v, np.float32)
+    max_pages = max(max(pages_per_seq) + extra_pages, 1)
+    pt, num_pages = synth.page_tables(seed, [p + extra_pages for p in pages_per_seq], max_pages)
+    O = opool.Pool(B, Hq, Hkv, 128, g, num_pages, max_pages, Rk, Rv, clip_k, clip_v)
+    O.page_table[:] = pt
+    P = ok.Pool(B, Hq, Hkv, g, num_pages, max_pages, torch.from_numpy(Rk), torch.from_numpy(Rv),
+                torch.from_numpy(clip_k), torch.from_numpy(clip_v))
+    P.set_page_table(pt)
+    return O, P
+
+
+POOL_ARRAYS = ("sink_k", "sink_v", "recent_k", "recent_v", "codes_k", "codes_v", "scale_k", "zero_k", "scale_v",
+               "zero_v")
+
+
+def device_array(P, name):
+    t = getattr(P, name)
+    return bits_of(t) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def assert_pools_equal(O, P, heads=None):
+    for name in POOL_ARRAYS:
+        a, b = getattr(O, name), device_array(P, name)
+        if heads is not None and name.startswith(("codes", "scale", "zero")):
+            a, b = a[:, heads], b[:, heads]
+        assert np.array_equal(a, b), f"pool array {name} differs ({np.count_nonzero(a != b)} entries)"
+    for name in ("sink_len", "hist_len", "recent_start", "recent_len"):
+        assert np.array_equal(getattr(O, name), getattr(P, name).cpu().numpy()), name
+
+
+def assert_attention_close(got: np.ndarray, ref: np.ndarray):
+    got = np.asarray(got, np.float64)
+    err = np.abs(got - ref)
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert np.isfinite(got).all(), "non-finite attention output"
+    assert err.max() <= ATOL, f"max-abs error {err.max():.3e} > {ATOL}"
+    assert rel <= RTOL_L2, f"relative L2 error {rel:.3e} > {RTOL_L2}"
+    return err.max(), rel

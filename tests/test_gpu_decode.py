@@ -1,0 +1,101 @@
+"""GPU parity: decode attention over the three-segment pool against the float64 oracle.
+
+INT2 history unpacked and dequantized with scale/zero point, BF16 sink/recent, online softmax merge
+("超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化", section "OSCAR 的设计"; "OSCAR: Offline
+Spectral Covariance-Aware Rotation for 2-bit KV Cache Quantization", Abstract).
+Bar: max-abs error <= 2e-3 and relative L2 error <= 1e-3 against exact float64 attention over the
+oracle's own pool (whose bytes must first equal the GPU pool's).
+"""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import bit_rotated_kv_02_gb300 as ok
+import synth
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+
+
+def _setup(lens, Hq, Hkv, g, seed, clip=None, heads=None, check_pool=True):
+    B = len(lens)
+    pages = [max(0, -(-(L - 320) // 64)) for L in lens]
+    clip_k, clip_v = (None, None) if clip is None else clip
+    O, P = helpers.make_pools(B, Hq, Hkv, g, pages, seed, clip_k, clip_v)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for b, L in enumerate(lens):
+        K = synth.outlier_kv(seed + 10 + b, L, Hkv, 128, ch)
+        V = synth.outlier_kv(seed + 500 + b, L, Hkv, 128, ch)
+        O.prefill(b, K, V, heads=heads)
+        ok.oscar_prefill_pool(P, b, helpers.to_dev_bf16(K), helpers.to_dev_bf16(V))
+    q = synth.outlier_q(seed + 7, B, Hq, Hkv, 128, ch)
+    torch.cuda.synchronize()
+    if check_pool:
+        helpers.assert_pools_equal(O, P, heads=heads)
+    return O, P, q
+
+
+def test_tiny_workload():
+    """Batch 1, 8 query / 2 KV heads, context 1024 = 64 sink + 704 history + 256 recent, group 128, clip 0.9."""
+    wl = synth.TINY
+    O, P, q = _setup(list(wl.context), wl.num_q_heads, wl.num_kv_heads, wl.group_size, wl.seed)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+    assert P.err() == 0
+
+
+def test_edge_lengths():
+    lens = [1, 40, 64, 65, 300, 320, 321, 384, 385, 449, 2000]
+    O, P, q = _setup(lens, 8, 2, 128, 300)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+
+
+@pytest.mark.parametrize("G,g", [(1, 32), (2, 64), (8, 32), (4, 64)])
+def test_gqa_ratios_and_group_sizes(G, g):
+    Hkv = 2
+    clip = (np.array([0.8, 0.95], np.float32), np.array([0.9, 0.85], np.float32))
+    O, P, q = _setup([900, 1500], G * Hkv, Hkv, g, 400 + G * 10 + g, clip=clip)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 64, 0])
+def test_split_counts(splits):
+    O, P, q = _setup([3000, 700], 8, 2, 128, 500)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q), num_splits=splits)
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+
+
+def test_decode_after_appends():
+    seed, Hkv, Hq = 600, 2, 8
+    O, P, q = _setup([340, 1000], Hq, Hkv, 128, seed)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for t in range(70):
+        kn = synth.outlier_kv(seed + 2000 + t, 2, Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, 2, Hkv, 128, ch)
+        O.append(kn, vn)
+        ok.oscar_append_kv(P, helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn))
+        if t % 23 == 0:
+            out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+            helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+    torch.cuda.synchronize()
+    helpers.assert_pools_equal(O, P)
+
+
+def test_100k_context_sampled_heads():
+    """Qwen3-8B layer shapes at 100k context: 99,680 history tokens on a shuffled page table (partial
+    last page); the oracle rebuilds KV heads 0 and 5 and checks their 8 query heads."""
+    wl = synth.DECODE_100K
+    heads = [0, 5]
+    O, P, q = _setup(list(wl.context), wl.num_q_heads, wl.num_kv_heads, wl.group_size, wl.seed, heads=heads)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q)).cpu().numpy()
+    qh = [h for kv in heads for h in range(kv * wl.group, (kv + 1) * wl.group)]
+    ref = O.decode(q, heads=qh)
+    helpers.assert_attention_close(out[:, qh], ref[:, qh])

@@ -136,3 +136,34 @@ def test_dequantize_closed_form():
     s = quant.f32_to_bf16_bits(np.array([[0.5]], F32))
     z = quant.f32_to_bf16_bits(np.array([[-1.0]], F32))
     assert np.array_equal(quant.dequantize(packed, s, z, 128)[0], np.array([-1.0, -0.5, 0.0, 0.5] * 32))
+
+
+@pytest.mark.parametrize("group", [32, 128])
+def test_many_row_paths_equal_plain_paths(group):
+    g = np.random.default_rng(9)
+    d = 128
+    R32 = rot.to_f32(rot.rotation_from_gaussian(synth.gaussian_matrix(9, d)))
+    ch = synth.outlier_channels(9, 1, d, 4)
+    xb = synth.outlier_kv(9, 40, 1, d, ch)[:, 0]
+    assert np.array_equal(quant.rotate_exact_many(xb, R32), quant.rotate_exact(xb, R32))
+    xh = quant.rotate_exact(xb, R32)
+    a = quant.quantize_rotated(xh, 0.9, group)
+    b = quant.quantize_rotated_many(xh, 0.9, group)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+    # degenerate groups (constant) agree too
+    const = np.full((3, d), 1.5, np.float32)
+    for u, v in zip(quant.quantize_rotated(const, 0.9, group), quant.quantize_rotated_many(const, 0.9, group)):
+        assert np.array_equal(u, v)
+
+
+def test_rotate_many_resolves_midpoints_exactly():
+    # y = 1 + 2^-24 (an exact float32 midpoint) plus/minus tiny residuals: the bound interval
+    # straddles the midpoint, so the exact path must decide.
+    R = np.zeros((128, 128), np.float32)
+    R[0, 0], R[1, 0], R[2, 0] = 1.0, 2.0 ** -24, 2.0 ** -60
+    for third, want in ((1.0, F32(1.0 + 2.0 ** -23)), (-1.0, F32(1.0)), (0.0, F32(1.0))):
+        x = np.zeros((1, 128), np.float32)
+        x[0, :3] = [1.0, 1.0, third]
+        xb = synth.to_bf16_bits(x)
+        assert quant.rotate_exact_many(xb, R)[0, 0] == want == quant.rotate_exact(xb, R)[0, 0]
