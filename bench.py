@@ -277,6 +277,10 @@ def main():
     if world > 1:
         dist.barrier()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for e4 in evs:              # torch creates the CUDA event on first record; create them all now
+        for e in e4:
+            e.record()
+    torch.cuda.synchronize()
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or "0"
     clocks = ClockSampler(gpu_index)
     time.sleep(0.3)

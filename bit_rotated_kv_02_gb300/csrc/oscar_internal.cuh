@@ -62,6 +62,44 @@ __device__ __forceinline__ void two_sum(double a, double b, double &s, double &e
   e = (a - (s - bp)) + (b - bp);
 }
 
+// Exact sign of (sum_i xs[i] * R[i][j]) - m, by fixed-point integer arithmetic: every product of a
+// float32-held bf16 and a float32 is an integer (< 2^48) times a power of two, and m (a float32
+// midpoint held in a double) is an integer < 2^53 times a power of two; all are aligned to the
+// smallest exponent and summed in 128-bit integers.  Returns -1, 0 or +1, or 2 when the exponent
+// span does not fit in 128 bits.  Runs serially on the calling lane (used only for exact ties).
+__device__ inline int exact_sign_minus(const float *xs, const float *R, int j, double m) {
+  int emin = 0x7fffffff, etop = -0x7fffffff;
+  for (int i = 0; i < D; ++i) {
+    const float x = xs[i], r = R[i * D + j];
+    if (x == 0.0f || r == 0.0f) continue;
+    int ex, er;
+    frexpf(x, &ex);
+    frexpf(r, &er);
+    const int e = ex + er - 48;            // product = (mx * mr) * 2^e with |mx|, |mr| < 2^24
+    emin = min(emin, e);
+    etop = max(etop, e + 48);
+  }
+  int em = 0;
+  if (m != 0.0) {
+    frexp(m, &em);
+    emin = min(emin, em - 53);
+    etop = max(etop, em);
+  }
+  if (emin == 0x7fffffff) return 0;        // every term is zero and m == 0
+  if (etop - emin > 118) return 2;         // 7 bits of headroom for 128 terms + sign
+  __int128 acc = 0;
+  for (int i = 0; i < D; ++i) {
+    const float x = xs[i], r = R[i * D + j];
+    if (x == 0.0f || r == 0.0f) continue;
+    int ex, er;
+    const long long mx = (long long)ldexpf(frexpf(x, &ex), 24);
+    const long long mr = (long long)ldexpf(frexpf(r, &er), 24);
+    acc += (__int128)(mx * mr) << (ex + er - 48 - emin);
+  }
+  if (m != 0.0) acc -= (__int128)(long long)ldexp(frexp(m, &em), 53) << (em - 53 - emin);
+  return acc > 0 ? 1 : (acc < 0 ? -1 : 0);
+}
+
 __device__ inline float exact_rot_elem(const float *xs, const float *R, int j, bool &unproven) {
   const int lane = threadIdx.x & 31;
   double s = 0.0, c = 0.0, sa = 0.0;
@@ -91,8 +129,16 @@ __device__ inline float exact_rot_elem(const float *xs, const float *R, int j, b
   const float rd = __double2float_rd(hi), ru = __double2float_ru(hi);
   if (rd == ru) return rd;                       // hi is a float32: |lo| < ulp64(hi)/2 cannot move it
   const double mid = 0.5 * ((double)rd + (double)ru);
-  const double dist = (hi - mid) + lo;           // hi - mid is exact (Sterbenz)
-  if (fabs(dist) <= 1e-27 * sa) unproven = true;
+  double dist = (hi - mid) + lo;                 // hi - mid is exact (Sterbenz)
+  if (fabs(dist) <= 1e-27 * sa) {
+    // Within the double-double's error bound of the midpoint (in practice an exact tie, which
+    // bf16 x float32 products make possible): decide with exact integer arithmetic.
+    int sg = 0;
+    if ((threadIdx.x & 31) == 0) sg = exact_sign_minus(xs, R, j, mid);
+    sg = __shfl_sync(FULL, sg, 0);
+    if (sg == 2) unproven = true;
+    else dist = (double)sg;
+  }
   if (dist > 0.0) return ru;
   if (dist < 0.0) return rd;
   return __double2float_rn(hi);                  // exact tie: to even

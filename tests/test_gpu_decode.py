@@ -23,11 +23,11 @@ def _built():
     __graft_entry__.build()
 
 
-def _setup(lens, Hq, Hkv, g, seed, clip=None, heads=None, check_pool=True):
+def _setup(lens, Hq, Hkv, g, seed, clip=None, heads=None, check_pool=True, extra_pages=0):
     B = len(lens)
     pages = [max(0, -(-(L - 320) // 64)) for L in lens]
     clip_k, clip_v = (None, None) if clip is None else clip
-    O, P = helpers.make_pools(B, Hq, Hkv, g, pages, seed, clip_k, clip_v)
+    O, P = helpers.make_pools(B, Hq, Hkv, g, pages, seed, clip_k, clip_v, extra_pages=extra_pages)
     ch = synth.outlier_channels(seed, Hkv, 128, 4)
     for b, L in enumerate(lens):
         K = synth.outlier_kv(seed + 10 + b, L, Hkv, 128, ch)
@@ -75,7 +75,7 @@ def test_split_counts(splits):
 
 def test_decode_after_appends():
     seed, Hkv, Hq = 600, 2, 8
-    O, P, q = _setup([340, 1000], Hq, Hkv, 128, seed)
+    O, P, q = _setup([340, 1000], Hq, Hkv, 128, seed, extra_pages=2)
     ch = synth.outlier_channels(seed, Hkv, 128, 4)
     for t in range(70):
         kn = synth.outlier_kv(seed + 2000 + t, 2, Hkv, 128, ch)

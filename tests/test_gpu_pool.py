@@ -72,7 +72,7 @@ def test_append_from_empty_fills_sink_then_recent_then_history():
     torch.cuda.synchronize()
     helpers.assert_pools_equal(O, P)
     c = P.counters()
-    assert (c["sink_len"][0], c["hist_len"][0], c["recent_len"][0]) == (64, 69, 256)
+    assert (c["sink_len"][0], c["hist_len"][0], c["recent_len"][0]) == (64, 70, 256)
 
 
 def test_masked_demote():
