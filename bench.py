@@ -139,7 +139,7 @@ class ClockSampler:
 def traffic_from_profiles(kernel_src: str):
     """DRAM bytes per launch of the history kernel from the committed ncu summary, if the kernel's
     source has not changed since that capture (else None)."""
-    path = os.path.join(ROOT, "profiles", "hist_partial_decode100k.md")
+    path = os.path.join(ROOT, "profiles", "attn_kernel_decode100k.md")
     if not os.path.exists(path):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
@@ -335,8 +335,9 @@ def main():
     # algorithmic bytes of the history kernel per launch (codes + scale/zero + page table + q)
     hist_tokens_avg = (tokens / args.steps) - SINK - RECENT
     hist_bytes = hist_tokens_avg * HKV * 2 * (D // 4 + 4 * (D // GROUP)) + 4 * math.ceil(hist_tokens_avg / PAGE) \
-        + HQ * D * 2
-    bf16_bytes = (SINK + RECENT) * HKV * 2 * D * 2
+        + HQ * D * 4
+    bf16_bytes = (SINK + RECENT) * HKV * 2 * D * 2 + HQ * D * 2
+    attn_bytes = hist_bytes + bf16_bytes      # the attention launch serves both history and BF16 CTAs
     step_bytes = hist_bytes + bf16_bytes + HQ * D * 4 + HKV * 2 * D * 2 * 3 + HKV * 2 * (D // 4 + 4)
     hist_mean_ms = statistics.mean(hist_ms)
     peaks = {}
@@ -347,7 +348,7 @@ def main():
     peak = peaks.get("hbm_gbs")
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
-    achieved = hist_bytes / (hist_mean_ms * 1e-3) / 1e9
+    achieved = attn_bytes / (hist_mean_ms * 1e-3) / 1e9
     value = world * tokens / (ms * 1e-3)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -364,17 +365,18 @@ def main():
             "decode_steps_per_s": world * args.steps / (ms * 1e-3),
             "bytes_per_step": step_bytes,
             "step_gbs": step_bytes * args.steps / (ms * 1e-3) / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "hist_partial_kernel", "achieved": achieved, "peak": peak,
+            "roofline": {"bound": "hbm", "kernel": "attn_kernel (INT2 history + BF16 sink/recent CTAs)",
+                         "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic_from_profiles(os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc",
                                                                        "decode.cu")),
-                         "algorithmic_bytes_per_launch": hist_bytes, "mean_launch_us": hist_mean_ms * 1e3},
+                         "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3},
             "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
                        statistics.mean(dem_ms) * 1e3, "note": "append+demote kernel, 1 token x 8 KV heads x K/V per launch"},
             "e2e": {"value": world * e2e_tokens / (e2e_ms * 1e-3), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 4,
+            "gpu_launches": args.steps * 4,   # append/demote, q rotation, attention, merge
             "clocks": clk,
             "cpu_baseline": cpu,
         }

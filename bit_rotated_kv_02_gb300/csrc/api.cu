@@ -211,8 +211,12 @@ oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_s
   if (st != OSCAR_OK) return st;
   if (bytes == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "bytes is NULL");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
-  const int s = num_splits == 0 ? auto_splits(a) : num_splits;
-  *bytes = decode_ws_bytes(a, s);
+  if (a.g == OSCAR_HEAD_DIM) {
+    *bytes = v1_ws_bytes(a);
+  } else {
+    const int s = num_splits == 0 ? auto_splits(a) : num_splits;
+    *bytes = decode_ws_bytes(a, s);
+  }
   return OSCAR_OK;
 }
 
@@ -224,6 +228,13 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
+  if (a.g == OSCAR_HEAD_DIM) {
+    const size_t need = v1_ws_bytes(a);
+    if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+    if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
+    return cuda_status(launch_decode_v1(a, q, out, softmax_scale, static_cast<float *>(ws), static_cast<cudaStream_t>(stream)),
+                       "decode_attention");
+  }
   const int s = num_splits == 0 ? auto_splits(a) : num_splits;
   const size_t need = decode_ws_bytes(a, s);
   if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);

@@ -1,0 +1,872 @@
+// Decode attention over the three-segment pool, tensor-core version (group size 128).
+//
+// "超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化", section "OSCAR 的设计": the INT2 kernel
+// unpacks the 2-bit codes, dequantizes with scale/zero point and accumulates in floating point; a
+// BF16 kernel handles the sink and recent window; an online-softmax merge combines the results.
+// "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache Quantization", Abstract: a
+// custom INT2 attention kernel compatible with paged KV-cache serving.
+//
+// Three launches:
+//   qrot_kernel   q_rot = q · R_k for every query head (row-vector convention), fp32.
+//   attn_kernel   BF16 CTAs (first block indices): 64 sink or recent tokens each, plain FMA, one
+//                 partial per chunk.  History CTAs: the flattened (sequence, KV head, page) space is
+//                 cut into equal contiguous ranges, one per CTA; a producer warp streams up to two
+//                 pages of one segment per ring stage (codes and scale/zero rows) into shared memory
+//                 with 1-D bulk async copies; four consumer warps each score one 16-token tile of
+//                 every page of the stage with warp MMAs (m16n8k16, f16 inputs, f32 accumulate) and
+//                 accumulate P·V the same way, with a lazily rescaled online softmax; one
+//                 (m, l, o_rot) partial per head is written per (CTA, segment).
+//   merge_kernel  LSE-combines a segment's partials, un-rotates the history part (o · R_v^T),
+//                 adds the BF16 part and normalises.
+//
+// Exactness of the tensor-core arithmetic: a 2-bit code c placed in the low mantissa bits of an
+// fp16 with a zero exponent field is the subnormal c * 4^k * 2^-24 (k = its bit position / 2), so
+// codes enter the MMA exactly with one AND per two codes.  q_rot and the softmax weights are split
+// into two fp16 terms (hi + lo, 22 significant bits), pre-scaled by powers of two (including 4^-k)
+// so that fp16 holds them; scale and zero point are applied in fp32 outside the MMA:
+//   score = scale * sum_c code_c q_c + zero * sum_c q_c,   o_rot = sum_t p_t scale_t code_t + sum_t p_t zero_t.
+// Softmax values are kept in base 2 (scores pre-multiplied by log2 e), so partials carry log2 maxima.
+#include "oscar_internal.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace oscar {
+
+namespace v1 {
+
+constexpr int NSTAGE = 4;
+constexpr int PAGE_BYTES = 4608;   // Kc 2048 | Vc 2048 | Ks 128 | Kz 128 | Vs 128 | Vz 128
+constexpr int STAGE_PAGES = 2;     // a stage holds up to two consecutive pages of one segment
+constexpr int STAGE_BYTES = PAGE_BYTES * STAGE_PAGES;
+constexpr int OFF_KC = 0, OFF_VC = 2048, OFF_KS = 4096, OFF_KZ = 4224, OFF_VS = 4352, OFF_VZ = 4480;
+constexpr int CONSUMER_WARPS = 4, THREADS = 160;
+constexpr int LAZY = 16;           // rescale the running output only when the max grows by > 2^16
+constexpr int WEXP = 14 - LAZY;    // weights p * scale * 2^tau < 2^14 with tau = WEXP - e, scale < 2^e
+
+struct Args {
+  PoolArgs p;
+  const float *qrot;   // [B][Hq][D]
+  const uint16_t *q;   // [B][Hq][D] bf16
+  float sm_log2;       // softmax_scale * log2(e)
+  int n_hist;          // history CTAs (block indices n_bf .. n_bf + n_hist - 1)
+  int n_bf;            // BF16 CTAs (block indices 0 .. n_bf - 1)
+  float *part;         // partial slots [*][G][PART_STRIDE]
+};
+
+__device__ __forceinline__ int npages_of(const PoolArgs &p, int b) {
+  int hl = p.hist_len[b];
+  hl = max(0, min(hl, p.max_pages * PAGE));
+  return (hl + PAGE - 1) / PAGE;
+}
+
+// Unpack one 32-bit word of 16 codes (code j at bits 2j) into 8 fp16x2 registers at r[base..base+7]:
+// register k holds (code k, code 8+k) as fp16 subnormals scaled by 4^k (k <= 4) or 4^(k-5) (k >= 5).
+__device__ __forceinline__ void unpack16(uint32_t x, uint32_t (&r)[16], int base) {
+#pragma unroll
+  for (int k = 0; k < 5; ++k) r[base + k] = x & (0x00030003u << (2 * k));
+  const uint32_t xs = x >> 10;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) r[base + 5 + k] = xs & (0x00030003u << (2 * k));
+}
+__device__ __forceinline__ float code_factor_inv(int k) {  // 1 / 4^k' for register k (0..7)
+  const int e = (k <= 4) ? 2 * k : 2 * (k - 5);
+  return __int_as_float((127 - e) << 23);
+}
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + max(-126, min(127, e))) << 23); }
+
+// Map a flattened page index to (b, kvh, local page) by a warp-cooperative scan over sequences.
+// Run by one full warp; results valid in every lane.  total receives the number of pages.
+__device__ void locate(const PoolArgs &p, long long start, int &b0, int &kvh0, int &local0, long long &total) {
+  const int lane = threadIdx.x & 31;
+  long long run = 0;
+  b0 = -1; kvh0 = 0; local0 = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    const long long v = (b < p.B) ? (long long)npages_of(p, b) * p.Hkv : 0;
+    long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const long long excl = run + inc - v;
+    const unsigned hit = __ballot_sync(FULL, b < p.B && v > 0 && start >= excl && start < excl + v);
+    if (b0 < 0 && hit) {
+      const int src = __ffs(hit) - 1;
+      const long long e = __shfl_sync(FULL, excl, src);
+      const int bb = base + src;
+      const int np = npages_of(p, bb);
+      b0 = bb;
+      kvh0 = (int)((start - e) / np);
+      local0 = (int)((start - e) % np);
+    }
+    run += __shfl_sync(FULL, inc, 31);
+  }
+  total = run;
+}
+
+template <int G>
+struct Smem {
+  static constexpr int NT = (2 * G + 7) / 8;
+  alignas(128) uint8_t ring[NSTAGE][STAGE_BYTES];
+  uint64_t full[NSTAGE], empty[NSTAGE];
+  int meta_seg[NSTAGE], meta_ntok[NSTAGE][STAGE_PAGES], meta_flags[NSTAGE];  // flags: 1 last, 2 abort
+  float qr[G][D];
+  float kfac[G], zfac[G];
+  int sigma[G];
+  float wm[CONSUMER_WARPS][G], wl[CONSUMER_WARPS][G], wz[CONSUMER_WARPS][G];
+  float wo[CONSUMER_WARPS][G][D];
+  float pbuf[CONSUMER_WARPS][G][16];
+  long long range_lo, range_n;
+  int b0, kvh0, local0;
+};
+
+// ---------------------------------------------------------------------------------------------
+template <int G>
+__global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot) {
+  __shared__ float qs[G][D];
+  __shared__ float part[3][G][D];
+  const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
+  const int tid = threadIdx.x, c = tid & (D - 1), qt = tid >> 7;  // quarter qt sums rows 32qt .. 32qt+31
+  for (int i = tid; i < G * D; i += 512) qs[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + kvh * G) * D + i]);
+  const float *R = p.R_k + (size_t)kvh * D * D + (size_t)(32 * qt) * D + c;
+  float r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = R[(size_t)i * D];
+  __syncthreads();
+  float acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][32 * qt + i], r[i], acc[h]);
+  if (qt > 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h) part[qt - 1][h][c] = acc[h];
+  __syncthreads();
+  if (qt == 0)
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      qrot[((size_t)b * p.Hq + kvh * G + h) * D + c] = ((acc[h] + part[0][h][c]) + part[1][h][c]) + part[2][h][c];
+}
+
+// ---------------------------------------------------------------------------------------------
+// BF16 sink/recent chunk: block index = segment * 5 + chunk (chunk 0 = sink, 1..4 = recent tokens
+// 64(chunk-1) .. 64 chunk - 1 counted from the oldest).
+template <int G>
+__device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
+  const PoolArgs &p = a.p;
+  const int idx = blockIdx.x;
+  const int seg = idx / 5, chunk = idx % 5, b = seg / p.Hkv, kvh = seg % p.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float *slot = a.part + ((size_t)a.n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5 + chunk) * G * PART_STRIDE;
+  if (warp >= CONSUMER_WARPS) return;
+  int slen = p.sink_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
+  slen = max(0, min(slen, SINK)); rs = max(0, min(rs, RECENT - 1)); rl = max(0, min(rl, RECENT));
+  const int n = (chunk == 0) ? slen : max(0, min(64, rl - (chunk - 1) * 64));
+  for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  const uint16_t *kb = chunk == 0 ? p.sink_k + ((size_t)b * p.Hkv + kvh) * SINK * D
+                                  : p.recent_k + ((size_t)b * p.Hkv + kvh) * RECENT * D;
+  const uint16_t *vb = chunk == 0 ? p.sink_v + ((size_t)b * p.Hkv + kvh) * SINK * D
+                                  : p.recent_v + ((size_t)b * p.Hkv + kvh) * RECENT * D;
+  auto row_of = [&](int i) { return chunk == 0 ? i : (rs + (chunk - 1) * 64 + i) % RECENT; };
+  // QK: lane -> token (lane & 15) of this warp's 16, channel half (lane >> 4)
+  const int tk = 16 * warp + (lane & 15), hf = lane >> 4;
+  const bool valid = tk < n;
+  float dot[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) dot[h] = 0.f;
+  if (valid) {
+    const uint4 *kr = reinterpret_cast<const uint4 *>(kb + (size_t)row_of(tk) * D + hf * 64);
+    uint4 w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = kr[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float kv = bf16_to_f32((ws[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+        const int c = hf * 64 + 8 * i + e;
+#pragma unroll
+        for (int h = 0; h < G; ++h) dot[h] = fmaf(kv, sm.qr[h][c], dot[h]);
+      }
+    }
+  }
+  float m2[G], l[G], o[G][4];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    dot[h] += __shfl_xor_sync(FULL, dot[h], 16);
+    const float s2 = valid ? dot[h] * a.sm_log2 : -INFINITY;
+    float mx = s2;
+#pragma unroll
+    for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o2));
+    const float pr = (s2 == -INFINITY) ? 0.f : exp2f(s2 - mx);
+    float sum = pr;
+#pragma unroll
+    for (int o2 = 1; o2 < 16; o2 <<= 1) sum += __shfl_xor_sync(FULL, sum, o2);
+    m2[h] = mx; l[h] = sum;
+    if (lane < 16) sm.pbuf[warp][h][lane] = pr;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[h][k] = 0.f;
+  }
+  __syncwarp();
+  // PV: lane -> channels 4*lane .. 4*lane+3
+  uint2 vv[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int t2 = 16 * warp + j;
+    vv[j] = t2 < n ? reinterpret_cast<const uint2 *>(vb + (size_t)row_of(t2) * D)[lane] : make_uint2(0, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float v[4] = {bf16_to_f32(vv[j].x & 0xffffu), bf16_to_f32(vv[j].x >> 16), bf16_to_f32(vv[j].y & 0xffffu),
+                        bf16_to_f32(vv[j].y >> 16)};
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float pj = sm.pbuf[warp][h][j];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[h][k] = fmaf(pj, v[k], o[h][k]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    if (lane == 0) { sm.wm[warp][h] = m2[h]; sm.wl[warp][h] = l[h]; }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sm.wo[warp][h][4 * lane + k] = o[h][k];
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < CONSUMER_WARPS; ++w) M = fmaxf(M, sm.wm[w][h]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < CONSUMER_WARPS; ++w) {
+        const float e = sm.wm[w][h] == -INFINITY ? 0.f : exp2f(sm.wm[w][h] - M);
+        L += e * sm.wl[w][h];
+        O += e * sm.wo[w][h][tid];
+      }
+    }
+    slot[h * PART_STRIDE + tid] = O;
+    if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int G>
+struct WarpState {
+  static constexpr int NT = (2 * G + 7) / 8;
+  float m2[NT], l[NT], oz[NT];
+  float O[NT][8][4];
+  int tau;        // weight scaling exponent (o accumulates in units of 2^-24 * 2^-tau per code step)
+  float tau_lim;  // largest V scale the current tau admits (0 until the first non-zero scale)
+};
+
+template <int G>
+__device__ __forceinline__ void reset(WarpState<G> &ws) {
+#pragma unroll
+  for (int nt = 0; nt < WarpState<G>::NT; ++nt) {
+    ws.m2[nt] = -INFINITY; ws.l[nt] = 0.f; ws.oz[nt] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) ws.O[nt][mt][r] = 0.f;
+  }
+  ws.tau = 0;
+  ws.tau_lim = 0.f;
+}
+
+// Segment setup (consumer threads only): load q_rot, derive per-head scaling, build B fragments.
+template <int G>
+__device__ __forceinline__ void setup_segment(const Args &a, Smem<G> &sm, int b, int kvh,
+                                              uint32_t (&bq)[Smem<G>::NT][8][2]) {
+  constexpr int NT = Smem<G>::NT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float *src = a.qrot + ((size_t)b * a.p.Hq + kvh * G) * D;
+  for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = src[i];
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  for (int h = warp; h < G; h += CONSUMER_WARPS) {
+    float amax = 0.f, sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = sm.qr[h][lane + 32 * k];
+      amax = fmaxf(amax, fabsf(v));
+      sum += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, o));
+      sum += __shfl_xor_sync(FULL, sum, o);
+    }
+    if (lane == 0) {
+      int e = 0;
+      if (amax > 0.f) frexpf(amax, &e);
+      const int sig = (amax > 0.f) ? 14 - e : 0;  // amax * 2^sig < 2^14
+      sm.sigma[h] = sig;
+      sm.kfac[h] = pow2f(24 - sig) * a.sm_log2;
+      sm.zfac[h] = sum * a.sm_log2;
+    }
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  const int gq = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = 4 * nt + (gq >> 1), split = gq & 1;
+    const bool live = h < G;
+    const float s2 = live ? pow2f(sm.sigma[h]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int i = 2 * j + hb;             // register index of the token's 16 (word i/8, slot i%8)
+        const int wi = i >> 3, k = i & 7;
+        const int ch_lo = 32 * t + 16 * wi + k, ch_hi = ch_lo + 8;
+        const float f = code_factor_inv(k) * s2;
+        float v[2];
+        const int chs[2] = {ch_lo, ch_hi};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x = live ? sm.qr[h][chs[e]] * f : 0.f;
+          const float hi = __half2float(__float2half_rn(x));
+          v[e] = split == 0 ? hi : x - hi;
+        }
+        bq[nt][j][hb] = pack_half2(v[0], v[1]);
+      }
+    }
+  }
+}
+
+// Flush the consumer warps' state for one segment into partial slot `slot`.
+template <int G>
+__device__ __forceinline__ void flush(const Args &a, Smem<G> &sm, WarpState<G> &ws, float *slot) {
+  constexpr int NT = Smem<G>::NT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gq = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float l = ws.l[nt], oz = ws.oz[nt];
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      l += __shfl_xor_sync(FULL, l, o);
+      oz += __shfl_xor_sync(FULL, oz, o);
+    }
+    const int h = 4 * nt + t;
+    if (h < G) {
+      if (gq == 0) { sm.wm[warp][h] = ws.m2[nt]; sm.wl[warp][h] = l; sm.wz[warp][h] = oz; }
+      const float unit = pow2f(24 - ws.tau);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int i = 2 * mt + r;
+          const int ch = 16 * gq + i;
+          sm.wo[warp][h][ch] = (ws.O[nt][mt][2 * r] + ws.O[nt][mt][2 * r + 1]) * unit * code_factor_inv(i & 7);
+        }
+    }
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  for (int h = 0; h < G; ++h) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < CONSUMER_WARPS; ++w) M = fmaxf(M, sm.wm[w][h]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < CONSUMER_WARPS; ++w) {
+        const float e = sm.wm[w][h] == -INFINITY ? 0.f : exp2f(sm.wm[w][h] - M);
+        L += e * sm.wl[w][h];
+        O += e * (sm.wo[w][h][tid] + sm.wz[w][h]);
+      }
+    }
+    slot[h * PART_STRIDE + tid] = O;
+    if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  reset(ws);
+}
+
+// One stage: tile `warp` (rows 16*warp .. +15) of each of the stage's pages; ntok[pg] = valid tokens
+// of page pg (0 when the page is absent or could not be loaded).  FULLP: both pages are full.
+template <int G, bool FULLP>
+__device__ __forceinline__ void stage_pass(const uint8_t *st, const int (&ntok)[STAGE_PAGES], const Smem<G> &sm,
+                                           WarpState<G> &ws, const uint32_t (&bq)[Smem<G>::NT][8][2]) {
+  constexpr int NT = Smem<G>::NT;
+  constexpr bool ALL_LIVE = (G % 4) == 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+  const int r0 = 16 * warp + gq, r1 = r0 + 8;
+  bool has[STAGE_PAGES];
+  float S[STAGE_PAGES][NT][4];
+  // ---- QK for both tiles: A = K codes (tokens r0, r1; lane t owns channels 32t .. 32t+31) ----
+#pragma unroll
+  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
+    has[pg] = FULLP || ntok[pg] > 16 * warp;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) S[pg][nt][0] = S[pg][nt][1] = S[pg][nt][2] = S[pg][nt][3] = 0.f;
+    if (has[pg]) {
+      const uint8_t *kc = st + pg * PAGE_BYTES + OFF_KC;
+      const uint2 ka = *reinterpret_cast<const uint2 *>(kc + r0 * 32 + 8 * t);
+      const uint2 kb = *reinterpret_cast<const uint2 *>(kc + r1 * 32 + 8 * t);
+      uint32_t T0[16], T1[16];
+      unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
+      unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          mma16816(S[pg][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+    }
+  }
+  // ---- scores and lazily rescaled online softmax over both tiles ----
+  float sc[STAGE_PAGES][2][NT], vz[STAGE_PAGES][2];
+  bool vld[STAGE_PAGES][2];
+#pragma unroll
+  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
+    const uint8_t *pb = st + pg * PAGE_BYTES;
+    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(pb + OFF_KS);
+    const uint16_t *Kz = reinterpret_cast<const uint16_t *>(pb + OFF_KZ);
+    const uint16_t *Vz = reinterpret_cast<const uint16_t *>(pb + OFF_VZ);
+    vld[pg][0] = FULLP || r0 < ntok[pg];
+    vld[pg][1] = FULLP || r1 < ntok[pg];
+    const float ks[2] = {bf16_to_f32(Ks[r0]), bf16_to_f32(Ks[r1])};
+    const float kz[2] = {bf16_to_f32(Kz[r0]), bf16_to_f32(Kz[r1])};
+    vz[pg][0] = vld[pg][0] ? bf16_to_f32(Vz[r0]) : 0.f;
+    vz[pg][1] = vld[pg][1] ? bf16_to_f32(Vz[r1]) : 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = ALL_LIVE ? 4 * nt + t : min(4 * nt + t, G - 1);
+      const float kf = sm.kfac[h], zf = sm.zfac[h];
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        sc[pg][e][nt] = vld[pg][e] ? fmaf((S[pg][nt][2 * e] + S[pg][nt][2 * e + 1]) * ks[e], kf, kz[e] * zf) : -INFINITY;
+    }
+  }
+  float P[STAGE_PAGES][2][NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float tmax = fmaxf(fmaxf(sc[0][0][nt], sc[0][1][nt]), fmaxf(sc[1][0][nt], sc[1][1][nt]));
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, o));
+    if (tmax > ws.m2[nt] + (float)LAZY) {
+      const float alpha = (ws.m2[nt] == -INFINITY) ? 0.f : fast_exp2(ws.m2[nt] - tmax);
+      ws.l[nt] *= alpha;
+      ws.oz[nt] *= alpha;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ws.O[nt][mt][r] *= alpha;
+      ws.m2[nt] = tmax;
+    }
+    const float m = ws.m2[nt];
+    const bool live = FULLP || m != -INFINITY;
+    float lsum = 0.f, zsum = 0.f;
+#pragma unroll
+    for (int pg = 0; pg < STAGE_PAGES; ++pg)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float pr = (live && vld[pg][e]) ? fast_exp2(sc[pg][e][nt] - m) : 0.f;
+        P[pg][e][nt] = pr;
+        lsum += pr;
+        zsum = fmaf(pr, vz[pg][e], zsum);
+      }
+    ws.l[nt] += lsum;
+    ws.oz[nt] += zsum;
+  }
+  // ---- weight scaling exponent from the V scales of both tiles (tokens t, t+4, t+8, t+12) ----
+  const int rb = 16 * warp;
+  float vs[STAGE_PAGES][4];
+  float vmax = 0.f;
+#pragma unroll
+  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
+    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(st + pg * PAGE_BYTES + OFF_VS);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int r = rb + t + 4 * e;
+      vs[pg][e] = (FULLP || r < ntok[pg]) ? bf16_to_f32(Vs[r]) : 0.f;
+      vmax = fmaxf(vmax, vs[pg][e]);
+    }
+  }
+  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 1));
+  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 2));
+  if (vmax >= ws.tau_lim && vmax > 0.f) {
+    int e;
+    frexpf(vmax, &e);
+    const int tnew = max(-100, min(100, WEXP - e));
+    if (ws.tau_lim > 0.f && tnew < ws.tau) {
+      const float f = pow2f(tnew - ws.tau);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) ws.O[nt][mt][r] *= f;
+    }
+    if (ws.tau_lim == 0.f || tnew < ws.tau) ws.tau = tnew;
+    ws.tau_lim = pow2f(WEXP - ws.tau);
+  }
+  const float tscale = pow2f(ws.tau);
+  // ---- P·V for each tile: A = V codes^T (lane g owns channels 16g .. 16g+15), B = split weights ----
+  const int hcol = gq >> 1;
+  const bool lo_split = (gq & 1) != 0;
+  const int srcA = 4 * t + hcol, srcB = 4 * (t + 4) + hcol;
+#pragma unroll
+  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
+    if (!has[pg]) continue;
+    uint32_t bw[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float p0 = P[pg][0][nt] * tscale, p1 = P[pg][1][nt] * tscale;
+      const float pa = __shfl_sync(FULL, p0, srcA), pc = __shfl_sync(FULL, p1, srcA);
+      const float pb = __shfl_sync(FULL, p0, srcB), pd = __shfl_sync(FULL, p1, srcB);
+      const bool live = ALL_LIVE || (4 * nt + hcol < G);
+      const float w0 = live ? pa * vs[pg][0] : 0.f, w1 = live ? pb * vs[pg][1] : 0.f;
+      const float w2 = live ? pc * vs[pg][2] : 0.f, w3 = live ? pd * vs[pg][3] : 0.f;
+      const uint32_t h01 = pack_half2(w0, w1), h23 = pack_half2(w2, w3);
+      const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
+      const uint32_t l01 = pack_half2(w0 - f01.x, w1 - f01.y), l23 = pack_half2(w2 - f23.x, w3 - f23.y);
+      bw[nt][0] = lo_split ? l01 : h01;
+      bw[nt][1] = lo_split ? l23 : h23;
+    }
+    const uint32_t *vrow = reinterpret_cast<const uint32_t *>(st + pg * PAGE_BYTES + OFF_VC);
+    const uint32_t xa = vrow[(rb + t) * 8 + gq], xb = vrow[(rb + t + 4) * 8 + gq];
+    const uint32_t xc = vrow[(rb + t + 8) * 8 + gq], xd = vrow[(rb + t + 12) * 8 + gq];
+    uint32_t VA[16], VB[16];
+    unpack16(prmt(xa, xb, 0x5410), VA, 0); unpack16(prmt(xa, xb, 0x7632), VA, 8);
+    unpack16(prmt(xc, xd, 0x5410), VB, 0); unpack16(prmt(xc, xd, 0x7632), VB, 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+        mma16816(ws.O[nt][mt], VA[2 * mt], VA[2 * mt + 1], VB[2 * mt], VB[2 * mt + 1], bw[nt][0], bw[nt][1]);
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int cta) {
+  constexpr int NT = Smem<G>::NT;
+  const PoolArgs &p = a.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], CONSUMER_WARPS); }
+    mbar_fence_init();
+  }
+  if (warp == CONSUMER_WARPS) {  // the producer warp locates this CTA's range
+    long long total;
+    int b0, kvh0, local0;
+    locate(p, 0, b0, kvh0, local0, total);  // total only
+    const long long chunk = (total + a.n_hist - 1) / a.n_hist;
+    const long long lo = (long long)cta * chunk;
+    const long long n = max(0ll, min(total, lo + chunk) - lo);
+    if (n > 0) locate(p, lo, b0, kvh0, local0, total);
+    if (lane == 0) { sm.range_lo = lo; sm.range_n = n; sm.b0 = b0; sm.kvh0 = kvh0; sm.local0 = local0; }
+  }
+  __syncthreads();
+  const long long n = sm.range_n;
+  if (n <= 0) return;
+
+  if (warp == CONSUMER_WARPS) {
+    // ---------------- producer: up to two pages of one segment per stage ----------------
+    if (lane == 0) {
+      int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
+      int np = npages_of(p, b);
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      long long done = 0;
+      while (done < n) {
+        bool abort = false;
+        if (it >= NSTAGE && !mbar_wait_bounded(&sm.empty[stage], phase ^ 1)) {
+          atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
+          abort = true;
+        }
+        const int seg = b * p.Hkv + kvh;
+        const int hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+        int bytes = 0, pages = 0;
+        int ntk[STAGE_PAGES] = {0, 0};
+        int phys[STAGE_PAGES] = {-1, -1};
+        while (!abort && pages < STAGE_PAGES && done < n && b * p.Hkv + kvh == seg) {
+          const int pp = p.page_table[(size_t)b * p.max_pages + local];
+          if (pp >= 0 && pp < p.num_pages) {
+            phys[pages] = pp;
+            ntk[pages] = min(PAGE, hl - local * PAGE);
+            bytes += PAGE_BYTES;
+          } else {
+            atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
+          }
+          ++pages;
+          ++done;
+          if (++local == np) {
+            local = 0;
+            if (++kvh == p.Hkv) {
+              kvh = 0;
+              do { ++b; } while (b < p.B && npages_of(p, b) == 0);
+              if (b < p.B) np = npages_of(p, b);
+            }
+          }
+        }
+        sm.meta_seg[stage] = seg;
+        sm.meta_ntok[stage][0] = ntk[0];
+        sm.meta_ntok[stage][1] = ntk[1];
+        sm.meta_flags[stage] = (done >= n ? 1 : 0) | (abort ? 2 : 0);
+        if (bytes > 0) {
+          mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)bytes);
+#pragma unroll
+          for (int pg = 0; pg < STAGE_PAGES; ++pg) {
+            if (phys[pg] < 0) continue;
+            uint8_t *dst = sm.ring[stage] + pg * PAGE_BYTES;
+            const size_t row = ((size_t)phys[pg] * p.Hkv + (seg % p.Hkv)) * PAGE;
+            bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, &sm.full[stage]);
+            bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, &sm.full[stage]);
+            bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, &sm.full[stage]);
+            bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, &sm.full[stage]);
+            bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, &sm.full[stage]);
+            bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, &sm.full[stage]);
+          }
+        } else {
+          mbar_arrive(&sm.full[stage]);
+        }
+        if (abort) {
+          // wait (bounded) for the copies still in flight into stages the consumers may not read
+          for (int k = max(0, it - NSTAGE + 1); k < it; ++k)
+            mbar_wait_bounded(&sm.full[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
+          break;
+        }
+        ++it;
+        if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
+      }
+    }
+    return;
+  }
+  // ---------------- consumers ----------------
+  WarpState<G> ws;
+  reset(ws);
+  uint32_t bq[NT][8][2];
+  int cur = -1, stage = 0;
+  uint32_t phase = 0;
+  while (true) {
+    if (!mbar_wait_bounded(&sm.full[stage], phase)) {
+      if (lane == 0) atomicOr(a.p.err, OSCAR_DEVERR_TIMEOUT);
+      break;
+    }
+    const int flags = sm.meta_flags[stage];
+    if (flags & 2) break;  // producer aborted
+    const int seg = sm.meta_seg[stage];
+    if (seg != cur) {
+      if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
+      cur = seg;
+      setup_segment(a, sm, seg / p.Hkv, seg % p.Hkv, bq);
+    }
+    const int ntok[STAGE_PAGES] = {sm.meta_ntok[stage][0], sm.meta_ntok[stage][1]};
+    if (ntok[0] == PAGE && ntok[1] == PAGE) stage_pass<G, true>(sm.ring[stage], ntok, sm, ws, bq);
+    else stage_pass<G, false>(sm.ring[stage], ntok, sm, ws, bq);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    if (flags & 1) break;
+    if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
+  }
+  if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
+}
+
+template <int G>
+__global__ void __launch_bounds__(THREADS) attn_kernel(Args a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
+  if ((int)blockIdx.x < a.n_bf) bf16_role<G>(a, sm);
+  else hist_role<G>(a, sm, (int)blockIdx.x - a.n_bf);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Merge: grid (G, Hkv, B), 512 threads; one CTA per (query head of the group, KV head, sequence).
+// The history partials of a segment sit in consecutive slots (CTA index + segment index).
+constexpr int MT = 512;
+template <int G>
+__global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out) {
+  __shared__ float ew[1032];
+  __shared__ float red[MT / 32];
+  __shared__ float Osl[4][D], Orot[D], Obf[D];
+  __shared__ long long s_pref, s_total;
+  const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == 0) {
+    long long total;
+    int bb, kk, ll;
+    locate(p, 0, bb, kk, ll, total);
+    long long run = 0;
+    for (int base = 0; base < b; base += 32) {
+      const int x = base + lane;
+      long long v = (x < b) ? (long long)npages_of(p, x) * p.Hkv : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+      run += v;
+    }
+    if (lane == 0) { s_pref = run; s_total = total; }
+  }
+  __syncthreads();
+  const int np = npages_of(p, b);
+  int nh = 0, i0 = 0;
+  if (np > 0) {
+    const long long chunk = (s_total + n_hist - 1) / n_hist;
+    const long long start = s_pref + (long long)kvh * np, end = start + np;
+    i0 = (int)(start / chunk);
+    nh = (int)((end - 1) / chunk) - i0 + 1;
+  }
+  const int nparts = nh + 5;
+  const size_t stride = (size_t)G * PART_STRIDE;
+  const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
+  const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
+  float mx = -INFINITY;
+  for (int i = tid; i < nparts; i += MT) {
+    const float m = (i < nh ? hp + i * stride : bp + (i - nh) * stride)[D];
+    ew[i] = m;
+    mx = fmaxf(mx, m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int w = 1; w < MT / 32; ++w) M = fmaxf(M, red[w]);
+  __syncthreads();
+  float ls = 0.f;
+  for (int i = tid; i < nparts; i += MT) {
+    const float e = (ew[i] == -INFINITY) ? 0.f : exp2f(ew[i] - M);
+    ew[i] = e;
+    ls += e * (i < nh ? hp + i * stride : bp + (i - nh) * stride)[D + 1];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+  if (lane == 0) red[warp] = ls;
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int w = 0; w < MT / 32; ++w) L += red[w];
+  // history sum in four slices; the BF16 chunks go to slice 3's threads afterwards
+  const int ch = tid & (D - 1), sl = tid >> 7;
+  float acc = 0.f;
+  {
+    const float *q = hp + (size_t)sl * stride + ch;
+    int i = sl;
+    for (; i + 12 < nh; i += 16, q += 16 * stride) {
+      const float x0 = q[0], x1 = q[4 * stride], x2 = q[8 * stride], x3 = q[12 * stride];
+      acc = fmaf(ew[i], x0, acc);
+      acc = fmaf(ew[i + 4], x1, acc);
+      acc = fmaf(ew[i + 8], x2, acc);
+      acc = fmaf(ew[i + 12], x3, acc);
+    }
+    for (; i < nh; i += 4, q += 4 * stride) acc = fmaf(ew[i], q[0], acc);
+  }
+  Osl[sl][ch] = acc;
+  if (sl == 3) {
+    float bfs = 0.f;
+#pragma unroll
+    for (int j = 0; j < 5; ++j) bfs = fmaf(ew[nh + j], bp[j * stride + ch], bfs);
+    Obf[ch] = bfs;
+  }
+  __syncthreads();
+  if (sl == 0) Orot[ch] = ((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch];
+  __syncthreads();
+  // un-rotate: o[ch] = sum_j o_rot[j] R_v[ch][j]; slice sl takes j in [32 sl, 32 sl + 32)
+  const float4 *Rrow = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + ch) * D + 32 * sl);
+  float4 rr[8];
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) rr[j4] = Rrow[j4];
+  float u = 0.f;
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const int j = 32 * sl + 4 * j4;
+    u = fmaf(rr[j4].x, Orot[j], u);
+    u = fmaf(rr[j4].y, Orot[j + 1], u);
+    u = fmaf(rr[j4].z, Orot[j + 2], u);
+    u = fmaf(rr[j4].w, Orot[j + 3], u);
+  }
+  __syncthreads();
+  Osl[sl][ch] = u;
+  __syncthreads();
+  if (sl == 0)
+    out[((size_t)b * p.Hq + kvh * G + h) * D + ch] =
+        L > 0.f ? ((((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch]) + Obf[ch]) / L : 0.f;
+}
+
+}  // namespace v1
+
+// ---------------------------------------------------------------------------------------------
+// Grid of the attention kernel: BF16 CTAs (5 per sequence and KV head) first, then history CTAs
+// sized so that both fit in one wave of resident CTAs (history CTAs get at least 3/4 of it).
+template <int G>
+static int resident_ctas() {
+  static int cached = 0;
+  if (cached == 0) {
+    int dev = 0, sms = 148, occ = 1;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = (int)sizeof(v1::Smem<G>);
+    cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v1::attn_kernel<G>, v1::THREADS, smem) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+    cached = sms * occ;
+  }
+  return cached;
+}
+
+static int resident_ctas_for(int G) {
+  switch (G) {
+    case 1: return resident_ctas<1>();
+    case 2: return resident_ctas<2>();
+    case 4: return resident_ctas<4>();
+    default: return resident_ctas<8>();
+  }
+}
+
+int v1_hist_ctas(const PoolArgs &p) {
+  const int slots = resident_ctas_for(p.Hq / p.Hkv);
+  const long long nbf = (long long)p.B * p.Hkv * 5;
+  long long n = slots - (nbf < slots / 4 ? nbf : slots / 4);
+  if (n > 1000) n = 1000;  // the merge kernel gathers at most 1032 partials per segment
+  const long long cap = (long long)p.B * p.Hkv * p.max_pages;
+  if (cap < n) n = cap;
+  return (int)(n < 1 ? 1 : n);
+}
+
+size_t v1_ws_bytes(const PoolArgs &p) {
+  const int G = p.Hq / p.Hkv;
+  const size_t slots = (size_t)v1_hist_ctas(p) + (size_t)p.B * p.Hkv * 6;
+  return (size_t)p.B * p.Hq * D * sizeof(float) + slots * G * PART_STRIDE * sizeof(float);
+}
+
+template <int G>
+static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
+                               cudaStream_t s) {
+  v1::Args a;
+  a.p = p;
+  a.q = q;
+  a.qrot = ws;
+  a.part = ws + (size_t)p.B * p.Hq * D;
+  a.sm_log2 = sm_scale * 1.4426950408889634f;
+  a.n_hist = v1_hist_ctas(p);
+  const int nbf = p.B * p.Hkv * 5;
+  a.n_bf = nbf;
+  const int smem = (int)sizeof(v1::Smem<G>);
+  cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  v1::qrot_kernel<G><<<p.B * p.Hkv, 512, 0, s>>>(p, q, ws);
+  profile_begin(OSCAR_PROFILE_HISTORY, s);
+  v1::attn_kernel<G><<<a.n_hist + nbf, v1::THREADS, smem, s>>>(a);
+  profile_end(OSCAR_PROFILE_HISTORY, s);
+  v1::merge_kernel<G><<<dim3(G, p.Hkv, p.B), v1::MT, 0, s>>>(p, a.part, a.n_hist, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
+                             cudaStream_t s) {
+  switch (p.Hq / p.Hkv) {
+    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s);
+    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s);
+    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s);
+    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace oscar

@@ -39,6 +39,11 @@ size_t decode_ws_bytes(const PoolArgs &p, int splits);
 cudaError_t launch_decode(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, int splits, float *ws,
                           cudaStream_t s);
 
+// decode_v1.cu (tensor-core path, group size 128)
+size_t v1_ws_bytes(const PoolArgs &p);
+cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
+                             cudaStream_t s);
+
 // rotation.cu
 size_t rotation_ws_bytes(int d);
 cudaError_t launch_make_rotation(int d, int mode, const double *M, double *R64, float *R32, void *ws,

@@ -156,14 +156,14 @@ struct QuantStats {
   uint32_t exact_elems, exact_groups, unproven;
 };
 
-__device__ inline void rotate_quantize_warp(const float *xs, const float *R, float clip, int g,
-                                            uint8_t *codes_out, uint16_t *scale_out, uint16_t *zero_out,
-                                            QuantStats &st) {
+// Partial fast-path dots over rows [i0, i1) of R: lane l accumulates channels 4l..4l+3 of x·R and of
+// |x|·|R| (the latter bounds the rounding error of the former).
+__device__ __forceinline__ void rot_dot_rows(const float *xs, const float *R, int i0, int i1, float (&acc)[4],
+                                             float (&sab)[4]) {
   const int lane = threadIdx.x & 31;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
   const float4 *R4 = reinterpret_cast<const float4 *>(R);
 #pragma unroll 8
-  for (int i = 0; i < D; ++i) {
+  for (int i = i0; i < i1; ++i) {
     const float xi = xs[i];
     const float ax = fabsf(xi);
     const float4 r = R4[i * (D / 4) + lane];
@@ -176,6 +176,36 @@ __device__ inline void rotate_quantize_warp(const float *xs, const float *R, flo
     sab[2] = fmaf(ax, fabsf(r.z), sab[2]);
     sab[3] = fmaf(ax, fabsf(r.w), sab[3]);
   }
+}
+
+// The same over exactly 32 rows starting at i0, with all 32 row loads issued before any use.
+__device__ __forceinline__ void rot_dot_32rows(const float *xs, const float *R, int i0, float (&acc)[4],
+                                               float (&sab)[4]) {
+  const int lane = threadIdx.x & 31;
+  const float4 *R4 = reinterpret_cast<const float4 *>(R) + (size_t)i0 * (D / 4) + lane;
+  float4 r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = R4[i * (D / 4)];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float xi = xs[i0 + i], ax = fabsf(xi);
+    acc[0] = fmaf(xi, r[i].x, acc[0]);
+    acc[1] = fmaf(xi, r[i].y, acc[1]);
+    acc[2] = fmaf(xi, r[i].z, acc[2]);
+    acc[3] = fmaf(xi, r[i].w, acc[3]);
+    sab[0] = fmaf(ax, fabsf(r[i].x), sab[0]);
+    sab[1] = fmaf(ax, fabsf(r[i].y), sab[1]);
+    sab[2] = fmaf(ax, fabsf(r[i].z), sab[2]);
+    sab[3] = fmaf(ax, fabsf(r[i].w), sab[3]);
+  }
+}
+
+// Quantize one vector from its fast-path dots (acc) and |x|·|R| sums (sab), however the 128
+// products were grouped and ordered (the error bound below holds for any summation order).
+__device__ inline void quantize_from_dots(const float *xs, const float *R, const float (&acc)[4], const float (&sab)[4],
+                                          float clip, int g, uint8_t *codes_out, uint16_t *scale_out,
+                                          uint16_t *zero_out, QuantStats &st) {
+  const int lane = threadIdx.x & 31;
   // gamma_128 = 7.6294e-6; 8e-6 also covers the rounding of sab itself; 1e-37 covers underflow.
   float a[4], b[4];
 #pragma unroll
@@ -286,6 +316,14 @@ __device__ inline void rotate_quantize_warp(const float *xs, const float *R, flo
     scale_out[lane / gl] = s;
     zero_out[lane / gl] = z;
   }
+}
+
+__device__ inline void rotate_quantize_warp(const float *xs, const float *R, float clip, int g,
+                                            uint8_t *codes_out, uint16_t *scale_out, uint16_t *zero_out,
+                                            QuantStats &st) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+  rot_dot_rows(xs, R, 0, D, acc, sab);
+  quantize_from_dots(xs, R, acc, sab, clip, g, codes_out, scale_out, zero_out, st);
 }
 
 // Load one bf16 head vector (128 values, 8-byte aligned) into the warp's shared float32 buffer.

@@ -10,18 +10,21 @@
 namespace oscar {
 
 // ---------------------------------------------------------------------------------------------
-// Demote (and optionally append): grid (Hkv, B), 64 threads.  Warp 0 handles K, warp 1 handles V
-// of KV head blockIdx.x of sequence blockIdx.y.  Every CTA reads the sequence's counters before
-// any CTA of that sequence can change them: the last CTA to arrive (arrival counter pool.sync[b])
-// updates the counters and returns the arrival counter to zero.
+// Demote (and optionally append): grid (Hkv, B), 256 threads.  Warps 0-3 rotate the K vector and
+// warps 4-7 the V vector of KV head blockIdx.x of sequence blockIdx.y, each warp over 32 rows of R
+// (all row loads issued at once); warps 0 and 4 then combine the partial dots and quantize.  Every
+// CTA reads the sequence's counters before any CTA of that sequence can change them: the last CTA to
+// arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
 // mode 2: as mode 0, then append k_new/v_new.
-__global__ void __launch_bounds__(64) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
-                                                           const uint16_t *k_new, const uint16_t *v_new) {
+__global__ void __launch_bounds__(256) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
+                                                            const uint16_t *k_new, const uint16_t *v_new) {
   __shared__ float xs[2][D];
+  __shared__ float pacc[8][32][4], psab[8][32][4];
   __shared__ int s_ok;
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv = warp >> 2, part = warp & 3;  // kv 0 = K, 1 = V
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
   bool demote = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
@@ -43,34 +46,46 @@ __global__ void __launch_bounds__(64) demote_append_kernel(PoolArgs p, const int
   // A demotion that cannot be stored leaves the whole sequence unchanged (no append either).
   const bool blocked = counters_ok && !demote && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
   if (demote) {
-    const uint16_t *src = (warp == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D;
-    load_vec_to_smem(src, xs[warp]);
-    const float *R = (warp == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
-    const float clip = (warp == 0 ? p.clip_k : p.clip_v)[kvh];
-    const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
-    QuantStats st{0, 0, 0};
-    rotate_quantize_warp(xs[warp], R, clip, p.g, (warp == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
-                         (warp == 0 ? p.scale_k : p.scale_v) + row * p.ng,
-                         (warp == 0 ? p.zero_k : p.zero_v) + row * p.ng, st);
+    const uint16_t *src = (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D;
+    const float *R = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
+    if (part == 0) load_vec_to_smem(src, xs[kv]);
+    __syncthreads();
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+    rot_dot_32rows(xs[kv], R, 32 * part, acc, sab);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { pacc[warp][lane][k] = acc[k]; psab[warp][lane][k] = sab[k]; }
+    __syncthreads();
+    if (part == 0) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[k] = ((pacc[warp][lane][k] + pacc[warp + 1][lane][k]) + pacc[warp + 2][lane][k]) + pacc[warp + 3][lane][k];
+        sab[k] = ((psab[warp][lane][k] + psab[warp + 1][lane][k]) + psab[warp + 2][lane][k]) + psab[warp + 3][lane][k];
+      }
+      const float clip = (kv == 0 ? p.clip_k : p.clip_v)[kvh];
+      const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
+      QuantStats st{0, 0, 0};
+      quantize_from_dots(xs[kv], R, acc, sab, clip, p.g, (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
+                         (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
+                         st);
+    }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
   const bool append = mode == 2 && counters_ok && !blocked;
   int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
   if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
-  if (append) {
-    uint16_t *dk, *dv;
+  if (append && (warp == 0 || warp == 4)) {
+    uint16_t *dst;
     if (nslen < SINK && nhl == 0 && nrl == 0) {
-      const size_t o = (((size_t)b * p.Hkv + kvh) * SINK + nslen) * D;
-      dk = p.sink_k + o; dv = p.sink_v + o;
-      nslen += 1;
+      dst = (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kvh) * SINK + nslen) * D;
     } else {
-      const size_t o = (((size_t)b * p.Hkv + kvh) * RECENT + (nrs + nrl) % RECENT) * D;
-      dk = p.recent_k + o; dv = p.recent_v + o;
-      nrl += 1;
+      dst = (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + (nrs + nrl) % RECENT) * D;
     }
     const size_t so = ((size_t)b * p.Hkv + kvh) * D;
-    if (warp == 0) reinterpret_cast<uint2 *>(dk)[lane] = reinterpret_cast<const uint2 *>(k_new + so)[lane];
-    else reinterpret_cast<uint2 *>(dv)[lane] = reinterpret_cast<const uint2 *>(v_new + so)[lane];
+    reinterpret_cast<uint2 *>(dst)[lane] = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + so)[lane];
+  }
+  if (append) {
+    if (nslen < SINK && nhl == 0 && nrl == 0) nslen += 1;
+    else nrl += 1;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -156,7 +171,7 @@ __global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl)
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
                           const uint16_t *v_new, cudaStream_t s) {
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
-  demote_append_kernel<<<dim3(p.Hkv, p.B), 64, 0, s>>>(p, mask, mode, k_new, v_new);
+  demote_append_kernel<<<dim3(p.Hkv, p.B), 256, 0, s>>>(p, mask, mode, k_new, v_new);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
   return cudaGetLastError();
 }

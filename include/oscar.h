@@ -55,6 +55,7 @@ typedef void *oscar_stream_t;  /* cudaStream_t */
 #define OSCAR_DEVERR_PAGE_INDEX 1u   /* page-table entry outside [0, num_pages)          */
 #define OSCAR_DEVERR_HISTORY_FULL 2u /* hist_len would exceed max_pages * 64             */
 #define OSCAR_DEVERR_COUNTERS 4u     /* sink_len/recent_start/recent_len/hist_len invalid */
+#define OSCAR_DEVERR_TIMEOUT 8u      /* an internal pipeline wait exceeded its time limit   */
 
 /* Rotation construction modes for oscar_make_rotation. */
 #define OSCAR_ROT_HAAR 0        /* M = d x d standard-normal draws; U = Q of QR(M), sign-fixed */
@@ -193,7 +194,9 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
  *   q       bf16 [batch][Hq][d]; query head h reads KV head h / (Hq/Hkv)
  *   out     fp32 [batch][Hq][d]
  *   softmax_scale   > 0 (usually 1/sqrt(d))
- *   num_splits      history split factor per (sequence, KV head); 0 = choose to fill the GPU
+ *   num_splits      history split factor per (sequence, KV head) for group sizes 32/64; 0 = choose
+ *                   to fill the GPU.  With group size 128 the library balances the history pages of
+ *                   all (sequence, KV head) pairs over a GPU-filling grid itself and ignores it.
  *   ws, ws_bytes    workspace of at least oscar_decode_workspace_size() bytes (same pool shape and
  *                   num_splits)
  * out[b][h] = sum over all pool tokens of softmax(score) * value, with score = q·k*scale for sink
