@@ -24,7 +24,9 @@ DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT = 1, 2, 
 
 __all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
            "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_demote", "oscar_append_kv",
-           "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events", "lib"]
+           "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events",
+           "oscar_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "lib"]
+NOALLOC_SCRATCH_BYTES = 8 << 20
 PROFILE_HISTORY, PROFILE_DEMOTE = 0, 1
 
 
@@ -198,3 +200,14 @@ def oscar_profile_events(which: int, start=None, stop=None):
     sp = None if start is None else C.c_void_p(start.cuda_event)
     ep = None if stop is None else C.c_void_p(stop.cuda_event)
     _lib.check(lib().oscar_profile_events(which, sp, ep), "oscar_profile_events")
+
+
+def oscar_decode_attention_noalloc(pool: Pool, q, out, softmax_scale=None, stream=None):
+    """Decode attention with the library's fixed device scratch (no allocation by the library or here):
+    q bf16 [B][Hq][128], out fp32 [B][Hq][128] caller-provided."""
+    _dev(q, torch.bfloat16, "q")
+    _dev(out, torch.float32, "out")
+    scale = 1.0 / math.sqrt(pool.d) if softmax_scale is None else float(softmax_scale)
+    _lib.check(lib().oscar_decode_attention_noalloc(pool.ref, _p(q), _p(out), scale, _s(stream)),
+               "oscar_decode_attention_noalloc")
+    return out

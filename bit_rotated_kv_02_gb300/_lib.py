@@ -48,6 +48,7 @@ SIGNATURES = {
     "oscar_decode_workspace_size": ([PP, I32, C.POINTER(C.c_size_t)], C.c_int),
     "oscar_decode_attention": ([PP, P, P, F32, I32, P, SZ, P], C.c_int),
     "oscar_profile_events": ([I32, P, P], C.c_int),
+    "oscar_decode_attention_noalloc": ([PP, P, P, F32, P], C.c_int),
 }
 
 _LIB = None

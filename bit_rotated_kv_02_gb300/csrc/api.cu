@@ -85,6 +85,7 @@ int auto_splits(const PoolArgs &a) {
 
 namespace oscar {
 ProfileSlot &profile_slot(int which) { return g_profile[which & 1]; }
+void set_last_error(const char *msg) { g_last_error = msg; }
 }  // namespace oscar
 
 extern "C" {

@@ -24,6 +24,9 @@ inline void profile_end(int which, cudaStream_t s) {
   p.start = p.stop = nullptr;
 }
 
+// Sets the calling thread's oscar_last_error_string() (api.cu).
+void set_last_error(const char *msg);
+
 // quantize.cu
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
                           const uint16_t *v_new, cudaStream_t s);

@@ -218,6 +218,26 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
 #define OSCAR_PROFILE_DEMOTE 1
 oscar_status_t oscar_profile_events(int32_t which, void *start, void *stop);
 
+/*
+ * Allocation-free decode attention (no counterpart on the pages: an interface convenience).
+ * Some callers cannot call cudaMalloc: a serving engine that has already handed all device memory to
+ * its KV pool and activation arenas, or a latency-critical decode loop that must not block on the
+ * device allocator (cudaMalloc may synchronize the device).  This entry point computes exactly what
+ * oscar_decode_attention(pool, q, out, softmax_scale, 0, ws, ...) computes, but its scratch space is a
+ * fixed device array of OSCAR_NOALLOC_SCRATCH_BYTES compiled into the library; every GPU that loads
+ * the library holds that array until the process exits.  It calls no allocator.
+ *   - Pools whose decode workspace (oscar_decode_workspace_size with num_splits 0) exceeds
+ *     OSCAR_NOALLOC_SCRATCH_BYTES are rejected with OSCAR_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks the array's device address up (cudaGetSymbolAddress) with
+ *     that device current; make that first call before starting any stream capture.
+ *   - All calls share the one array, and each call writes every scratch word it later reads, so
+ *     nothing needs clearing; but two calls whose kernels overlap on the GPU (different streams, or
+ *     different host threads) race on it.  Order such calls on one stream.
+ */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (8u << 20)
+oscar_status_t oscar_decode_attention_noalloc(const oscar_pool *pool, const oscar_bf16 *q, float *out,
+                                              float softmax_scale, oscar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
