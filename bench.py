@@ -369,7 +369,7 @@ def main():
                          "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic_from_profiles(os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc",
-                                                                       "decode.cu")),
+                                                                       "decode_v1.cu")),
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3},
             "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
                        statistics.mean(dem_ms) * 1e3, "note": "append+demote kernel, 1 token x 8 KV heads x K/V per launch"},
