@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed"], default="decode100k",
+                    help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -90,6 +92,25 @@ def run_cpu_baseline(budget_s: float) -> dict:
         return {"value": None, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------------------------
+# Multi-GPU: one replica of the workload per rank (the path shards into independent sequences and
+# has no exchange step), a barrier before and after the timed region, the slowest rank's time.
+def max_over_ranks(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, max_ms: float, world: int) -> float:
+    """Whole-job units per second: every rank processed units_per_rank in at most max_ms."""
+    return world * units_per_rank / (max_ms * 1e-3)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -203,6 +224,148 @@ def setup_layers(n_layers: int, extra_tokens: int, seed: int = 2024):
     return layers
 
 
+# ---------------------------------------------------------------------------------------------
+# The other workloads (one JSON line each): synthetic data generated on the GPU from seeded torch
+# generators (N(0,1) with outlier channels x20), Haar rotations built by the library.
+def _gpu_rotations(ok, n, d, seed):
+    import torch
+    import synth
+    return torch.stack([ok.oscar_make_rotation(torch.from_numpy(synth.gaussian_matrix(seed + i, d)).cuda(),
+                                               ok.ROT_HAAR)[1] for i in range(n)])
+
+
+def _gpu_kv(gen, n, hkv, chan, factor=20.0):
+    import torch
+    x = torch.randn((n, hkv, D), generator=gen, device="cuda")
+    idx = chan[None].expand(n, -1, -1)
+    x.scatter_(2, idx, x.gather(2, idx) * factor)
+    return x.to(torch.bfloat16)
+
+
+def _time(fn, steps, warmup):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps   # ms per step
+
+
+def other_workload(args):
+    import numpy as np
+    import torch
+    import bit_rotated_kv_02_gb300 as ok
+    import synth
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs") or 6800.0
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(4242)
+    lines = []
+    if args.workload == "bulk":
+        wl = synth.BULK_128K
+        N, Hkv = wl.context[0], wl.num_kv_heads
+        chan = torch.from_numpy(synth.outlier_channels(wl.seed, Hkv, D, wl.n_outliers).astype(np.int64)).cuda()
+        K, V = _gpu_kv(gen, N, Hkv, chan), _gpu_kv(gen, N, Hkv, chan)
+        Rk, Rv = _gpu_rotations(ok, Hkv, D, 10), _gpu_rotations(ok, Hkv, D, 50)
+        clip = torch.full((Hkv,), 0.9, device="cuda")
+        out = [ok.oscar_quantize_kv(K, Rk, clip, 128), ok.oscar_quantize_kv(V, Rv, clip, 128)]
+
+        def step():
+            ok.oscar_quantize_kv(K, Rk, clip, 128, *out[0])
+            ok.oscar_quantize_kv(V, Rv, clip, 128, *out[1])
+        ms = _time(step, max(3, args.steps), max(3, args.warmup))
+        byts = 2 * (N * Hkv * D * 2 + N * Hkv * (D // 4 + 4))
+        lines.append({"metric": "bulk prefill quantize: tokens/s (K and V of all KV heads)", "value": N / (ms * 1e-3),
+                      "unit": "tokens/s", "ms_per_step": ms, "workload": wl.name,
+                      "config": {"tokens": N, "num_kv_heads": Hkv, "head_dim": D, "group_size": 128, "clip": 0.9,
+                                 "l2": "inputs 537 MB > L2"},
+                      "roofline": {"bound": "hbm", "achieved": byts / (ms * 1e-3) / 1e9, "peak": peak,
+                                   "frac": byts / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s",
+                                   "algorithmic_bytes": byts,
+                                   "flops_fp32_rotation": 2.0 * 2 * N * Hkv * D * D}})
+        return lines
+    if args.workload == "batch-sweep":
+        for B in (1, 16, 64, 256):
+            wl = synth.batch_sweep(B)
+            L, Hq, Hkv = wl.context[0], wl.num_q_heads, wl.num_kv_heads
+            hist = L - SINK - RECENT
+            steps = max(3, min(args.steps, 200 if B < 64 else 40))
+            pages = -(-(hist + steps + args.warmup + 8) // PAGE)
+            chan = torch.from_numpy(synth.outlier_channels(wl.seed, Hkv, D, 4).astype(np.int64)).cuda()
+            Rk, Rv = _gpu_rotations(ok, Hkv, D, 100), _gpu_rotations(ok, Hkv, D, 200)
+            clip = torch.full((Hkv,), 0.9)
+            P = ok.Pool(B, Hq, Hkv, 128, B * pages, pages, Rk, Rv, clip, clip)
+            P.set_page_table(torch.randperm(B * pages, generator=gen, device="cuda").to(torch.int32).reshape(B, pages))
+            for b in range(B):
+                ok.oscar_prefill_pool(P, b, _gpu_kv(gen, L, Hkv, chan), _gpu_kv(gen, L, Hkv, chan))
+            q = (torch.randn((B, Hq, D), generator=gen, device="cuda") * 3).to(torch.bfloat16)
+            kn, vn = _gpu_kv(gen, B, Hkv, chan), _gpu_kv(gen, B, Hkv, chan)
+            out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+            ws = torch.empty(ok.oscar_decode_workspace_size(P), dtype=torch.uint8, device="cuda")
+
+            def step():
+                ok.oscar_append_kv(P, kn, vn)
+                ok.oscar_decode_attention(P, q, out=out, ws=ws)
+            ms = _time(step, steps, max(3, min(args.warmup, 20)))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                ok.oscar_append_kv(P, kn, vn)
+            e1.record()
+            torch.cuda.synchronize()
+            dem_ms = e0.elapsed_time(e1) / steps
+            assert P.err() == 0, hex(P.err())
+            byts = B * (hist * Hkv * 2 * (D // 4 + 4) + (SINK + RECENT) * Hkv * 2 * D * 2)
+            lines.append({"metric": "decode step (append+demote + attention): KV tokens/s", "batch": B,
+                          "value": B * L / (ms * 1e-3), "unit": "KV tokens/s", "decode_steps_per_s": 1e3 / ms,
+                          "ms_per_step": ms, "workload": wl.name,
+                          "demote": {"ms_per_call": dem_ms, "tokens_per_s": B / (dem_ms * 1e-3)},
+                          "step_gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak})
+            del P, ws
+            torch.cuda.empty_cache()
+        return lines
+    # mixed long-context batch (group 32, per-head clip ratios in [0.8, 1.0])
+    wl = synth.mixed_long()
+    Hq, Hkv, B = wl.num_q_heads, wl.num_kv_heads, wl.batch
+    lens = list(wl.context)
+    pages_b = [-(-(max(L - SINK - RECENT, 0) + 64) // PAGE) for L in lens]
+    chan = torch.from_numpy(synth.outlier_channels(wl.seed, Hkv, D, 4).astype(np.int64)).cuda()
+    Rk, Rv = _gpu_rotations(ok, Hkv, D, 300), _gpu_rotations(ok, Hkv, D, 400)
+    ck = torch.from_numpy(synth.clip_ratios(wl.seed, Hkv, 0.8, 1.0))
+    cv = torch.from_numpy(synth.clip_ratios(wl.seed + 1, Hkv, 0.8, 1.0))
+    mp = max(pages_b)
+    P = ok.Pool(B, Hq, Hkv, 32, sum(pages_b), mp, Rk, Rv, ck, cv)
+    perm = torch.randperm(sum(pages_b), generator=gen, device="cuda").to(torch.int32).cpu()
+    pt = torch.full((B, mp), -1, dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(pages_b):
+        pt[b, :n] = perm[o:o + n]
+        o += n
+    P.set_page_table(pt)
+    for b, L in enumerate(lens):
+        ok.oscar_prefill_pool(P, b, _gpu_kv(gen, L, Hkv, chan), _gpu_kv(gen, L, Hkv, chan))
+    q = (torch.randn((B, Hq, D), generator=gen, device="cuda") * 3).to(torch.bfloat16)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ok.oscar_decode_workspace_size(P), dtype=torch.uint8, device="cuda")
+    ms = _time(lambda: ok.oscar_decode_attention(P, q, out=out, ws=ws), max(3, min(args.steps, 100)), 5)
+    assert P.err() == 0, hex(P.err())
+    hist = sum(max(L - SINK - RECENT, 0) for L in lens)
+    byts = hist * Hkv * 2 * (D // 4 + 4 * 4) + B * (SINK + RECENT) * Hkv * 2 * D * 2
+    lines.append({"metric": "decode attention: KV tokens/s", "value": sum(lens) / (ms * 1e-3), "unit": "KV tokens/s",
+                  "ms_per_step": ms, "workload": wl.name, "lengths": lens,
+                  "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak})
+    return lines
+
+
 def main():
     args = parse()
     if args.cpu_baseline_child:
@@ -236,6 +399,11 @@ def main():
     import bit_rotated_kv_02_gb300 as ok
     from bit_rotated_kv_02_gb300 import _lib
     lib = ok.lib()
+    if args.workload != "decode100k":
+        if rank == 0:
+            for line in other_workload(args):
+                print(json.dumps(line))
+        return
 
     NL = args.layers
     total = args.warmup + args.steps + args.e2e_steps
@@ -296,10 +464,7 @@ def main():
     ms = t_start.elapsed_time(t_stop)
     hist_ms = [e[0].elapsed_time(e[1]) for e in evs]
     dem_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms)
     for P in layers:
         if P.err() != 0:
             raise RuntimeError(f"device error flags {P.err():#x}")
@@ -327,10 +492,7 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms)
 
     # algorithmic bytes of the history kernel per launch (codes + scale/zero + page table + q)
     hist_tokens_avg = (tokens / args.steps) - SINK - RECENT
@@ -349,7 +511,7 @@ def main():
     peak_src = "measured" if peak else "fallback"
     peak = peak or 6800.0
     achieved = attn_bytes / (hist_mean_ms * 1e-3) / 1e9
-    value = world * tokens / (ms * 1e-3)
+    value = replica_throughput(tokens, ms, world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.cpu_seconds)
@@ -373,7 +535,7 @@ def main():
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3},
             "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
                        statistics.mean(dem_ms) * 1e3, "note": "append+demote kernel, 1 token x 8 KV heads x K/V per launch"},
-            "e2e": {"value": world * e2e_tokens / (e2e_ms * 1e-3), "unit": "KV tokens/s",
+            "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
             "gpu_launches": args.steps * 4,   # append/demote, q rotation, attention, merge
