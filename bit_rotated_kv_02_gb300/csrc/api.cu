@@ -62,6 +62,9 @@ oscar_status_t check_pool(const oscar_pool *pool, PoolArgs &a) {
        reinterpret_cast<uintptr_t>(p.recent_k) | reinterpret_cast<uintptr_t>(p.recent_v) |
        reinterpret_cast<uintptr_t>(p.R_k) | reinterpret_cast<uintptr_t>(p.R_v)) & 15u)
     return fail(OSCAR_ERR_INVALID_ARG, "pool arrays must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(p.scale_k) | reinterpret_cast<uintptr_t>(p.zero_k) |
+       reinterpret_cast<uintptr_t>(p.scale_v) | reinterpret_cast<uintptr_t>(p.zero_v)) & 7u)
+    return fail(OSCAR_ERR_INVALID_ARG, "pool scale/zero arrays must be 8-byte aligned");
   a.B = p.batch; a.Hq = p.num_q_heads; a.Hkv = p.num_kv_heads; a.d = p.head_dim; a.g = p.group_size;
   a.ng = p.head_dim / p.group_size; a.num_pages = p.num_pages; a.max_pages = p.max_pages;
   a.sink_k = p.sink_k; a.sink_v = p.sink_v; a.recent_k = p.recent_k; a.recent_v = p.recent_v;
@@ -163,8 +166,10 @@ oscar_status_t oscar_quantize_kv(int64_t n_tokens, int32_t num_kv_heads, int32_t
   if (n_tokens == 0) return OSCAR_OK;
   if (x == nullptr || R32 == nullptr || clip == nullptr || codes == nullptr || scale == nullptr || zero == nullptr)
     return fail(OSCAR_ERR_INVALID_ARG, "NULL pointer");
-  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(R32)) & 15u)
-    return fail(OSCAR_ERR_INVALID_ARG, "x and R32 must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(R32) | reinterpret_cast<uintptr_t>(codes)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "x, R32 and codes must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(scale) | reinterpret_cast<uintptr_t>(zero)) & 7u)
+    return fail(OSCAR_ERR_INVALID_ARG, "scale and zero must be 8-byte aligned");
   return cuda_status(launch_quantize_rows(n_tokens, num_kv_heads, group_size, x, (int64_t)num_kv_heads * head_dim, R32,
                                           clip, codes, scale, zero, nullptr, 0, nullptr, stats,
                                           static_cast<cudaStream_t>(stream)),

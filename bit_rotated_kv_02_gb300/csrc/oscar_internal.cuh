@@ -67,10 +67,12 @@ __device__ __forceinline__ void two_sum(double a, double b, double &s, double &e
 // midpoint held in a double) is an integer < 2^53 times a power of two; all are aligned to the
 // smallest exponent and summed in 128-bit integers.  Returns -1, 0 or +1, or 2 when the exponent
 // span does not fit in 128 bits.  Runs serially on the calling lane (used only for exact ties).
-__device__ inline int exact_sign_minus(const float *xs, const float *R, int j, double m) {
+// XF: callable giving x_i (a float32-held bf16) for i in [0, 128).
+template <class XF>
+__device__ inline int exact_sign_minus_f(XF xs, const float *R, int j, double m) {
   int emin = 0x7fffffff, etop = -0x7fffffff;
   for (int i = 0; i < D; ++i) {
-    const float x = xs[i], r = R[i * D + j];
+    const float x = xs(i), r = R[i * D + j];
     if (x == 0.0f || r == 0.0f) continue;
     int ex, er;
     frexpf(x, &ex);
@@ -89,7 +91,7 @@ __device__ inline int exact_sign_minus(const float *xs, const float *R, int j, d
   if (etop - emin > 118) return 2;         // 7 bits of headroom for 128 terms + sign
   __int128 acc = 0;
   for (int i = 0; i < D; ++i) {
-    const float x = xs[i], r = R[i * D + j];
+    const float x = xs(i), r = R[i * D + j];
     if (x == 0.0f || r == 0.0f) continue;
     int ex, er;
     const long long mx = (long long)ldexpf(frexpf(x, &ex), 24);
@@ -100,13 +102,18 @@ __device__ inline int exact_sign_minus(const float *xs, const float *R, int j, d
   return acc > 0 ? 1 : (acc < 0 ? -1 : 0);
 }
 
-__device__ inline float exact_rot_elem(const float *xs, const float *R, int j, bool &unproven) {
+__device__ inline int exact_sign_minus(const float *xs, const float *R, int j, double m) {
+  return exact_sign_minus_f([xs](int i) { return xs[i]; }, R, j, m);
+}
+
+template <class XF>
+__device__ inline float exact_rot_elem_f(XF xs, const float *R, int j, bool &unproven) {
   const int lane = threadIdx.x & 31;
   double s = 0.0, c = 0.0, sa = 0.0;
 #pragma unroll
   for (int k = 0; k < D / 32; ++k) {
     const int i = lane + 32 * k;
-    const double p = (double)xs[i] * (double)R[i * D + j];
+    const double p = (double)xs(i) * (double)R[i * D + j];
     double t, e;
     two_sum(s, p, t, e);
     s = t;
@@ -134,7 +141,7 @@ __device__ inline float exact_rot_elem(const float *xs, const float *R, int j, b
     // Within the double-double's error bound of the midpoint (in practice an exact tie, which
     // bf16 x float32 products make possible): decide with exact integer arithmetic.
     int sg = 0;
-    if ((threadIdx.x & 31) == 0) sg = exact_sign_minus(xs, R, j, mid);
+    if ((threadIdx.x & 31) == 0) sg = exact_sign_minus_f(xs, R, j, mid);
     sg = __shfl_sync(FULL, sg, 0);
     if (sg == 2) unproven = true;
     else dist = (double)sg;
@@ -142,6 +149,10 @@ __device__ inline float exact_rot_elem(const float *xs, const float *R, int j, b
   if (dist > 0.0) return ru;
   if (dist < 0.0) return rd;
   return __double2float_rn(hi);                  // exact tie: to even
+}
+
+__device__ inline float exact_rot_elem(const float *xs, const float *R, int j, bool &unproven) {
+  return exact_rot_elem_f([xs](int i) { return xs[i]; }, R, j, unproven);
 }
 
 // ---- warp-cooperative rotate -> clip -> quantize -> pack of one head vector ----------------

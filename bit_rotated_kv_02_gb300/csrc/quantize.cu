@@ -106,50 +106,6 @@ __global__ void __launch_bounds__(256) demote_append_kernel(PoolArgs p, const in
   }
 }
 
-// ---------------------------------------------------------------------------------------------
-// Rotate/quantize rows of one KV head with R staged in shared memory.  grid (ceil(n/ROWS), Hkv),
-// 256 threads (8 warps), each warp loops over rows.  Output addressing: contiguous
-// [n][Hkv][...] (pt == nullptr) or paged through one page-table row (pt != nullptr, row t goes to
-// page pt[t/64], slot t%64).
-constexpr int QROWS = 64;
-
-__global__ void __launch_bounds__(256) quantize_rows_kernel(int64_t n, int Hkv, int g, const uint16_t *x,
-                                                           int64_t x_row_stride, const float *R32, const float *clip,
-                                                           uint8_t *codes, uint16_t *scale, uint16_t *zero,
-                                                           const int32_t *pt, int num_pages, uint32_t *err,
-                                                           uint32_t *stats) {
-  extern __shared__ float4 smem4[];
-  float *Rs = reinterpret_cast<float *>(smem4);
-  float *xs_all = Rs + D * D;
-  const int kvh = blockIdx.y;
-  const int warp = threadIdx.x >> 5;
-  const float *Rg = R32 + (size_t)kvh * D * D;
-  for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x) smem4[i] = reinterpret_cast<const float4 *>(Rg)[i];
-  __syncthreads();
-  float *xs = xs_all + warp * D;
-  const float c = clip[kvh];
-  const int ng = D / g;
-  QuantStats st{0, 0, 0};
-  const int64_t r0 = (int64_t)blockIdx.x * QROWS;
-  for (int64_t r = r0 + warp; r < r0 + QROWS && r < n; r += 8) {
-    size_t orow;
-    if (pt == nullptr) {
-      orow = (size_t)r * Hkv + kvh;
-    } else {
-      const int page = pt[r / PAGE];
-      if (page < 0 || page >= num_pages) {
-        if ((threadIdx.x & 31) == 0) atomicOr(err, OSCAR_DEVERR_PAGE_INDEX);
-        continue;
-      }
-      orow = ((size_t)page * Hkv + kvh) * PAGE + (r % PAGE);
-    }
-    load_vec_to_smem(x + (size_t)r * x_row_stride + (size_t)kvh * D, xs);
-    rotate_quantize_warp(xs, Rs, c, g, codes + orow * (D / 4), scale + orow * ng, zero + orow * ng, st);
-    __syncwarp();
-  }
-  flush_stats(stats, st);
-}
-
 // Copy token rows [t0, t0+n) of x [L][Hkv][D] into dst [Hkv][cap][D] rows [0, n) of one sequence.
 __global__ void copy_rows_kernel(const uint16_t *x, int64_t t0, int n, int Hkv, uint16_t *dst, int cap) {
   const int kvh = blockIdx.y;
@@ -173,21 +129,6 @@ cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, cons
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
   demote_append_kernel<<<dim3(p.Hkv, p.B), 256, 0, s>>>(p, mask, mode, k_new, v_new);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
-  return cudaGetLastError();
-}
-
-static size_t quant_smem_bytes() { return (size_t)D * D * 4 + 8 * D * 4; }
-
-cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride, const float *R32,
-                                 const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
-                                 const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  const size_t smem = quant_smem_bytes();
-  cudaError_t e = cudaFuncSetAttribute(quantize_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((n + QROWS - 1) / QROWS), Hkv);
-  quantize_rows_kernel<<<grid, 256, smem, s>>>(n, Hkv, g, x, x_row_stride, R32, clip, codes, scale, zero, pt,
-                                               num_pages, err, stats);
   return cudaGetLastError();
 }
 

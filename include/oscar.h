@@ -145,7 +145,9 @@ oscar_status_t oscar_calib_covariance_v(int64_t T, int32_t heads, int32_t d, con
  *   codes   u8   [n_tokens][Hkv][d/4]        output
  *   scale, zero  bf16 [n_tokens][Hkv][d/group_size]  output
  *   stats   uint32 [4] or NULL: [0] += elements re-evaluated exactly, [1] += groups whose scale/zero
- *           needed the exact path, [2] += results not proven correctly rounded (expected 0)
+ *           needed the exact path, [2] += results not proven correctly rounded (expected 0),
+ *           [3] |= OSCAR_DEVERR_* bits of device-side failures (a pipeline wait that timed out)
+ *   Alignment: x, R32 and codes 16 bytes; scale and zero 8 bytes.
  * Arithmetic per group (IEEE float32, nearest-even): x_hat = nearest float32 to the exact x · R;
  * lo = c*min, hi = c*max, s = (hi-lo)/3, scale = bf16(s), zero = bf16(lo),
  * code = clamp(rint((x_hat - zero)/scale), 0, 3) with the stored bf16 scale/zero; scale 0 -> codes 0.

@@ -103,3 +103,17 @@ def test_bulk_full_size_sampled():
     rows = np.concatenate([[0, 1, N - 2, N - 1], rows])
     check_rows(xb, R32, (0.9,) * Hkv, 128, gc, gs, gz, rows)
     assert st[2] == 0
+
+
+@pytest.mark.parametrize("g,Hkv", [(32, 3), (128, 2)])
+def test_many_tiles_per_block_every_row(g, Hkv):
+    """Enough rows that each block runs several tiles through its pipeline and crosses into the next
+    head's rotation (head switches, ring wrap-around, both epilogue groups); every row checked."""
+    d, N = 128, 50_000 + 17
+    R32 = helpers.oracle_rotations(90 + g, Hkv)
+    ch = synth.outlier_channels(91 + g, Hkv, d, 4)
+    xb = synth.outlier_kv(92 + g, N, Hkv, d, ch)
+    clip = (0.9, 0.8, 0.95)[:Hkv]
+    gc, gs, gz, st = run_gpu(xb, R32, clip, g)
+    check_rows(xb, R32, clip, g, gc, gs, gz)
+    assert st[2] == 0 and st[3] == 0
