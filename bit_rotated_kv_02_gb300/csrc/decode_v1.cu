@@ -126,6 +126,8 @@ template <int G>
 __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot) {
   __shared__ float qs[G][D];
   __shared__ float part[3][G][D];
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
   const int tid = threadIdx.x, c = tid & (D - 1), qt = tid >> 7;  // quarter qt sums rows 32qt .. 32qt+31
   for (int i = tid; i < G * D; i += 512) qs[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + kvh * G) * D + i]);
@@ -672,22 +674,37 @@ template <int G>
 __global__ void __launch_bounds__(THREADS) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
+  pdl_wait();
+  pdl_trigger();
   if ((int)blockIdx.x < a.n_bf) bf16_role<G>(a, sm);
   else hist_role<G>(a, sm, (int)blockIdx.x - a.n_bf);
 }
 
 // ---------------------------------------------------------------------------------------------
 // Merge: grid (G, Hkv, B), 512 threads; one CTA per (query head of the group, KV head, sequence).
-// The history partials of a segment sit in consecutive slots (CTA index + segment index).
+// The history partials of a segment sit in consecutive slots (CTA index + segment index).  Latency
+// bound, so the global reads are issued in few dependent rounds: the pool counters (to locate the
+// segment's partials) together with this thread's R_v rows, then every partial's (m, l) together with
+// up to OV output values per thread; the softmax weights are applied once the maximum is known.
 constexpr int MT = 512;
+constexpr int MAXPARTS = 1040;
 template <int G>
 __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out) {
-  __shared__ float ew[1032];
+  constexpr int OV = 36;  // partials per slice issued at once (4 slices: 144 partials)
+  __shared__ float wgt[MAXPARTS], lsum[MAXPARTS];
   __shared__ float red[MT / 32];
-  __shared__ float Osl[4][D], Orot[D], Obf[D];
+  __shared__ float Osl[4][D], Obs[4][D], Orot[D];
   __shared__ long long s_pref, s_total;
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ch = tid & (D - 1), sl = tid >> 7;
+  // un-rotation rows: o[ch] = sum_j o_rot[j] R_v[ch][j]; slice sl takes j in [32 sl, 32 sl + 32)
+  const float4 *Rrow = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + ch) * D + 32 * sl);
+  float4 rr[8];
+#pragma unroll
+  for (int j4 = 0; j4 < 8; ++j4) rr[j4] = Rrow[j4];
   if (warp == 0) {
     long long total;
     int bb, kk, ll;
@@ -715,11 +732,20 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   const size_t stride = (size_t)G * PART_STRIDE;
   const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
   const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
+  auto slot = [&](int i) { return i < nh ? hp + (size_t)i * stride : bp + (size_t)(i - nh) * stride; };
   float mx = -INFINITY;
   for (int i = tid; i < nparts; i += MT) {
-    const float m = (i < nh ? hp + i * stride : bp + (i - nh) * stride)[D];
-    ew[i] = m;
+    const float *q = slot(i);
+    const float m = q[D];
+    wgt[i] = m;
+    lsum[i] = q[D + 1];
     mx = fmaxf(mx, m);
+  }
+  float ov[OV];
+#pragma unroll
+  for (int k = 0; k < OV; ++k) {
+    const int i = sl + 4 * k;
+    ov[k] = i < nparts ? slot(i)[ch] : 0.f;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
@@ -731,9 +757,9 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   __syncthreads();
   float ls = 0.f;
   for (int i = tid; i < nparts; i += MT) {
-    const float e = (ew[i] == -INFINITY) ? 0.f : exp2f(ew[i] - M);
-    ew[i] = e;
-    ls += e * (i < nh ? hp + i * stride : bp + (i - nh) * stride)[D + 1];
+    const float e = (wgt[i] == -INFINITY) ? 0.f : exp2f(wgt[i] - M);
+    wgt[i] = e;
+    ls += e * lsum[i];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
@@ -742,36 +768,24 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   float L = 0.f;
 #pragma unroll
   for (int w = 0; w < MT / 32; ++w) L += red[w];
-  // history sum in four slices; the BF16 chunks go to slice 3's threads afterwards
-  const int ch = tid & (D - 1), sl = tid >> 7;
-  float acc = 0.f;
-  {
-    const float *q = hp + (size_t)sl * stride + ch;
-    int i = sl;
-    for (; i + 12 < nh; i += 16, q += 16 * stride) {
-      const float x0 = q[0], x1 = q[4 * stride], x2 = q[8 * stride], x3 = q[12 * stride];
-      acc = fmaf(ew[i], x0, acc);
-      acc = fmaf(ew[i + 4], x1, acc);
-      acc = fmaf(ew[i + 8], x2, acc);
-      acc = fmaf(ew[i + 12], x3, acc);
-    }
-    for (; i < nh; i += 4, q += 4 * stride) acc = fmaf(ew[i], q[0], acc);
+  // weighted sums: history partials (rotated space) and BF16 partials (original space) apart
+  float acc = 0.f, accb = 0.f;
+#pragma unroll
+  for (int k = 0; k < OV; ++k) {
+    const int i = sl + 4 * k;
+    const float w = i < nparts ? wgt[i] : 0.f;
+    if (i < nh) acc = fmaf(w, ov[k], acc);
+    else accb = fmaf(w, ov[k], accb);
+  }
+  for (int i = sl + 4 * OV; i < nparts; i += 4) {
+    if (i < nh) acc = fmaf(wgt[i], slot(i)[ch], acc);
+    else accb = fmaf(wgt[i], slot(i)[ch], accb);
   }
   Osl[sl][ch] = acc;
-  if (sl == 3) {
-    float bfs = 0.f;
-#pragma unroll
-    for (int j = 0; j < 5; ++j) bfs = fmaf(ew[nh + j], bp[j * stride + ch], bfs);
-    Obf[ch] = bfs;
-  }
+  Obs[sl][ch] = accb;
   __syncthreads();
   if (sl == 0) Orot[ch] = ((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch];
   __syncthreads();
-  // un-rotate: o[ch] = sum_j o_rot[j] R_v[ch][j]; slice sl takes j in [32 sl, 32 sl + 32)
-  const float4 *Rrow = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + ch) * D + 32 * sl);
-  float4 rr[8];
-#pragma unroll
-  for (int j4 = 0; j4 < 8; ++j4) rr[j4] = Rrow[j4];
   float u = 0.f;
 #pragma unroll
   for (int j4 = 0; j4 < 8; ++j4) {
@@ -784,9 +798,11 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   __syncthreads();
   Osl[sl][ch] = u;
   __syncthreads();
-  if (sl == 0)
-    out[((size_t)b * p.Hq + kvh * G + h) * D + ch] =
-        L > 0.f ? ((((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch]) + Obf[ch]) / L : 0.f;
+  if (sl == 0) {
+    const float o = (((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch]) +
+                    (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
+    out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
+  }
 }
 
 }  // namespace v1
@@ -823,7 +839,7 @@ int v1_hist_ctas(const PoolArgs &p) {
   const int slots = resident_ctas_for(p.Hq / p.Hkv);
   const long long nbf = (long long)p.B * p.Hkv * 5;
   long long n = slots - (nbf < slots / 4 ? nbf : slots / 4);
-  if (n > 1000) n = 1000;  // the merge kernel gathers at most 1032 partials per segment
+  if (n > 1000) n = 1000;  // the merge kernel gathers at most MAXPARTS partials per segment
   const long long cap = (long long)p.B * p.Hkv * p.max_pages;
   if (cap < n) n = cap;
   return (int)(n < 1 ? 1 : n);
@@ -850,12 +866,12 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   const int smem = (int)sizeof(v1::Smem<G>);
   cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  v1::qrot_kernel<G><<<p.B * p.Hkv, 512, 0, s>>>(p, q, ws);
+  if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws)) != cudaSuccess) return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
-  v1::attn_kernel<G><<<a.n_hist + nbf, v1::THREADS, smem, s>>>(a);
+  if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
-  v1::merge_kernel<G><<<dim3(G, p.Hkv, p.B), v1::MT, 0, s>>>(p, a.part, a.n_hist, out);
-  return cudaGetLastError();
+  return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), 0, s, p, (const float *)a.part, a.n_hist,
+                    out);
 }
 
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,

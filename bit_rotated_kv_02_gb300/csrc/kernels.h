@@ -27,6 +27,23 @@ inline void profile_end(int which, cudaStream_t s) {
 // Sets the calling thread's oscar_last_error_string() (api.cu).
 void set_last_error(const char *msg);
 
+// Launch with programmatic stream serialization (the kernel must start with pdl_wait()): its blocks
+// may be scheduled while the previous kernel of the stream finishes, hiding the launch gap.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // quantize.cu
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
                           const uint16_t *v_new, cudaStream_t s);

@@ -158,45 +158,17 @@ __device__ inline float exact_rot_elem(const float *xs, const float *R, int j, b
 // ---- warp-cooperative rotate -> clip -> quantize -> pack of one head vector ----------------
 // xs: this warp's float32 copy of the bf16 input vector (128 entries, shared memory).
 // R:  row-major fp32 [128][128] (global or shared).  Lane l owns rotated channels 4l..4l+3.
-// Fast path: sequential float32 FMA dots plus the running sum of |x_i R_ij|; the classical bound
+// Fast path: float32 FMA dots plus the running sum of |x_i R_ij|; the classical bound
 // |fl(dot) - dot| <= gamma_128 * sum|x_i R_ij| (gamma_n = n u / (1 - n u), u = 2^-24) gives an
-// interval [a, b] that must contain the correctly rounded x_hat.  scale/zero are taken from the
-// interval when every corner gives the same bf16 result, and a code when both ends give the same
-// code (every quantizer step is monotone); otherwise the affected elements are evaluated exactly.
+// interval that must contain the correctly rounded x_hat.  Every quantizer step is monotone, so a
+// decision taken at both ends of an interval holds for every value inside it.
 struct QuantStats {
   uint32_t exact_elems, exact_groups, unproven;
 };
 
-// Partial fast-path dots over rows [i0, i1) of R: lane l accumulates channels 4l..4l+3 of x·R and of
-// |x|·|R| (the latter bounds the rounding error of the former).
-__device__ __forceinline__ void rot_dot_rows(const float *xs, const float *R, int i0, int i1, float (&acc)[4],
-                                             float (&sab)[4]) {
-  const int lane = threadIdx.x & 31;
-  const float4 *R4 = reinterpret_cast<const float4 *>(R);
-#pragma unroll 8
-  for (int i = i0; i < i1; ++i) {
-    const float xi = xs[i];
-    const float ax = fabsf(xi);
-    const float4 r = R4[i * (D / 4) + lane];
-    acc[0] = fmaf(xi, r.x, acc[0]);
-    acc[1] = fmaf(xi, r.y, acc[1]);
-    acc[2] = fmaf(xi, r.z, acc[2]);
-    acc[3] = fmaf(xi, r.w, acc[3]);
-    sab[0] = fmaf(ax, fabsf(r.x), sab[0]);
-    sab[1] = fmaf(ax, fabsf(r.y), sab[1]);
-    sab[2] = fmaf(ax, fabsf(r.z), sab[2]);
-    sab[3] = fmaf(ax, fabsf(r.w), sab[3]);
-  }
-}
-
-// The same over exactly 32 rows starting at i0, with all 32 row loads issued before any use.
-__device__ __forceinline__ void rot_dot_32rows(const float *xs, const float *R, int i0, float (&acc)[4],
-                                               float (&sab)[4]) {
-  const int lane = threadIdx.x & 31;
-  const float4 *R4 = reinterpret_cast<const float4 *>(R) + (size_t)i0 * (D / 4) + lane;
-  float4 r[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) r[i] = R4[i * (D / 4)];
+// The same over 32 rows i0 .. i0+31 already in registers (r[i] = row i0 + i, this lane's four channels).
+__device__ __forceinline__ void rot_dot_32rows_pre(const float *xs, const float4 (&r)[32], int i0, float (&acc)[4],
+                                                   float (&sab)[4]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const float xi = xs[i0 + i], ax = fabsf(xi);
@@ -211,115 +183,148 @@ __device__ __forceinline__ void rot_dot_32rows(const float *xs, const float *R, 
   }
 }
 
+// Warp-cooperative interval [x, y] containing the float32 nearest to the exact x . R_j (xs: float32
+// copy of the bf16 vector; R row-major fp32).  Products are split error-free (p + e = x r, FMA),
+// partial sums carry their rounding errors (TwoSum), and the errors are summed in plain float32,
+// whose own error is below gamma_2n * gamma_n * sum|x r| < 2^-33 sum|x r|; the interval uses 2^-31
+// times the computed sum.  Every lane returns the same interval.
+__device__ __forceinline__ void two_sum_f32(float a, float b, float &s, float &e) {
+  s = __fadd_rn(a, b);
+  const float bp = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+static __device__ __noinline__ float2 dot2_interval_xs(const float *xs, const float *R, int j) {
+  const int lane = threadIdx.x & 31;
+  float s = 0.f, c = 0.f, sab = 0.f;
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) {
+    const int i = lane + 32 * k;
+    const float xv = xs[i], rv = R[i * D + j];
+    const float p = __fmul_rn(xv, rv);
+    const float e = fmaf(xv, rv, -p);
+    float t, q;
+    two_sum_f32(s, p, t, q);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(q, e));
+    sab = fmaf(fabsf(xv), fabsf(rv), sab);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float s2 = __shfl_xor_sync(FULL, s, off);
+    const float c2 = __shfl_xor_sync(FULL, c, off);
+    const float a2 = __shfl_xor_sync(FULL, sab, off);
+    float t, q;
+    two_sum_f32(s, s2, t, q);
+    s = t;
+    c = __fadd_rn(__fadd_rn(c, c2), q);
+    sab = __fadd_rn(sab, a2);
+  }
+  float hi, lo;
+  two_sum_f32(s, c, hi, lo);
+  const float B = __fadd_ru(__fmul_ru(sab, 0x1p-31f), 1e-36f);
+  return make_float2(__fadd_rd(hi, __fsub_rd(lo, B)), __fadd_ru(hi, __fadd_ru(lo, B)));
+}
+
 // Quantize one vector from its fast-path dots (acc) and |x|·|R| sums (sab), however the 128
 // products were grouped and ordered (the error bound below holds for any summation order).
+// Every element carries an interval [lo, hi] that contains its correctly rounded x_hat: first the
+// fast one; for the elements a decision needs, a Dot2 interval; if that still leaves the decision
+// open, the exact value.  A group's zero is decided when both ends of its minimum's interval give
+// the same bf16 zero, its scale when both extreme corners give the same bf16 scale (zero increases
+// with the minimum; scale increases with the maximum and decreases with the minimum), and a code
+// when both ends of the element's interval give the same code.
 __device__ inline void quantize_from_dots(const float *xs, const float *R, const float (&acc)[4], const float (&sab)[4],
                                           float clip, int g, uint8_t *codes_out, uint16_t *scale_out,
                                           uint16_t *zero_out, QuantStats &st) {
   const int lane = threadIdx.x & 31;
+  const int gl = g / 4;  // lanes per group (8, 16 or 32)
   // gamma_128 = 7.6294e-6; 8e-6 also covers the rounding of sab itself; 1e-37 covers underflow.
-  float a[4], b[4];
+  float lo[4], hi[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const float E = __fadd_ru(__fmul_ru(sab[k], 8.0e-6f), 1e-37f);
-    a[k] = __fsub_rd(acc[k], E);
-    b[k] = __fadd_ru(acc[k], E);
+    lo[k] = __fsub_rd(acc[k], E);
+    hi[k] = __fadd_ru(acc[k], E);
   }
-  const int gl = g / 4;  // lanes per group (8, 16 or 32)
-  float mn_lo = fminf(fminf(a[0], a[1]), fminf(a[2], a[3]));
-  float mn_hi = fminf(fminf(b[0], b[1]), fminf(b[2], b[3]));
-  float mx_lo = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
-  float mx_hi = fmaxf(fmaxf(b[0], b[1]), fmaxf(b[2], b[3]));
-  for (int off = gl / 2; off > 0; off >>= 1) {
-    mn_lo = fminf(mn_lo, __shfl_xor_sync(FULL, mn_lo, off));
-    mn_hi = fminf(mn_hi, __shfl_xor_sync(FULL, mn_hi, off));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(FULL, mx_lo, off));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(FULL, mx_hi, off));
-  }
-  uint16_t z = zero_of(clip, mn_lo);
-  uint16_t s = scale_of(clip, mn_lo, mx_lo);
-  const bool decided = z == zero_of(clip, mn_hi) && s == scale_of(clip, mn_lo, mx_hi) &&
-                       s == scale_of(clip, mn_hi, mx_lo) && s == scale_of(clip, mn_hi, mx_hi);
-
-  float xe[4];
-  bool known[4] = {false, false, false, false};
+  auto group_min = [&](float v) {
+    for (int off = gl / 2; off > 0; off >>= 1) v = fminf(v, __shfl_xor_sync(FULL, v, off));
+    return v;
+  };
+  auto group_max = [&](float v) {
+    for (int off = gl / 2; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, off));
+    return v;
+  };
+  const float mn_lo = group_min(fminf(fminf(lo[0], lo[1]), fminf(lo[2], lo[3])));
+  const float mn_hi = group_min(fminf(fminf(hi[0], hi[1]), fminf(hi[2], hi[3])));
+  const float mx_lo = group_max(fmaxf(fmaxf(lo[0], lo[1]), fmaxf(lo[2], lo[3])));
+  const float mx_hi = group_max(fmaxf(fmaxf(hi[0], hi[1]), fmaxf(hi[2], hi[3])));
+  uint16_t z = zero_of(clip, mn_lo), s = scale_of(clip, mn_hi, mx_lo);
+  bool uz = z != zero_of(clip, mn_hi), us = s != scale_of(clip, mn_lo, mx_hi);
+  st.exact_groups += __popc(__ballot_sync(FULL, (uz || us) && (lane & (gl - 1)) == 0));
   bool unproven = false;
-  // Exact min/max where the interval leaves scale or zero open: only elements whose interval
-  // reaches the group's extreme can be the extreme.
-  bool candmin[4], candmax[4];
+  // candidates for the extremes: only elements whose interval reaches the group's extreme
+  bool cmin[4], cmax[4], cand[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    candmin[k] = !decided && a[k] <= mn_hi;
-    candmax[k] = !decided && b[k] >= mx_lo;
+    cmin[k] = (uz || us) && lo[k] <= mn_hi;
+    cmax[k] = us && hi[k] >= mx_lo;
+    cand[k] = cmin[k] || cmax[k];
   }
-  unsigned pend = __ballot_sync(FULL, candmin[0] || candmin[1] || candmin[2] || candmin[3] ||
-                                          candmax[0] || candmax[1] || candmax[2] || candmax[3]);
-  while (pend) {
-    const int src = __ffs(pend) - 1;
-    uint32_t mymask = 0;
+  int done[4] = {-1, -1, -1, -1};  // highest tier already applied to the element
+  // evaluate the flagged elements of the warp at `tier` (0: Dot2 interval, 1: exact value)
+  auto evaluate = [&](const bool (&flag)[4], int tier) {
+    uint32_t mine = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if ((candmin[k] || candmax[k]) && !known[k]) mymask |= 1u << k;
-    mymask = __shfl_sync(FULL, mymask, src);
-    const int k = __ffs(mymask) - 1;
-    const float v = exact_rot_elem(xs, R, 4 * src + k, unproven);
-    if (lane == src) {
+      if (flag[k] && done[k] < tier) mine |= 1u << k;
+    while (__any_sync(FULL, mine != 0)) {
+      const int src = __ffs(__ballot_sync(FULL, mine != 0)) - 1;
+      const int k = __ffs(__shfl_sync(FULL, mine, src)) - 1;
+      float2 iv;
+      if (tier == 0) iv = dot2_interval_xs(xs, R, 4 * src + k);
+      else iv.x = iv.y = exact_rot_elem(xs, R, 4 * src + k, unproven);
+      if (lane == src) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        if (kk == k) { xe[kk] = v; known[kk] = true; }
+        for (int kk = 0; kk < 4; ++kk)
+          if (kk == k) { lo[kk] = iv.x; hi[kk] = iv.y; done[kk] = tier; }
+        mine &= mine - 1;
+      }
+      ++st.exact_elems;
     }
-    ++st.exact_elems;
-    bool more = false;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) more |= (candmin[kk] || candmax[kk]) && !known[kk];
-    pend = __ballot_sync(FULL, more);
-  }
-  {
-    // every lane takes part in the reduction; only undecided groups use its result
-    float mn = INFINITY, mx = -INFINITY;
+  };
+  for (int tier = 0; tier < 2 && __any_sync(FULL, uz || us); ++tier) {
+    evaluate(cand, tier);
+    float a0 = INFINITY, a1 = INFINITY, b0 = -INFINITY, b1 = -INFINITY;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      if (candmin[k]) mn = fminf(mn, xe[k]);
-      if (candmax[k]) mx = fmaxf(mx, xe[k]);
+      if (cmin[k]) { a0 = fminf(a0, lo[k]); a1 = fminf(a1, hi[k]); }
+      if (cmax[k]) { b0 = fmaxf(b0, lo[k]); b1 = fmaxf(b1, hi[k]); }
     }
-    for (int off = gl / 2; off > 0; off >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(FULL, mn, off));
-      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, off));
+    a0 = group_min(a0);
+    a1 = group_min(a1);
+    b0 = group_max(b0);
+    b1 = group_max(b1);
+    if (uz) {
+      const uint16_t z1 = zero_of(clip, a0);
+      if (z1 == zero_of(clip, a1) || tier == 1) { z = z1; uz = false; }
     }
-    if (!decided) {
-      z = zero_of(clip, mn);
-      s = scale_of(clip, mn, mx);
+    if (us) {
+      const uint16_t s1 = scale_of(clip, a1, b0);
+      if (s1 == scale_of(clip, a0, b1) || tier == 1) { s = s1; us = false; }
     }
-    st.exact_groups += __popc(__ballot_sync(FULL, !decided && (lane & (gl - 1)) == 0));
   }
   const float zf = bf16_to_f32(z), sf = bf16_to_f32(s);
   const bool valid = sf != 0.0f && isfinite(sf);
   int code[4];
-  bool need[4];
+  for (int tier = 0; tier < 3; ++tier) {
+    bool need[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (known[k]) {
-      code[k] = code_of(xe[k], zf, sf, valid);
-      need[k] = false;
-    } else {
-      code[k] = code_of(a[k], zf, sf, valid);
-      need[k] = code[k] != code_of(b[k], zf, sf, valid);
+    for (int k = 0; k < 4; ++k) {
+      code[k] = code_of(lo[k], zf, sf, valid);
+      need[k] = code[k] != code_of(hi[k], zf, sf, valid);
     }
-  }
-  pend = __ballot_sync(FULL, need[0] || need[1] || need[2] || need[3]);
-  while (pend) {
-    const int src = __ffs(pend) - 1;
-    uint32_t mymask = (need[0] ? 1u : 0u) | (need[1] ? 2u : 0u) | (need[2] ? 4u : 0u) | (need[3] ? 8u : 0u);
-    mymask = __shfl_sync(FULL, mymask, src);
-    const int k = __ffs(mymask) - 1;
-    const float v = exact_rot_elem(xs, R, 4 * src + k, unproven);
-    if (lane == src) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        if (kk == k) { code[kk] = code_of(v, zf, sf, valid); need[kk] = false; }
-    }
-    ++st.exact_elems;
-    pend = __ballot_sync(FULL, need[0] || need[1] || need[2] || need[3]);
+    if (tier == 2 || !__any_sync(FULL, need[0] || need[1] || need[2] || need[3])) break;
+    evaluate(need, tier);
   }
   if (__any_sync(FULL, unproven) && lane == 0) ++st.unproven;
   codes_out[lane] = (uint8_t)(code[0] | (code[1] << 2) | (code[2] << 4) | (code[3] << 6));
@@ -327,14 +332,6 @@ __device__ inline void quantize_from_dots(const float *xs, const float *R, const
     scale_out[lane / gl] = s;
     zero_out[lane / gl] = z;
   }
-}
-
-__device__ inline void rotate_quantize_warp(const float *xs, const float *R, float clip, int g,
-                                            uint8_t *codes_out, uint16_t *scale_out, uint16_t *zero_out,
-                                            QuantStats &st) {
-  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
-  rot_dot_rows(xs, R, 0, D, acc, sab);
-  quantize_from_dots(xs, R, acc, sab, clip, g, codes_out, scale_out, zero_out, st);
 }
 
 // Load one bf16 head vector (128 values, 8-byte aligned) into the warp's shared float32 buffer.

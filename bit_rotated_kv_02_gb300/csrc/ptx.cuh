@@ -8,6 +8,14 @@ namespace oscar {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while the previous kernel of the stream is still running; it must call pdl_wait() before touching
+// any global memory (the wait returns once the previous grid has completed and its writes are
+// visible).  pdl_trigger() lets the next kernel start launching early.  Both are no-ops for a kernel
+// launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }

@@ -6,6 +6,7 @@
 // recent stay BF16.
 #include "oscar_internal.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace oscar {
 
@@ -17,17 +18,38 @@ namespace oscar {
 // arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
 // mode 2: as mode 0, then append k_new/v_new.
-__global__ void __launch_bounds__(256) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
+__global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
                                                             const uint16_t *k_new, const uint16_t *v_new) {
   __shared__ float xs[2][D];
   __shared__ float pacc[8][32][4], psab[8][32][4];
   __shared__ int s_ok;
+  pdl_wait();
+  pdl_trigger();
   const int kvh = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kv = warp >> 2, part = warp & 3;  // kv 0 = K, 1 = V
+  // This warp's 32 rows of R, loaded before (and in parallel with) the pool counters they do not
+  // depend on: the dependent global reads of a demotion are its latency.
+  const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
+  float4 rrow[32];
+  {
+    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(32 * part) * (D / 4) + lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rrow[i] = R4[i * (D / 4)];
+  }
+  // the appended token's row (mode 2; warps 0 and 4), also independent of the counters
+  uint2 newrow = make_uint2(0u, 0u);
+  if (mode == 2 && part == 0)
+    newrow = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[lane];
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
-  bool demote = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
+  const bool want = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
+  // the oldest recent vector and the page-table entry are read together
+  uint2 xw = make_uint2(0u, 0u);
+  if (want && part == 0)
+    xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
+                                         (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D)[lane];
+  bool demote = want;
   int page = -1;
   if (demote) {
     const int pidx = hl / PAGE;
@@ -44,14 +66,18 @@ __global__ void __launch_bounds__(256) demote_append_kernel(PoolArgs p, const in
   }
   if (!counters_ok && threadIdx.x == 0) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
   // A demotion that cannot be stored leaves the whole sequence unchanged (no append either).
-  const bool blocked = counters_ok && !demote && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
+  const bool blocked = want && !demote;
   if (demote) {
-    const uint16_t *src = (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D;
-    const float *R = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
-    if (part == 0) load_vec_to_smem(src, xs[kv]);
+    const float *R = Rw;
+    if (part == 0) {
+      xs[kv][4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
+      xs[kv][4 * lane + 1] = bf16_to_f32(xw.x >> 16);
+      xs[kv][4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
+      xs[kv][4 * lane + 3] = bf16_to_f32(xw.y >> 16);
+    }
     __syncthreads();
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
-    rot_dot_32rows(xs[kv], R, 32 * part, acc, sab);
+    rot_dot_32rows_pre(xs[kv], rrow, 32 * part, acc, sab);
 #pragma unroll
     for (int k = 0; k < 4; ++k) { pacc[warp][lane][k] = acc[k]; psab[warp][lane][k] = sab[k]; }
     __syncthreads();
@@ -80,8 +106,7 @@ __global__ void __launch_bounds__(256) demote_append_kernel(PoolArgs p, const in
     } else {
       dst = (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + (nrs + nrl) % RECENT) * D;
     }
-    const size_t so = ((size_t)b * p.Hkv + kvh) * D;
-    reinterpret_cast<uint2 *>(dst)[lane] = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + so)[lane];
+    reinterpret_cast<uint2 *>(dst)[lane] = newrow;
   }
   if (append) {
     if (nslen < SINK && nhl == 0 && nrl == 0) nslen += 1;
@@ -127,9 +152,9 @@ __global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl)
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
                           const uint16_t *v_new, cudaStream_t s) {
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
-  demote_append_kernel<<<dim3(p.Hkv, p.B), 256, 0, s>>>(p, mask, mode, k_new, v_new);
+  const cudaError_t e = launch_pdl(demote_append_kernel, dim3(p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
