@@ -313,8 +313,7 @@ def other_workload(args):
             ws = torch.empty(ok.oscar_decode_workspace_size(P), dtype=torch.uint8, device="cuda")
 
             def step():
-                ok.oscar_append_kv(P, kn, vn)
-                ok.oscar_decode_attention(P, q, out=out, ws=ws)
+                ok.oscar_decode_step(P, kn, vn, q, out=out, ws=ws)
             ms = _time(step, steps, max(3, min(args.warmup, 20)))
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -431,9 +430,9 @@ def main():
             lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
             lib.oscar_profile_events(1, C.c_void_p(ev[2].cuda_event), C.c_void_p(ev[3].cuda_event))
         j = i % NQ
-        st = lib.oscar_append_kv(P.ref, C.c_void_p(kn[j].data_ptr()), C.c_void_p(vn[j].data_ptr()), sp)
-        st |= lib.oscar_decode_attention(P.ref, C.c_void_p(qs[j].data_ptr()), C.c_void_p(outs[l].data_ptr()),
-                                         scale, 0, C.c_void_p(ws.data_ptr()), ws_bytes, sp)
+        st = lib.oscar_decode_step(P.ref, C.c_void_p(kn[j].data_ptr()), C.c_void_p(vn[j].data_ptr()),
+                                   C.c_void_p(qs[j].data_ptr()), C.c_void_p(outs[l].data_ptr()), scale,
+                                   C.c_void_p(ws.data_ptr()), ws_bytes, sp)
         if st:
             raise RuntimeError(lib.oscar_last_error_string().decode())
         appended[l] += 1
@@ -488,8 +487,7 @@ def main():
     for i in range(args.e2e_steps):
         l = (base + i) % NL
         dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
-        ok.oscar_append_kv(layers[l], dk, dv)
-        ok.oscar_decode_attention(layers[l], dq, out=outs[l], num_splits=0, ws=ws)
+        ok.oscar_decode_step(layers[l], dk, dv, dq, out=outs[l], ws=ws)
         hout.copy_(outs[l], non_blocking=True)
         appended[l] += 1
         e2e_tokens += L_CTX + appended[l]
@@ -539,11 +537,12 @@ def main():
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3,
                          "timed_launches": len(hist_ms), "sampling": f"every {EVERY}th step of the timed region"},
             "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
-                       statistics.mean(dem_ms) * 1e3, "note": "append+demote kernel, 1 token x 8 KV heads x K/V per launch"},
+                       statistics.mean(dem_ms) * 1e3,
+                       "note": "append + demote + query rotation kernel, 1 token x 8 KV heads x K/V per launch"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 4,   # append/demote, q rotation, attention, merge
+            "gpu_launches": args.steps * 3,   # append + demote + q rotation, attention, merge
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -194,6 +194,20 @@ def oscar_decode_attention(pool: Pool, q, out=None, softmax_scale=None, num_spli
     return out
 
 
+def oscar_decode_step(pool: Pool, k_new, v_new, q, out=None, softmax_scale=None, ws=None, stream=None):
+    """One decode step (append k_new/v_new bf16 [B][Hkv][128], demote, attention of q bf16 [B][Hq][128]):
+    what oscar_append_kv then oscar_decode_attention give, in fewer launches.  Returns fp32 out."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (q, "q")):
+        _dev(t, torch.bfloat16, n)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    if ws is None:
+        ws = torch.empty(oscar_decode_workspace_size(pool, 0), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(pool.d) if softmax_scale is None else float(softmax_scale)
+    _lib.check(lib().oscar_decode_step(pool.ref, _p(k_new), _p(v_new), _p(q), _p(out), scale, _p(ws), ws.numel(),
+                                       _s(stream)), "oscar_decode_step")
+    return out
+
+
 def oscar_profile_events(which: int, start=None, stop=None):
     """Arm the timing hook: the next launch of kernel kind `which` on this thread records torch.cuda.Event
     `start` before and `stop` after that kernel (on the call's stream)."""

@@ -49,6 +49,7 @@ SIGNATURES = {
     "oscar_decode_attention": ([PP, P, P, F32, I32, P, SZ, P], C.c_int),
     "oscar_profile_events": ([I32, P, P], C.c_int),
     "oscar_decode_attention_noalloc": ([PP, P, P, F32, P], C.c_int),
+    "oscar_decode_step": ([PP, P, P, P, P, F32, P, SZ, P], C.c_int),
 }
 
 _LIB = None

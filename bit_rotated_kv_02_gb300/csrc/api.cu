@@ -248,4 +248,27 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
                      "decode_attention");
 }
 
+oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
+                                 const oscar_bf16 *q, float *out, float softmax_scale, void *ws, size_t ws_bytes,
+                                 oscar_stream_t stream) {
+  PoolArgs a;
+  oscar_status_t st = check_pool(pool, a);
+  if (st != OSCAR_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "k_new/v_new NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 7u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 8-byte aligned");
+  if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
+  if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  if (a.g != OSCAR_HEAD_DIM) {
+    if ((st = oscar_append_kv(pool, k_new, v_new, stream)) != OSCAR_OK) return st;
+    return oscar_decode_attention(pool, q, out, softmax_scale, 0, ws, ws_bytes, stream);
+  }
+  const size_t need = v1_ws_bytes(a);
+  if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws),
+                                    static_cast<cudaStream_t>(stream)),
+                     "decode_step");
+}
+
 }  // extern "C"

@@ -34,12 +34,12 @@ namespace oscar {
 
 namespace v1 {
 
-constexpr int NSTAGE = 4;
+constexpr int NSTAGE = 3;
 constexpr int PAGE_BYTES = 4608;   // Kc 2048 | Vc 2048 | Ks 128 | Kz 128 | Vs 128 | Vz 128
-constexpr int STAGE_PAGES = 2;     // a stage holds up to two consecutive pages of one segment
+constexpr int CONSUMER_WARPS = 4, THREADS = 160;
+constexpr int STAGE_PAGES = CONSUMER_WARPS;  // a stage holds up to one page of one segment per consumer warp
 constexpr int STAGE_BYTES = PAGE_BYTES * STAGE_PAGES;
 constexpr int OFF_KC = 0, OFF_VC = 2048, OFF_KS = 4096, OFF_KZ = 4224, OFF_VS = 4352, OFF_VZ = 4480;
-constexpr int CONSUMER_WARPS = 4, THREADS = 160;
 constexpr int LAZY = 16;           // rescale the running output only when the max grows by > 2^16
 constexpr int WEXP = 14 - LAZY;    // weights p * scale * 2^tau < 2^14 with tau = WEXP - e, scale < 2^e
 
@@ -390,27 +390,34 @@ __device__ __forceinline__ void flush(const Args &a, Smem<G> &sm, WarpState<G> &
   reset(ws);
 }
 
-// One stage: tile `warp` (rows 16*warp .. +15) of each of the stage's pages; ntok[pg] = valid tokens
-// of page pg (0 when the page is absent or could not be loaded).  FULLP: both pages are full.
-template <int G, bool FULLP>
-__device__ __forceinline__ void stage_pass(const uint8_t *st, const int (&ntok)[STAGE_PAGES], const Smem<G> &sm,
-                                           WarpState<G> &ws, const uint32_t (&bq)[Smem<G>::NT][8][2]) {
+// 8x8 transpose of a matrix of 16-bit values held one 32-bit pair per lane in the mma fragment
+// layout (lane (g, t) holds row g, columns 2t and 2t+1); the result is in the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// One page in one consumer warp: all 64 tokens (four 16-token tiles); ntok = valid tokens (1..64).
+// Lane (g, t) owns the rows g + 8j (j = 0..7: tile j/2, row half j%2) of the QK accumulators for head
+// column t; the softmax weights are formed in that layout, split into fp16 hi + lo and transposed
+// with movmatrix into the B operand of the P.V products, whose A operand pairs tokens (2t, 2t+1).
+template <int G, bool FULL>
+__device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, const Smem<G> &sm, WarpState<G> &ws,
+                                          const uint32_t (&bq)[Smem<G>::NT][8][2]) {
   constexpr int NT = Smem<G>::NT;
   constexpr bool ALL_LIVE = (G % 4) == 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
-  const int r0 = 16 * warp + gq, r1 = r0 + 8;
-  bool has[STAGE_PAGES];
-  float S[STAGE_PAGES][NT][4];
-  // ---- QK for both tiles: A = K codes (tokens r0, r1; lane t owns channels 32t .. 32t+31) ----
+  const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+  // ---- QK: A = K codes (tokens 16mt + g, 16mt + g + 8; lane t owns channels 32t .. 32t+31) ----
+  float S[4][NT][4];
+  const uint8_t *kc = pb + OFF_KC + gq * 32 + 8 * t;
 #pragma unroll
-  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
-    has[pg] = FULLP || ntok[pg] > 16 * warp;
+  for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) S[pg][nt][0] = S[pg][nt][1] = S[pg][nt][2] = S[pg][nt][3] = 0.f;
-    if (has[pg]) {
-      const uint8_t *kc = st + pg * PAGE_BYTES + OFF_KC;
-      const uint2 ka = *reinterpret_cast<const uint2 *>(kc + r0 * 32 + 8 * t);
-      const uint2 kb = *reinterpret_cast<const uint2 *>(kc + r1 * 32 + 8 * t);
+    for (int nt = 0; nt < NT; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
+    if (FULL || 16 * mt < ntok) {
+      const uint2 ka = *reinterpret_cast<const uint2 *>(kc + (16 * mt) * 32);
+      const uint2 kb = *reinterpret_cast<const uint2 *>(kc + (16 * mt + 8) * 32);
       uint32_t T0[16], T1[16];
       unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
       unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
@@ -418,80 +425,28 @@ __device__ __forceinline__ void stage_pass(const uint8_t *st, const int (&ntok)[
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          mma16816(S[pg][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+          mma16816(S[mt][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
     }
   }
-  // ---- scores and lazily rescaled online softmax over both tiles ----
-  float sc[STAGE_PAGES][2][NT], vz[STAGE_PAGES][2];
-  bool vld[STAGE_PAGES][2];
+  // ---- per-row scale / zero of the lane's 8 rows ----
+  const uint16_t *Ks = reinterpret_cast<const uint16_t *>(pb + OFF_KS) + gq;
+  const uint16_t *Kz = reinterpret_cast<const uint16_t *>(pb + OFF_KZ) + gq;
+  const uint16_t *Vs = reinterpret_cast<const uint16_t *>(pb + OFF_VS) + gq;
+  const uint16_t *Vz = reinterpret_cast<const uint16_t *>(pb + OFF_VZ) + gq;
+  float ks[8], kz[8], vs[8], vz[8];
 #pragma unroll
-  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
-    const uint8_t *pb = st + pg * PAGE_BYTES;
-    const uint16_t *Ks = reinterpret_cast<const uint16_t *>(pb + OFF_KS);
-    const uint16_t *Kz = reinterpret_cast<const uint16_t *>(pb + OFF_KZ);
-    const uint16_t *Vz = reinterpret_cast<const uint16_t *>(pb + OFF_VZ);
-    vld[pg][0] = FULLP || r0 < ntok[pg];
-    vld[pg][1] = FULLP || r1 < ntok[pg];
-    const float ks[2] = {bf16_to_f32(Ks[r0]), bf16_to_f32(Ks[r1])};
-    const float kz[2] = {bf16_to_f32(Kz[r0]), bf16_to_f32(Kz[r1])};
-    vz[pg][0] = vld[pg][0] ? bf16_to_f32(Vz[r0]) : 0.f;
-    vz[pg][1] = vld[pg][1] ? bf16_to_f32(Vz[r1]) : 0.f;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int h = ALL_LIVE ? 4 * nt + t : min(4 * nt + t, G - 1);
-      const float kf = sm.kfac[h], zf = sm.zfac[h];
-#pragma unroll
-      for (int e = 0; e < 2; ++e)
-        sc[pg][e][nt] = vld[pg][e] ? fmaf((S[pg][nt][2 * e] + S[pg][nt][2 * e + 1]) * ks[e], kf, kz[e] * zf) : -INFINITY;
-    }
+  for (int j = 0; j < 8; ++j) {
+    const bool valid = FULL || gq + 8 * j < ntok;
+    ks[j] = bf16_to_f32(Ks[8 * j]);
+    kz[j] = bf16_to_f32(Kz[8 * j]);
+    vs[j] = valid ? bf16_to_f32(Vs[8 * j]) : 0.f;
+    vz[j] = valid ? bf16_to_f32(Vz[8 * j]) : 0.f;
   }
-  float P[STAGE_PAGES][2][NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    float tmax = fmaxf(fmaxf(sc[0][0][nt], sc[0][1][nt]), fmaxf(sc[1][0][nt], sc[1][1][nt]));
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, o));
-    if (tmax > ws.m2[nt] + (float)LAZY) {
-      const float alpha = (ws.m2[nt] == -INFINITY) ? 0.f : fast_exp2(ws.m2[nt] - tmax);
-      ws.l[nt] *= alpha;
-      ws.oz[nt] *= alpha;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) ws.O[nt][mt][r] *= alpha;
-      ws.m2[nt] = tmax;
-    }
-    const float m = ws.m2[nt];
-    const bool live = FULLP || m != -INFINITY;
-    float lsum = 0.f, zsum = 0.f;
-#pragma unroll
-    for (int pg = 0; pg < STAGE_PAGES; ++pg)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float pr = (live && vld[pg][e]) ? fast_exp2(sc[pg][e][nt] - m) : 0.f;
-        P[pg][e][nt] = pr;
-        lsum += pr;
-        zsum = fmaf(pr, vz[pg][e], zsum);
-      }
-    ws.l[nt] += lsum;
-    ws.oz[nt] += zsum;
-  }
-  // ---- weight scaling exponent from the V scales of both tiles (tokens t, t+4, t+8, t+12) ----
-  const int rb = 16 * warp;
-  float vs[STAGE_PAGES][4];
-  float vmax = 0.f;
-#pragma unroll
-  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
-    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(st + pg * PAGE_BYTES + OFF_VS);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int r = rb + t + 4 * e;
-      vs[pg][e] = (FULLP || r < ntok[pg]) ? bf16_to_f32(Vs[r]) : 0.f;
-      vmax = fmaxf(vmax, vs[pg][e]);
-    }
-  }
-  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 1));
-  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 2));
+  // ---- weight scaling exponent tau: weights p * vs * 2^tau stay below 2^14 ----
+  float vmax = fmaxf(max3f(vs[0], vs[1], vs[2]), max3f(max3f(vs[3], vs[4], vs[5]), vs[6], vs[7]));
+  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 4));
+  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 8));
+  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 16));
   if (vmax >= ws.tau_lim && vmax > 0.f) {
     int e;
     frexpf(vmax, &e);
@@ -501,47 +456,78 @@ __device__ __forceinline__ void stage_pass(const uint8_t *st, const int (&ntok)[
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
+        for (int m8 = 0; m8 < 8; ++m8)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) ws.O[nt][mt][r] *= f;
+          for (int r = 0; r < 4; ++r) ws.O[nt][m8][r] *= f;
     }
     if (ws.tau_lim == 0.f || tnew < ws.tau) ws.tau = tnew;
     ws.tau_lim = pow2f(WEXP - ws.tau);
   }
-  const float tscale = pow2f(ws.tau);
-  // ---- P·V for each tile: A = V codes^T (lane g owns channels 16g .. 16g+15), B = split weights ----
-  const int hcol = gq >> 1;
-  const bool lo_split = (gq & 1) != 0;
-  const int srcA = 4 * t + hcol, srcB = 4 * (t + 4) + hcol;
+  const float untau = pow2f(-ws.tau);
+  // ---- scores, lazily rescaled online softmax, weights ----
+  uint32_t bw[NT][4][2];
 #pragma unroll
-  for (int pg = 0; pg < STAGE_PAGES; ++pg) {
-    if (!has[pg]) continue;
-    uint32_t bw[NT][2];
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = ALL_LIVE ? 4 * nt + t : min(4 * nt + t, G - 1);
+    const bool live_h = ALL_LIVE || 4 * nt + t < G;
+    const float kf = sm.kfac[h], zf = sm.zfac[h];
+    float sc[8];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const float p0 = P[pg][0][nt] * tscale, p1 = P[pg][1][nt] * tscale;
-      const float pa = __shfl_sync(FULL, p0, srcA), pc = __shfl_sync(FULL, p1, srcA);
-      const float pb = __shfl_sync(FULL, p0, srcB), pd = __shfl_sync(FULL, p1, srcB);
-      const bool live = ALL_LIVE || (4 * nt + hcol < G);
-      const float w0 = live ? pa * vs[pg][0] : 0.f, w1 = live ? pb * vs[pg][1] : 0.f;
-      const float w2 = live ? pc * vs[pg][2] : 0.f, w3 = live ? pd * vs[pg][3] : 0.f;
-      const uint32_t h01 = pack_half2(w0, w1), h23 = pack_half2(w2, w3);
-      const float2 f01 = unpack_half2(h01), f23 = unpack_half2(h23);
-      const uint32_t l01 = pack_half2(w0 - f01.x, w1 - f01.y), l23 = pack_half2(w2 - f23.x, w3 - f23.y);
-      bw[nt][0] = lo_split ? l01 : h01;
-      bw[nt][1] = lo_split ? l23 : h23;
+    for (int j = 0; j < 8; ++j) {
+      const int mt = j >> 1, e = j & 1;
+      sc[j] = (FULL || gq + 8 * j < ntok) ? fmaf((S[mt][nt][2 * e] + S[mt][nt][2 * e + 1]) * ks[j], kf, kz[j] * zf)
+                                          : -INFINITY;
     }
-    const uint32_t *vrow = reinterpret_cast<const uint32_t *>(st + pg * PAGE_BYTES + OFF_VC);
-    const uint32_t xa = vrow[(rb + t) * 8 + gq], xb = vrow[(rb + t + 4) * 8 + gq];
-    const uint32_t xc = vrow[(rb + t + 8) * 8 + gq], xd = vrow[(rb + t + 12) * 8 + gq];
+    float tmax = fmaxf(max3f(sc[0], sc[1], sc[2]), max3f(max3f(sc[3], sc[4], sc[5]), sc[6], sc[7]));
+    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 4));
+    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 8));
+    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 16));
+    if (tmax > ws.m2[nt] + (float)LAZY) {
+      const float alpha = (ws.m2[nt] == -INFINITY) ? 0.f : fast_exp2(ws.m2[nt] - tmax);
+      ws.l[nt] *= alpha;
+      ws.oz[nt] *= alpha;
+#pragma unroll
+      for (int m8 = 0; m8 < 8; ++m8)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) ws.O[nt][m8][r] *= alpha;
+      ws.m2[nt] = tmax;
+    }
+    // p * 2^tau = exp2(score - (m - tau)); l and the zero-point sum take p itself
+    const float mref = ws.m2[nt] - (float)ws.tau;
+    float lsum = 0.f, zsum = 0.f;
+    uint32_t wp[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float pr = fast_exp2(sc[j] - mref);  // 0 for rows past ntok (score -inf)
+      lsum += pr;
+      zsum = fmaf(pr, vz[j], zsum);
+      const float w = live_h ? pr * vs[j] : 0.f;
+      const __half hh = __float2half_rn(w);
+      wp[j] = pack_half2(__half2float(hh), w - __half2float(hh));  // (hi, lo)
+    }
+    ws.l[nt] = fmaf(lsum, untau, ws.l[nt]);
+    ws.oz[nt] = fmaf(zsum, untau, ws.oz[nt]);
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      bw[nt][mt][0] = movmatrix_trans(wp[2 * mt]);
+      bw[nt][mt][1] = movmatrix_trans(wp[2 * mt + 1]);
+    }
+  }
+  // ---- P.V per tile: A = V codes^T (tokens 2t, 2t+1 | 2t+8, 2t+9; group g: channels 16g .. 16g+15) ----
+  const uint32_t *vrow = reinterpret_cast<const uint32_t *>(pb + OFF_VC) + gq + 2 * t * 8;
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    if (!(FULL || 16 * mt < ntok)) continue;
+    const uint32_t *vr = vrow + 16 * mt * 8;
+    const uint32_t xa = vr[0], xb = vr[8], xc = vr[64], xd = vr[72];
     uint32_t VA[16], VB[16];
     unpack16(prmt(xa, xb, 0x5410), VA, 0); unpack16(prmt(xa, xb, 0x7632), VA, 8);
     unpack16(prmt(xc, xd, 0x5410), VB, 0); unpack16(prmt(xc, xd, 0x7632), VB, 8);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-        mma16816(ws.O[nt][mt], VA[2 * mt], VA[2 * mt + 1], VB[2 * mt], VB[2 * mt + 1], bw[nt][0], bw[nt][1]);
+      for (int m8 = 0; m8 < 8; ++m8)
+        mma16816(ws.O[nt][m8], VA[2 * m8], VA[2 * m8 + 1], VB[2 * m8], VB[2 * m8 + 1], bw[nt][mt][0], bw[nt][mt][1]);
   }
 }
 
@@ -569,74 +555,80 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   if (n <= 0) return;
 
   if (warp == CONSUMER_WARPS) {
-    // ---------------- producer: up to two pages of one segment per stage ----------------
-    if (lane == 0) {
-      int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
-      int np = npages_of(p, b);
-      int stage = 0, it = 0;
-      uint32_t phase = 0;
-      long long done = 0;
-      while (done < n) {
-        bool abort = false;
-        if (it >= NSTAGE && !mbar_wait_bounded(&sm.empty[stage], phase ^ 1)) {
-          atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
-          abort = true;
+    // ---------------- producer warp: up to STAGE_PAGES pages of one segment per stage ----------------
+    // Lane i owns page i of a stage: the page-table entries of a stage are read in one round trip and
+    // each lane issues its own page's bulk copies.  hist_len is read once per sequence.
+    int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
+    int np = npages_of(p, b);
+    int hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+    int stage = 0, it = 0;
+    uint32_t phase = 0;
+    long long done = 0;
+    while (done < n) {
+      bool abort = false;
+      if (it >= NSTAGE) {
+        bool okw = true;
+        if (lane == 0) okw = mbar_wait_bounded(&sm.empty[stage], phase ^ 1);
+        abort = !__shfl_sync(FULL, okw, 0);
+        if (abort && lane == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
+      }
+      const int seg = b * p.Hkv + kvh;
+      const int cnt = abort ? 0 : (int)min((long long)STAGE_PAGES, min(n - done, (long long)(np - local)));
+      int pp = -1, ntk = 0;
+      if (lane < cnt) {
+        const int lp = local + lane;
+        pp = p.page_table[(size_t)b * p.max_pages + lp];
+        ntk = min(PAGE, hl - lp * PAGE);
+        if (pp < 0 || pp >= p.num_pages) {
+          atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
+          pp = -1;
         }
-        const int seg = b * p.Hkv + kvh;
-        const int hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
-        int bytes = 0, pages = 0;
-        int ntk[STAGE_PAGES] = {0, 0};
-        int phys[STAGE_PAGES] = {-1, -1};
-        while (!abort && pages < STAGE_PAGES && done < n && b * p.Hkv + kvh == seg) {
-          const int pp = p.page_table[(size_t)b * p.max_pages + local];
-          if (pp >= 0 && pp < p.num_pages) {
-            phys[pages] = pp;
-            ntk[pages] = min(PAGE, hl - local * PAGE);
-            bytes += PAGE_BYTES;
-          } else {
-            atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
-          }
-          ++pages;
-          ++done;
-          if (++local == np) {
-            local = 0;
-            if (++kvh == p.Hkv) {
-              kvh = 0;
-              do { ++b; } while (b < p.B && npages_of(p, b) == 0);
-              if (b < p.B) np = npages_of(p, b);
-            }
-          }
-        }
+      }
+      const bool have = pp >= 0;
+      const int bytes = __popc(__ballot_sync(FULL, have)) * PAGE_BYTES;
+      if (lane < STAGE_PAGES) sm.meta_ntok[stage][lane] = have ? ntk : 0;
+      if (lane == 0) {
         sm.meta_seg[stage] = seg;
-        sm.meta_ntok[stage][0] = ntk[0];
-        sm.meta_ntok[stage][1] = ntk[1];
-        sm.meta_flags[stage] = (done >= n ? 1 : 0) | (abort ? 2 : 0);
-        if (bytes > 0) {
-          mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)bytes);
-#pragma unroll
-          for (int pg = 0; pg < STAGE_PAGES; ++pg) {
-            if (phys[pg] < 0) continue;
-            uint8_t *dst = sm.ring[stage] + pg * PAGE_BYTES;
-            const size_t row = ((size_t)phys[pg] * p.Hkv + (seg % p.Hkv)) * PAGE;
-            bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, &sm.full[stage]);
-            bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, &sm.full[stage]);
-            bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, &sm.full[stage]);
-            bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, &sm.full[stage]);
-            bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, &sm.full[stage]);
-            bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, &sm.full[stage]);
-          }
-        } else {
-          mbar_arrive(&sm.full[stage]);
-        }
-        if (abort) {
-          // wait (bounded) for the copies still in flight into stages the consumers may not read
+        sm.meta_flags[stage] = (done + cnt >= n ? 1 : 0) | (abort ? 2 : 0);
+      }
+      __syncwarp();  // the stage's metadata is written before its barrier phase can complete
+      if (lane == 0) {
+        if (bytes > 0) mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)bytes);
+        else mbar_arrive(&sm.full[stage]);
+      }
+      __syncwarp();
+      if (have) {
+        uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
+        const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
+        bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, &sm.full[stage]);
+        bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, &sm.full[stage]);
+        bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, &sm.full[stage]);
+        bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, &sm.full[stage]);
+        bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, &sm.full[stage]);
+        bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, &sm.full[stage]);
+      }
+      if (abort) {
+        // wait (bounded) for the copies still in flight into stages the consumers may not read
+        if (lane == 0)
           for (int k = max(0, it - NSTAGE + 1); k < it; ++k)
             mbar_wait_bounded(&sm.full[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
-          break;
-        }
-        ++it;
-        if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
+        break;
       }
+      done += cnt;
+      local += cnt;
+      if (local == np && done < n) {
+        local = 0;
+        if (++kvh == p.Hkv) {
+          kvh = 0;
+          do { ++b; } while (b < p.B && npages_of(p, b) == 0);
+          if (b < p.B) {
+            np = npages_of(p, b);
+            hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+          }
+        }
+      }
+      ++it;
+      if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
     }
     return;
   }
@@ -659,9 +651,10 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
       cur = seg;
       setup_segment(a, sm, seg / p.Hkv, seg % p.Hkv, bq);
     }
-    const int ntok[STAGE_PAGES] = {sm.meta_ntok[stage][0], sm.meta_ntok[stage][1]};
-    if (ntok[0] == PAGE && ntok[1] == PAGE) stage_pass<G, true>(sm.ring[stage], ntok, sm, ws, bq);
-    else stage_pass<G, false>(sm.ring[stage], ntok, sm, ws, bq);
+    const int ntok = sm.meta_ntok[stage][warp];
+    const uint8_t *pb = sm.ring[stage] + warp * PAGE_BYTES;
+    if (ntok == PAGE) page_pass<G, true>(pb, ntok, sm, ws, bq);
+    else if (ntok > 0) page_pass<G, false>(pb, ntok, sm, ws, bq);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
     if (flags & 1) break;
@@ -851,9 +844,11 @@ size_t v1_ws_bytes(const PoolArgs &p) {
   return (size_t)p.B * p.Hq * D * sizeof(float) + slots * G * PART_STRIDE * sizeof(float);
 }
 
+// k_new != NULL: the step form (append + demote + query rotation fused in the demote kernel);
+// otherwise the query rotation runs as its own kernel.
 template <int G>
 static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
-                               cudaStream_t s) {
+                               cudaStream_t s, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr) {
   v1::Args a;
   a.p = p;
   a.q = q;
@@ -866,7 +861,11 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   const int smem = (int)sizeof(v1::Smem<G>);
   cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws)) != cudaSuccess) return e;
+  if (k_new != nullptr) {
+    if ((e = launch_demote(p, nullptr, 2, k_new, v_new, s, q, ws)) != cudaSuccess) return e;
+  } else if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws)) != cudaSuccess) {
+    return e;
+  }
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
@@ -881,6 +880,17 @@ cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, f
     case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s);
     case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s);
     case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
+                           float *out, float sm_scale, float *ws, cudaStream_t s) {
+  switch (p.Hq / p.Hkv) {
+    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s, k_new, v_new);
+    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s, k_new, v_new);
+    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s, k_new, v_new);
+    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s, k_new, v_new);
     default: return cudaErrorInvalidValue;
   }
 }

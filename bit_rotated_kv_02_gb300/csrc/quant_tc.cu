@@ -97,27 +97,6 @@ __device__ __forceinline__ void two_sum_f(float a, float b, float &s, float &e) 
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
 }
 
-// Three-input float32 min / max (NaN inputs are ignored), max of absolute values, saturating FMA.
-__device__ __forceinline__ float min3f(float a, float b, float c) {
-  float d;
-  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float max3abs(float a, float b, float c) {
-  float d;
-  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_sat(float a, float b, float c) {
-  float d;
-  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
 // (s0, s1) += (lo^2, hi^2) of the two bf16 values packed in w (one paired float32 FMA).
 __device__ __forceinline__ void sq2_acc(float &s0, float &s1, uint32_t w) {
   const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);

@@ -17,11 +17,17 @@ namespace oscar {
 // CTA reads the sequence's counters before any CTA of that sequence can change them: the last CTA to
 // arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
-// mode 2: as mode 0, then append k_new/v_new.
+// mode 2: as mode 0, then append k_new/v_new.  With q != NULL the CTA also writes the rotated queries
+// q_rot = q . R_k of its KV head's query heads (the decode step's query rotation, fused here because
+// this CTA already holds R_k in registers).
 __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
-                                                            const uint16_t *k_new, const uint16_t *v_new) {
+                                                            const uint16_t *k_new, const uint16_t *v_new,
+                                                            const uint16_t *q, float *qrot) {
+  constexpr int GMAX = 8;
   __shared__ float xs[2][D];
   __shared__ float pacc[8][32][4], psab[8][32][4];
+  __shared__ float qsm[GMAX][D];
+  __shared__ float4 qpart[4][GMAX][32];
   __shared__ int s_ok;
   pdl_wait();
   pdl_trigger();
@@ -41,6 +47,11 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   uint2 newrow = make_uint2(0u, 0u);
   if (mode == 2 && part == 0)
     newrow = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[lane];
+  // fused query rotation (q != NULL): q of the G query heads of this KV head, staged for warps 0-3
+  const int G = p.Hq / p.Hkv;
+  if (q != nullptr && kv == 0)
+    for (int i = threadIdx.x; i < G * D; i += 128)
+      qsm[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + (size_t)kvh * G) * D + i]);
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
   const bool want = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
@@ -96,6 +107,32 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
+  if (q != nullptr) {
+    // q_rot[h] = q[h] . R_k: warp `part` of the K half sums its 32 rows of R_k (already in registers)
+    if (kv == 0) {
+      for (int h = 0; h < G; ++h) {
+        float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float qi = qsm[h][32 * part + i];
+          acc4.x = fmaf(qi, rrow[i].x, acc4.x);
+          acc4.y = fmaf(qi, rrow[i].y, acc4.y);
+          acc4.z = fmaf(qi, rrow[i].z, acc4.z);
+          acc4.w = fmaf(qi, rrow[i].w, acc4.w);
+        }
+        qpart[part][h][lane] = acc4;
+      }
+    }
+    __syncthreads();
+    if (kv == 0) {
+      for (int h = part; h < G; h += 4) {
+        const float4 a0 = qpart[0][h][lane], a1 = qpart[1][h][lane], a2 = qpart[2][h][lane], a3 = qpart[3][h][lane];
+        reinterpret_cast<float4 *>(qrot + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D)[lane] =
+            make_float4(((a0.x + a1.x) + a2.x) + a3.x, ((a0.y + a1.y) + a2.y) + a3.y, ((a0.z + a1.z) + a2.z) + a3.z,
+                        ((a0.w + a1.w) + a2.w) + a3.w);
+      }
+    }
+  }
   const bool append = mode == 2 && counters_ok && !blocked;
   int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
   if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
@@ -150,9 +187,10 @@ __global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl)
 
 // ---- launchers ------------------------------------------------------------------------------
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
-                          const uint16_t *v_new, cudaStream_t s) {
+                          const uint16_t *v_new, cudaStream_t s, const uint16_t *q, float *qrot) {
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
-  const cudaError_t e = launch_pdl(demote_append_kernel, dim3(p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new);
+  const cudaError_t e =
+      launch_pdl(demote_append_kernel, dim3(p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new, q, qrot);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
   return e;
 }

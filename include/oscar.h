@@ -209,6 +209,20 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
                                       int32_t num_splits, void *ws, size_t ws_bytes, oscar_stream_t stream);
 
 /*
+ * One decode step: oscar_append_kv(pool, k_new, v_new) followed by oscar_decode_attention(pool, q,
+ * out, softmax_scale, 0, ws, ws_bytes), with the same results ("OSCAR 的设计": the new token enters
+ * the recent window, the oldest recent token is demoted into the INT2 history, then attention runs
+ * over the three segments).  With group size 128 the demotion, the append and the query rotation
+ * share one launch (the demotion already reads R_k); other group sizes run the two calls in turn.
+ *   k_new, v_new   bf16 [batch][Hkv][d] (8-byte aligned); q bf16 [batch][Hq][d] (16-byte aligned)
+ *   ws, ws_bytes   at least oscar_decode_workspace_size(pool, 0) bytes
+ * Errors as for the two calls; all checks run before any launch.
+ */
+oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
+                                 const oscar_bf16 *q, float *out, float softmax_scale, void *ws, size_t ws_bytes,
+                                 oscar_stream_t stream);
+
+/*
  * Kernel timing hook (measurement support; no counterpart on the pages).  Arms the calling thread so
  * that its next call that launches the kernel of kind `which` records cudaEvent_t `start` on the call's
  * stream immediately before that kernel and `stop` immediately after it, then disarms.

@@ -89,6 +89,32 @@ def test_decode_after_appends():
     helpers.assert_pools_equal(O, P)
 
 
+@pytest.mark.parametrize("G,g", [(4, 128), (8, 128), (2, 32)])
+def test_decode_step_matches_oracle_and_separate_calls(G, g):
+    """oscar_decode_step (append + demote + query rotation fused for group 128) gives the oracle's result
+    at every step, and exactly what oscar_append_kv followed by oscar_decode_attention gives."""
+    seed, Hkv = 640 + G + g, 2
+    Hq = G * Hkv
+    O, P, q = _setup([330, 1100], Hq, Hkv, g, seed, extra_pages=2)
+    _, P2, _ = _setup([330, 1100], Hq, Hkv, g, seed, extra_pages=2)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for t in range(20):
+        kn = synth.outlier_kv(seed + 2000 + t, 2, Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, 2, Hkv, 128, ch)
+        qt = synth.outlier_q(seed + 4000 + t, 2, Hq, Hkv, 128, ch)
+        O.append(kn, vn)
+        kd, vd, qd = helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn), helpers.to_dev_bf16(qt)
+        out = ok.oscar_decode_step(P, kd, vd, qd)
+        ok.oscar_append_kv(P2, kd, vd)
+        out2 = ok.oscar_decode_attention(P2, qd)
+        assert torch.equal(out, out2)
+        if t % 7 == 0:
+            helpers.assert_attention_close(out.cpu().numpy(), O.decode(qt))
+    torch.cuda.synchronize()
+    helpers.assert_pools_equal(O, P)
+    assert P.err() == 0
+
+
 def test_100k_context_sampled_heads():
     """Qwen3-8B layer shapes at 100k context: 99,680 history tokens on a shuffled page table (partial
     last page); the oracle rebuilds KV heads 0 and 5 and checks their 8 query heads."""
