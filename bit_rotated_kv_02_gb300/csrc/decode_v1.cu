@@ -105,6 +105,53 @@ __device__ void locate(const PoolArgs &p, long long start, int &b0, int &kvh0, i
   total = run;
 }
 
+// This CTA's share of the flattened (sequence, KV head, page) space: pages [lo, lo + n) with
+// chunk = ceil(total / n_hist), lo = cta * chunk, and the position (b0, kvh0, local0) of page lo plus
+// the page count np0 and history length hl0 of sequence b0.  Run by one full warp; results valid in
+// every lane.  Up to 32 sequences one load of hist_len per lane serves everything.
+__device__ void locate_range(const PoolArgs &p, int n_hist, int cta, long long &lo, long long &n, int &b0, int &kvh0,
+                             int &local0, int &np0, int &hl0) {
+  const int lane = threadIdx.x & 31;
+  b0 = 0; kvh0 = 0; local0 = 0; np0 = 0; hl0 = 0;
+  if (p.B <= 32) {
+    const int hl = lane < p.B ? max(0, min(p.hist_len[lane], p.max_pages * PAGE)) : 0;
+    const int np = (hl + PAGE - 1) / PAGE;
+    const long long v = (long long)np * p.Hkv;
+    long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const long long total = __shfl_sync(FULL, inc, 31);
+    const long long chunk = (total + n_hist - 1) / n_hist;
+    lo = (long long)cta * chunk;
+    n = max(0ll, min(total, lo + chunk) - lo);
+    const long long excl = inc - v;
+    const unsigned hit = __ballot_sync(FULL, v > 0 && lo >= excl && lo < excl + v);
+    if (n > 0 && hit) {
+      const int src = __ffs(hit) - 1;
+      const long long e = __shfl_sync(FULL, excl, src);
+      np0 = __shfl_sync(FULL, np, src);
+      hl0 = __shfl_sync(FULL, hl, src);
+      b0 = src;
+      kvh0 = (int)((lo - e) / np0);
+      local0 = (int)((lo - e) % np0);
+    }
+    return;
+  }
+  long long total;
+  locate(p, 0, b0, kvh0, local0, total);  // total only
+  const long long chunk = (total + n_hist - 1) / n_hist;
+  lo = (long long)cta * chunk;
+  n = max(0ll, min(total, lo + chunk) - lo);
+  if (n > 0) {
+    locate(p, lo, b0, kvh0, local0, total);
+    np0 = npages_of(p, b0);
+    hl0 = max(0, min(p.hist_len[b0], p.max_pages * PAGE));
+  }
+}
+
 template <int G>
 struct Smem {
   static constexpr int NT = (2 * G + 7) / 8;
@@ -118,7 +165,7 @@ struct Smem {
   float wo[CONSUMER_WARPS][G][D];
   float pbuf[CONSUMER_WARPS][G][16];
   long long range_lo, range_n;
-  int b0, kvh0, local0;
+  int b0, kvh0, local0, np0, hl0;
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -541,14 +588,12 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     mbar_fence_init();
   }
   if (warp == CONSUMER_WARPS) {  // the producer warp locates this CTA's range
-    long long total;
-    int b0, kvh0, local0;
-    locate(p, 0, b0, kvh0, local0, total);  // total only
-    const long long chunk = (total + a.n_hist - 1) / a.n_hist;
-    const long long lo = (long long)cta * chunk;
-    const long long n = max(0ll, min(total, lo + chunk) - lo);
-    if (n > 0) locate(p, lo, b0, kvh0, local0, total);
-    if (lane == 0) { sm.range_lo = lo; sm.range_n = n; sm.b0 = b0; sm.kvh0 = kvh0; sm.local0 = local0; }
+    long long lo, n;
+    int b0, kvh0, local0, np0, hl0;
+    locate_range(p, a.n_hist, cta, lo, n, b0, kvh0, local0, np0, hl0);
+    if (lane == 0) {
+      sm.range_lo = lo; sm.range_n = n; sm.b0 = b0; sm.kvh0 = kvh0; sm.local0 = local0; sm.np0 = np0; sm.hl0 = hl0;
+    }
   }
   __syncthreads();
   const long long n = sm.range_n;
@@ -559,8 +604,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     // Lane i owns page i of a stage: the page-table entries of a stage are read in one round trip and
     // each lane issues its own page's bulk copies.  hist_len is read once per sequence.
     int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
-    int np = npages_of(p, b);
-    int hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+    int np = sm.np0, hl = sm.hl0;
     int stage = 0, it = 0;
     uint32_t phase = 0;
     long long done = 0;
@@ -636,7 +680,9 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   WarpState<G> ws;
   reset(ws);
   uint32_t bq[NT][8][2];
-  int cur = -1, stage = 0;
+  // the first segment's query setup needs no pages: it overlaps the first bulk copies
+  int cur = sm.b0 * p.Hkv + sm.kvh0, stage = 0;
+  setup_segment(a, sm, sm.b0, sm.kvh0, bq);
   uint32_t phase = 0;
   while (true) {
     if (!mbar_wait_bounded(&sm.full[stage], phase)) {
