@@ -156,7 +156,8 @@ template <int G>
 struct Smem {
   static constexpr int NT = (2 * G + 7) / 8;
   alignas(128) uint8_t ring[NSTAGE][STAGE_BYTES];
-  uint64_t full[NSTAGE], empty[NSTAGE];
+  uint64_t full[NSTAGE][STAGE_PAGES], empty[NSTAGE][STAGE_PAGES];  // one pair per page slot
+  uint64_t csync;                                                    // consumer-warp barrier
   int meta_seg[NSTAGE], meta_ntok[NSTAGE][STAGE_PAGES], meta_flags[NSTAGE];  // flags: 1 last, 2 abort
   float qr[G][D];
   float kfac[G], zfac[G];
@@ -313,7 +314,20 @@ struct WarpState {
   float O[NT][8][4];
   int tau;        // weight scaling exponent (o accumulates in units of 2^-24 * 2^-tau per code step)
   float tau_lim;  // largest V scale the current tau admits (0 until the first non-zero scale)
+  uint32_t csync_par;  // phase parity of the consumer barrier
 };
+
+// Barrier among the consumer warps: an mbarrier counting one arrival per warp, waited with a time
+// limit, so that no thread can wait forever when a warp has left the pipeline after a timeout (the
+// error bit is set and the results of the launch are not valid).
+template <int G>
+__device__ __forceinline__ void consumer_sync(Smem<G> &sm, uint32_t &par, uint32_t *err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&sm.csync);
+  const bool ok = __all_sync(FULL, mbar_wait_bounded(&sm.csync, par));
+  par ^= 1u;
+  if (!ok && (threadIdx.x & 31) == 0) atomicOr(err, OSCAR_DEVERR_TIMEOUT);
+}
 
 template <int G>
 __device__ __forceinline__ void reset(WarpState<G> &ws) {
@@ -332,12 +346,12 @@ __device__ __forceinline__ void reset(WarpState<G> &ws) {
 // Segment setup (consumer threads only): load q_rot, derive per-head scaling, build B fragments.
 template <int G>
 __device__ __forceinline__ void setup_segment(const Args &a, Smem<G> &sm, int b, int kvh,
-                                              uint32_t (&bq)[Smem<G>::NT][8][2]) {
+                                              uint32_t (&bq)[Smem<G>::NT][8][2], uint32_t &par) {
   constexpr int NT = Smem<G>::NT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float *src = a.qrot + ((size_t)b * a.p.Hq + kvh * G) * D;
   for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = src[i];
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  consumer_sync(sm, par, a.p.err);
   for (int h = warp; h < G; h += CONSUMER_WARPS) {
     float amax = 0.f, sum = 0.f;
 #pragma unroll
@@ -360,7 +374,7 @@ __device__ __forceinline__ void setup_segment(const Args &a, Smem<G> &sm, int b,
       sm.zfac[h] = sum * a.sm_log2;
     }
   }
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  consumer_sync(sm, par, a.p.err);
   const int gq = lane >> 2, t = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -416,7 +430,7 @@ __device__ __forceinline__ void flush(const Args &a, Smem<G> &sm, WarpState<G> &
         }
     }
   }
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  consumer_sync(sm, ws.csync_par, a.p.err);
   for (int h = 0; h < G; ++h) {
     float M = -INFINITY;
 #pragma unroll
@@ -433,7 +447,7 @@ __device__ __forceinline__ void flush(const Args &a, Smem<G> &sm, WarpState<G> &
     slot[h * PART_STRIDE + tid] = O;
     if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
   }
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  consumer_sync(sm, ws.csync_par, a.p.err);
   reset(ws);
 }
 
@@ -584,7 +598,9 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   const PoolArgs &p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], CONSUMER_WARPS); }
+    for (int s = 0; s < NSTAGE; ++s)
+      for (int pg = 0; pg < STAGE_PAGES; ++pg) { mbar_init(&sm.full[s][pg], 1); mbar_init(&sm.empty[s][pg], 1); }
+    mbar_init(&sm.csync, CONSUMER_WARPS);
     mbar_fence_init();
   }
   if (warp == CONSUMER_WARPS) {  // the producer warp locates this CTA's range
@@ -610,10 +626,10 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     long long done = 0;
     while (done < n) {
       bool abort = false;
-      if (it >= NSTAGE) {
+      if (it >= NSTAGE) {  // every page slot of the stage released by its consumer warp
         bool okw = true;
-        if (lane == 0) okw = mbar_wait_bounded(&sm.empty[stage], phase ^ 1);
-        abort = !__shfl_sync(FULL, okw, 0);
+        if (lane < STAGE_PAGES) okw = mbar_wait_bounded(&sm.empty[stage][lane], phase ^ 1);
+        abort = !__all_sync(FULL, okw);
         if (abort && lane == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
       }
       const int seg = b * p.Hkv + kvh;
@@ -629,33 +645,33 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
         }
       }
       const bool have = pp >= 0;
-      const int bytes = __popc(__ballot_sync(FULL, have)) * PAGE_BYTES;
       if (lane < STAGE_PAGES) sm.meta_ntok[stage][lane] = have ? ntk : 0;
       if (lane == 0) {
         sm.meta_seg[stage] = seg;
         sm.meta_flags[stage] = (done + cnt >= n ? 1 : 0) | (abort ? 2 : 0);
       }
-      __syncwarp();  // the stage's metadata is written before its barrier phase can complete
-      if (lane == 0) {
-        if (bytes > 0) mbar_arrive_expect_tx(&sm.full[stage], (uint32_t)bytes);
-        else mbar_arrive(&sm.full[stage]);
-      }
-      __syncwarp();
-      if (have) {
-        uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
-        const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
-        bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, &sm.full[stage]);
-        bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, &sm.full[stage]);
-        bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, &sm.full[stage]);
-        bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, &sm.full[stage]);
-        bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, &sm.full[stage]);
-        bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, &sm.full[stage]);
+      __syncwarp();  // the stage's metadata is written before any of its slots can complete
+      if (lane < STAGE_PAGES) {
+        uint64_t *bar = &sm.full[stage][lane];
+        if (have) {
+          mbar_arrive_expect_tx(bar, (uint32_t)PAGE_BYTES);
+          uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
+          const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
+          bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar);
+          bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar);
+          bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, bar);
+          bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, bar);
+          bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, bar);
+          bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, bar);
+        } else {
+          mbar_arrive(bar);
+        }
       }
       if (abort) {
         // wait (bounded) for the copies still in flight into stages the consumers may not read
-        if (lane == 0)
+        if (lane < STAGE_PAGES)
           for (int k = max(0, it - NSTAGE + 1); k < it; ++k)
-            mbar_wait_bounded(&sm.full[k % NSTAGE], (uint32_t)((k / NSTAGE) & 1));
+            mbar_wait_bounded(&sm.full[k % NSTAGE][lane], (uint32_t)((k / NSTAGE) & 1));
         break;
       }
       done += cnt;
@@ -682,10 +698,11 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   uint32_t bq[NT][8][2];
   // the first segment's query setup needs no pages: it overlaps the first bulk copies
   int cur = sm.b0 * p.Hkv + sm.kvh0, stage = 0;
-  setup_segment(a, sm, sm.b0, sm.kvh0, bq);
+  ws.csync_par = 0;
+  setup_segment(a, sm, sm.b0, sm.kvh0, bq, ws.csync_par);
   uint32_t phase = 0;
   while (true) {
-    if (!mbar_wait_bounded(&sm.full[stage], phase)) {
+    if (!mbar_wait_bounded(&sm.full[stage][warp], phase)) {
       if (lane == 0) atomicOr(a.p.err, OSCAR_DEVERR_TIMEOUT);
       break;
     }
@@ -695,14 +712,14 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     if (seg != cur) {
       if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
       cur = seg;
-      setup_segment(a, sm, seg / p.Hkv, seg % p.Hkv, bq);
+      setup_segment(a, sm, seg / p.Hkv, seg % p.Hkv, bq, ws.csync_par);
     }
     const int ntok = sm.meta_ntok[stage][warp];
     const uint8_t *pb = sm.ring[stage] + warp * PAGE_BYTES;
     if (ntok == PAGE) page_pass<G, true>(pb, ntok, sm, ws, bq);
     else if (ntok > 0) page_pass<G, false>(pb, ntok, sm, ws, bq);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);
+    if (lane == 0) mbar_arrive(&sm.empty[stage][warp]);
     if (flags & 1) break;
     if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
   }
@@ -710,7 +727,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
 }
 
 template <int G>
-__global__ void __launch_bounds__(THREADS) attn_kernel(Args a) {
+__global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
   pdl_wait();
