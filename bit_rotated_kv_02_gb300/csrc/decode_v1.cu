@@ -170,35 +170,41 @@ struct Smem {
 };
 
 // ---------------------------------------------------------------------------------------------
+// q_rot = q . R_k for the G query heads of one (sequence, KV head): grid B * Hkv, 512 threads; thread
+// (c, quarter) sums rows 16k .. 16k+15 for k = 2 quarter, 2 quarter + 1 of column c, and the eight
+// partial sums are added as ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) — the order the demotion
+// kernel uses when it rotates the queries in oscar_decode_step, so both paths give the same bits.
 template <int G>
 __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot) {
   __shared__ float qs[G][D];
-  __shared__ float part[3][G][D];
+  __shared__ float part[8][G][D];
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
-  const int tid = threadIdx.x, c = tid & (D - 1), qt = tid >> 7;  // quarter qt sums rows 32qt .. 32qt+31
+  const int tid = threadIdx.x, c = tid & (D - 1), qt = tid >> 7;
   for (int i = tid; i < G * D; i += 512) qs[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + kvh * G) * D + i]);
   const float *R = p.R_k + (size_t)kvh * D * D + (size_t)(32 * qt) * D + c;
   float r[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = R[(size_t)i * D];
   __syncthreads();
-  float acc[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+  for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
+    for (int h = 0; h < G; ++h) {
+      float acc = 0.f;
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][32 * qt + i], r[i], acc[h]);
-  if (qt > 0)
-#pragma unroll
-    for (int h = 0; h < G; ++h) part[qt - 1][h][c] = acc[h];
+      for (int i = 0; i < 16; ++i) acc = fmaf(qs[h][32 * qt + 16 * hf + i], r[16 * hf + i], acc);
+      part[2 * qt + hf][h][c] = acc;
+    }
+  }
   __syncthreads();
   if (qt == 0)
 #pragma unroll
     for (int h = 0; h < G; ++h)
-      qrot[((size_t)b * p.Hq + kvh * G + h) * D + c] = ((acc[h] + part[0][h][c]) + part[1][h][c]) + part[2][h][c];
+      qrot[((size_t)b * p.Hq + kvh * G + h) * D + c] =
+          ((part[0][h][c] + part[1][h][c]) + (part[2][h][c] + part[3][h][c])) +
+          ((part[4][h][c] + part[5][h][c]) + (part[6][h][c] + part[7][h][c]));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -740,8 +746,10 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
 // Merge: grid (G, Hkv, B), 512 threads; one CTA per (query head of the group, KV head, sequence).
 // The history partials of a segment sit in consecutive slots (CTA index + segment index).  Latency
 // bound, so the global reads are issued in few dependent rounds: the pool counters (to locate the
-// segment's partials) together with this thread's R_v rows, then every partial's (m, l) together with
-// up to OV output values per thread; the softmax weights are applied once the maximum is known.
+// segment's partials), then every partial's (m, l) together with up to OV output values per thread and
+// the R_v rows of the un-rotation; the softmax weights are applied once the maximum is known.  The
+// un-rotation o[c] = sum_j o_rot[j] R_v[c][j] gives each warp 8 outputs c, its lanes splitting j, so
+// that each R_v row is read as one contiguous 512-byte run.
 constexpr int MT = 512;
 constexpr int MAXPARTS = 1040;
 template <int G>
@@ -756,11 +764,6 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
-  // un-rotation rows: o[ch] = sum_j o_rot[j] R_v[ch][j]; slice sl takes j in [32 sl, 32 sl + 32)
-  const float4 *Rrow = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + ch) * D + 32 * sl);
-  float4 rr[8];
-#pragma unroll
-  for (int j4 = 0; j4 < 8; ++j4) rr[j4] = Rrow[j4];
   if (warp == 0) {
     long long total;
     int bb, kk, ll;
@@ -803,6 +806,12 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
     const int i = sl + 4 * k;
     ov[k] = i < nparts ? slot(i)[ch] : 0.f;
   }
+  // R_v rows c = warp + 16 k (k < 8), lane's four columns 4 lane .. 4 lane + 3
+  constexpr int UW = MT / 32, UPW = D / UW;
+  float4 rv[UPW];
+#pragma unroll
+  for (int k = 0; k < UPW; ++k)
+    rv[k] = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + warp + UW * k) * D)[lane];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
   if (lane == 0) red[warp] = mx;
@@ -842,21 +851,19 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   __syncthreads();
   if (sl == 0) Orot[ch] = ((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch];
   __syncthreads();
-  float u = 0.f;
+  {
+    const float4 o4 = reinterpret_cast<const float4 *>(Orot)[lane];
 #pragma unroll
-  for (int j4 = 0; j4 < 8; ++j4) {
-    const int j = 32 * sl + 4 * j4;
-    u = fmaf(rr[j4].x, Orot[j], u);
-    u = fmaf(rr[j4].y, Orot[j + 1], u);
-    u = fmaf(rr[j4].z, Orot[j + 2], u);
-    u = fmaf(rr[j4].w, Orot[j + 3], u);
+    for (int k = 0; k < UPW; ++k) {
+      float u = fmaf(rv[k].x, o4.x, fmaf(rv[k].y, o4.y, fmaf(rv[k].z, o4.z, rv[k].w * o4.w)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
+      if (lane == 0) Osl[0][warp + UW * k] = u;  // slot 0 of Osl is free again
+    }
   }
   __syncthreads();
-  Osl[sl][ch] = u;
-  __syncthreads();
   if (sl == 0) {
-    const float o = (((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch]) +
-                    (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
+    const float o = Osl[0][ch] + (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
     out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
   }
 }

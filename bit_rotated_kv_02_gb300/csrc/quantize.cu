@@ -11,53 +11,53 @@
 namespace oscar {
 
 // ---------------------------------------------------------------------------------------------
-// Demote (and optionally append): grid (Hkv, B), 256 threads.  Warps 0-3 rotate the K vector and
-// warps 4-7 the V vector of KV head blockIdx.x of sequence blockIdx.y, each warp over 32 rows of R
-// (all row loads issued at once); warps 0 and 4 then combine the partial dots and quantize.  Every
-// CTA reads the sequence's counters before any CTA of that sequence can change them: the last CTA to
-// arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival counter to zero.
+// Demote (and optionally append): grid (2 * Hkv, B), 256 threads; CTA 2h handles the K vector and CTA
+// 2h + 1 the V vector of KV head h of sequence blockIdx.y.  Each of the 8 warps holds 16 rows of R in
+// registers (loaded at entry, with the appended token and the pool counters: a demotion is a chain of
+// dependent reads, so everything independent is issued first); warp 0 combines the partial dots and
+// quantizes.  Every CTA reads the sequence's counters before any CTA of that sequence can change them:
+// the last CTA to arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival
+// counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
-// mode 2: as mode 0, then append k_new/v_new.  With q != NULL the CTA also writes the rotated queries
+// mode 2: as mode 0, then append k_new/v_new.  With q != NULL the K CTA also writes the rotated queries
 // q_rot = q . R_k of its KV head's query heads (the decode step's query rotation, fused here because
-// this CTA already holds R_k in registers).
+// this CTA already holds R_k in registers), summed in the order of v1::qrot_kernel.
+constexpr int DEMOTE_WARPS = 8, DEMOTE_ROWS = D / DEMOTE_WARPS;  // 16 rows of R per warp
 __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
                                                             const uint16_t *k_new, const uint16_t *v_new,
                                                             const uint16_t *q, float *qrot) {
   constexpr int GMAX = 8;
-  __shared__ float xs[2][D];
-  __shared__ float pacc[8][32][4], psab[8][32][4];
+  __shared__ float xs[D];
+  __shared__ float pacc[DEMOTE_WARPS][32][4], psab[DEMOTE_WARPS][32][4];
   __shared__ float qsm[GMAX][D];
-  __shared__ float4 qpart[4][GMAX][32];
+  __shared__ float4 qpart[DEMOTE_WARPS][GMAX][32];
   __shared__ int s_ok;
   pdl_wait();
   pdl_trigger();
-  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int kvh = blockIdx.x >> 1, kv = blockIdx.x & 1, b = blockIdx.y;  // kv 0 = K, 1 = V
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kv = warp >> 2, part = warp & 3;  // kv 0 = K, 1 = V
-  // This warp's 32 rows of R, loaded before (and in parallel with) the pool counters they do not
-  // depend on: the dependent global reads of a demotion are its latency.
   const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
-  float4 rrow[32];
+  float4 rrow[DEMOTE_ROWS];
   {
-    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(32 * part) * (D / 4) + lane;
+    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(DEMOTE_ROWS * warp) * (D / 4) + lane;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) rrow[i] = R4[i * (D / 4)];
+    for (int i = 0; i < DEMOTE_ROWS; ++i) rrow[i] = R4[i * (D / 4)];
   }
-  // the appended token's row (mode 2; warps 0 and 4), also independent of the counters
+  // the appended token's row (mode 2; warp 0), also independent of the counters
   uint2 newrow = make_uint2(0u, 0u);
-  if (mode == 2 && part == 0)
+  if (mode == 2 && warp == 0)
     newrow = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[lane];
-  // fused query rotation (q != NULL): q of the G query heads of this KV head, staged for warps 0-3
+  // fused query rotation (q != NULL): q of the G query heads of this KV head
   const int G = p.Hq / p.Hkv;
   if (q != nullptr && kv == 0)
-    for (int i = threadIdx.x; i < G * D; i += 128)
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x)
       qsm[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + (size_t)kvh * G) * D + i]);
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
   const bool want = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
   // the oldest recent vector and the page-table entry are read together
   uint2 xw = make_uint2(0u, 0u);
-  if (want && part == 0)
+  if (want && warp == 0)
     xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
                                          (((size_t)b * p.Hkv + kvh) * RECENT + rs) * D)[lane];
   bool demote = want;
@@ -79,64 +79,83 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   // A demotion that cannot be stored leaves the whole sequence unchanged (no append either).
   const bool blocked = want && !demote;
   if (demote) {
-    const float *R = Rw;
-    if (part == 0) {
-      xs[kv][4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
-      xs[kv][4 * lane + 1] = bf16_to_f32(xw.x >> 16);
-      xs[kv][4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
-      xs[kv][4 * lane + 3] = bf16_to_f32(xw.y >> 16);
+    if (warp == 0) {
+      xs[4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
+      xs[4 * lane + 1] = bf16_to_f32(xw.x >> 16);
+      xs[4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
+      xs[4 * lane + 3] = bf16_to_f32(xw.y >> 16);
     }
     __syncthreads();
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
-    rot_dot_32rows_pre(xs[kv], rrow, 32 * part, acc, sab);
+#pragma unroll
+    for (int i = 0; i < DEMOTE_ROWS; ++i) {
+      const float xi = xs[DEMOTE_ROWS * warp + i], ax = fabsf(xi);
+      acc[0] = fmaf(xi, rrow[i].x, acc[0]);
+      acc[1] = fmaf(xi, rrow[i].y, acc[1]);
+      acc[2] = fmaf(xi, rrow[i].z, acc[2]);
+      acc[3] = fmaf(xi, rrow[i].w, acc[3]);
+      sab[0] = fmaf(ax, fabsf(rrow[i].x), sab[0]);
+      sab[1] = fmaf(ax, fabsf(rrow[i].y), sab[1]);
+      sab[2] = fmaf(ax, fabsf(rrow[i].z), sab[2]);
+      sab[3] = fmaf(ax, fabsf(rrow[i].w), sab[3]);
+    }
 #pragma unroll
     for (int k = 0; k < 4; ++k) { pacc[warp][lane][k] = acc[k]; psab[warp][lane][k] = sab[k]; }
     __syncthreads();
-    if (part == 0) {
+    if (warp == 0) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        acc[k] = ((pacc[warp][lane][k] + pacc[warp + 1][lane][k]) + pacc[warp + 2][lane][k]) + pacc[warp + 3][lane][k];
-        sab[k] = ((psab[warp][lane][k] + psab[warp + 1][lane][k]) + psab[warp + 2][lane][k]) + psab[warp + 3][lane][k];
+        float a8 = 0.f, s8 = 0.f;
+#pragma unroll
+        for (int w = 0; w < DEMOTE_WARPS; ++w) { a8 += pacc[w][lane][k]; s8 += psab[w][lane][k]; }
+        acc[k] = a8;
+        sab[k] = s8;
       }
       const float clip = (kv == 0 ? p.clip_k : p.clip_v)[kvh];
       const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
       QuantStats st{0, 0, 0};
-      quantize_from_dots(xs[kv], R, acc, sab, clip, p.g, (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
+      quantize_from_dots(xs, Rw, acc, sab, clip, p.g, (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
                          (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
                          st);
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
-  if (q != nullptr) {
-    // q_rot[h] = q[h] . R_k: warp `part` of the K half sums its 32 rows of R_k (already in registers)
-    if (kv == 0) {
-      for (int h = 0; h < G; ++h) {
-        float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (q != nullptr && kv == 0) {
+    // q_rot[h] = q[h] . R_k: warp w sums rows 16w .. 16w+15 (already in registers)
+    for (int h = 0; h < G; ++h) {
+      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float qi = qsm[h][32 * part + i];
-          acc4.x = fmaf(qi, rrow[i].x, acc4.x);
-          acc4.y = fmaf(qi, rrow[i].y, acc4.y);
-          acc4.z = fmaf(qi, rrow[i].z, acc4.z);
-          acc4.w = fmaf(qi, rrow[i].w, acc4.w);
-        }
-        qpart[part][h][lane] = acc4;
+      for (int i = 0; i < DEMOTE_ROWS; ++i) {
+        const float qi = qsm[h][DEMOTE_ROWS * warp + i];
+        acc4.x = fmaf(qi, rrow[i].x, acc4.x);
+        acc4.y = fmaf(qi, rrow[i].y, acc4.y);
+        acc4.z = fmaf(qi, rrow[i].z, acc4.z);
+        acc4.w = fmaf(qi, rrow[i].w, acc4.w);
       }
+      qpart[warp][h][lane] = acc4;
     }
-    __syncthreads();
-    if (kv == 0) {
-      for (int h = part; h < G; h += 4) {
-        const float4 a0 = qpart[0][h][lane], a1 = qpart[1][h][lane], a2 = qpart[2][h][lane], a3 = qpart[3][h][lane];
-        reinterpret_cast<float4 *>(qrot + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D)[lane] =
-            make_float4(((a0.x + a1.x) + a2.x) + a3.x, ((a0.y + a1.y) + a2.y) + a3.y, ((a0.z + a1.z) + a2.z) + a3.z,
-                        ((a0.w + a1.w) + a2.w) + a3.w);
-      }
+  }
+  __syncthreads();
+  if (q != nullptr && kv == 0) {
+    for (int h = warp; h < G; h += DEMOTE_WARPS) {
+      float4 pr[DEMOTE_WARPS];
+#pragma unroll
+      for (int w = 0; w < DEMOTE_WARPS; ++w) pr[w] = qpart[w][h][lane];
+      // ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)), as v1::qrot_kernel
+      auto t8 = [&](float a0, float a1, float a2, float a3, float a4, float a5, float a6, float a7) {
+        return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+      };
+      reinterpret_cast<float4 *>(qrot + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D)[lane] = make_float4(
+          t8(pr[0].x, pr[1].x, pr[2].x, pr[3].x, pr[4].x, pr[5].x, pr[6].x, pr[7].x),
+          t8(pr[0].y, pr[1].y, pr[2].y, pr[3].y, pr[4].y, pr[5].y, pr[6].y, pr[7].y),
+          t8(pr[0].z, pr[1].z, pr[2].z, pr[3].z, pr[4].z, pr[5].z, pr[6].z, pr[7].z),
+          t8(pr[0].w, pr[1].w, pr[2].w, pr[3].w, pr[4].w, pr[5].w, pr[6].w, pr[7].w));
     }
   }
   const bool append = mode == 2 && counters_ok && !blocked;
   int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
   if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
-  if (append && (warp == 0 || warp == 4)) {
+  if (append && warp == 0) {
     uint16_t *dst;
     if (nslen < SINK && nhl == 0 && nrl == 0) {
       dst = (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kvh) * SINK + nslen) * D;
@@ -153,7 +172,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   if (threadIdx.x == 0) {
     __threadfence();
     const int arrived = atomicAdd(p.sync + b, 1);
-    s_ok = arrived == p.Hkv - 1;
+    s_ok = arrived == 2 * p.Hkv - 1;
   }
   __syncthreads();
   if (s_ok && threadIdx.x == 0) {
@@ -190,7 +209,7 @@ cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, cons
                           const uint16_t *v_new, cudaStream_t s, const uint16_t *q, float *qrot) {
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
   const cudaError_t e =
-      launch_pdl(demote_append_kernel, dim3(p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new, q, qrot);
+      launch_pdl(demote_append_kernel, dim3(2 * p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new, q, qrot);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
   return e;
 }
