@@ -184,7 +184,7 @@ __device__ __forceinline__ void rot_dot_32rows_pre(const float *xs, const float4
 }
 
 // Warp-cooperative interval [x, y] containing the float32 nearest to the exact x . R_j (xs: float32
-// copy of the bf16 vector; R row-major fp32).  Products are split error-free (p + e = x r, FMA),
+// copy of the bf16 vector; R row-major fp32 with leading dimension ld, e.g. a padded shared copy).  Products are split error-free (p + e = x r, FMA),
 // partial sums carry their rounding errors (TwoSum), and the errors are summed in plain float32,
 // whose own error is below gamma_2n * gamma_n * sum|x r| < 2^-33 sum|x r|; the interval uses 2^-31
 // times the computed sum.  Every lane returns the same interval.
@@ -193,13 +193,13 @@ __device__ __forceinline__ void two_sum_f32(float a, float b, float &s, float &e
   const float bp = __fsub_rn(s, a);
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
 }
-static __device__ __noinline__ float2 dot2_interval_xs(const float *xs, const float *R, int j) {
+static __device__ __noinline__ float2 dot2_interval_xs(const float *xs, const float *R, int ld, int j) {
   const int lane = threadIdx.x & 31;
   float s = 0.f, c = 0.f, sab = 0.f;
 #pragma unroll
   for (int k = 0; k < D / 32; ++k) {
     const int i = lane + 32 * k;
-    const float xv = xs[i], rv = R[i * D + j];
+    const float xv = xs[i], rv = R[i * ld + j];
     const float p = __fmul_rn(xv, rv);
     const float e = fmaf(xv, rv, -p);
     float t, q;
@@ -233,9 +233,12 @@ static __device__ __noinline__ float2 dot2_interval_xs(const float *xs, const fl
 // the same bf16 zero, its scale when both extreme corners give the same bf16 scale (zero increases
 // with the minimum; scale increases with the maximum and decreases with the minimum), and a code
 // when both ends of the element's interval give the same code.
-__device__ inline void quantize_from_dots(const float *xs, const float *R, const float (&acc)[4], const float (&sab)[4],
-                                          float clip, int g, uint8_t *codes_out, uint16_t *scale_out,
-                                          uint16_t *zero_out, QuantStats &st) {
+// R: the rotation in global memory (float64 / integer tier); R2, ld2: the same values for the Dot2
+// tier (a shared-memory copy with row stride ld2, or R itself with ld2 = 128).
+__device__ inline void quantize_from_dots(const float *xs, const float *R, const float *R2, int ld2,
+                                          const float (&acc)[4], const float (&sab)[4], float clip, int g,
+                                          uint8_t *codes_out, uint16_t *scale_out, uint16_t *zero_out,
+                                          QuantStats &st) {
   const int lane = threadIdx.x & 31;
   const int gl = g / 4;  // lanes per group (8, 16 or 32)
   // gamma_128 = 7.6294e-6; 8e-6 also covers the rounding of sab itself; 1e-37 covers underflow.
@@ -281,7 +284,7 @@ __device__ inline void quantize_from_dots(const float *xs, const float *R, const
       const int src = __ffs(__ballot_sync(FULL, mine != 0)) - 1;
       const int k = __ffs(__shfl_sync(FULL, mine, src)) - 1;
       float2 iv;
-      if (tier == 0) iv = dot2_interval_xs(xs, R, 4 * src + k);
+      if (tier == 0) iv = dot2_interval_xs(xs, R2, ld2, 4 * src + k);
       else iv.x = iv.y = exact_rot_elem(xs, R, 4 * src + k, unproven);
       if (lane == src) {
 #pragma unroll

@@ -23,6 +23,8 @@ namespace oscar {
 // q_rot = q . R_k of its KV head's query heads (the decode step's query rotation, fused here because
 // this CTA already holds R_k in registers), summed in the order of v1::qrot_kernel.
 constexpr int DEMOTE_WARPS = 8, DEMOTE_ROWS = D / DEMOTE_WARPS;  // 16 rows of R per warp
+constexpr int RS_LD = D + 4;  // padded row stride of the shared copy of R (16-byte rows, 4-way reads)
+constexpr size_t DEMOTE_SMEM = (size_t)D * RS_LD * sizeof(float);
 __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
                                                             const uint16_t *k_new, const uint16_t *v_new,
                                                             const uint16_t *q, float *qrot) {
@@ -32,6 +34,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   __shared__ float qsm[GMAX][D];
   __shared__ float4 qpart[DEMOTE_WARPS][GMAX][32];
   __shared__ int s_ok;
+  extern __shared__ float4 rs4[];  // this CTA's R, row stride RS_LD floats, for the Dot2 tier
   pdl_wait();
   pdl_trigger();
   const int kvh = blockIdx.x >> 1, kv = blockIdx.x & 1, b = blockIdx.y;  // kv 0 = K, 1 = V
@@ -42,6 +45,8 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(DEMOTE_ROWS * warp) * (D / 4) + lane;
 #pragma unroll
     for (int i = 0; i < DEMOTE_ROWS; ++i) rrow[i] = R4[i * (D / 4)];
+#pragma unroll
+    for (int i = 0; i < DEMOTE_ROWS; ++i) rs4[(DEMOTE_ROWS * warp + i) * (RS_LD / 4) + lane] = rrow[i];
   }
   // the appended token's row (mode 2; warp 0), also independent of the counters
   uint2 newrow = make_uint2(0u, 0u);
@@ -114,7 +119,8 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
       const float clip = (kv == 0 ? p.clip_k : p.clip_v)[kvh];
       const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
       QuantStats st{0, 0, 0};
-      quantize_from_dots(xs, Rw, acc, sab, clip, p.g, (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
+      quantize_from_dots(xs, Rw, reinterpret_cast<const float *>(rs4), RS_LD, acc, sab, clip, p.g,
+                         (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
                          (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
                          st);
     }
@@ -207,9 +213,11 @@ __global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl)
 // ---- launchers ------------------------------------------------------------------------------
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
                           const uint16_t *v_new, cudaStream_t s, const uint16_t *q, float *qrot) {
+  cudaError_t e = cudaFuncSetAttribute(demote_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEMOTE_SMEM);
+  if (e != cudaSuccess) return e;
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
-  const cudaError_t e =
-      launch_pdl(demote_append_kernel, dim3(2 * p.Hkv, p.B), dim3(256), 0, s, p, mask, mode, k_new, v_new, q, qrot);
+  e = launch_pdl(demote_append_kernel, dim3(2 * p.Hkv, p.B), dim3(256), DEMOTE_SMEM, s, p, mask, mode, k_new, v_new, q,
+                 qrot);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
   return e;
 }
