@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed"], default="decode100k",
+    ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed", "bf16-compare"],
+                    default="decode100k",
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -256,6 +257,89 @@ def _time(fn, steps, warmup):
     return e0.elapsed_time(e1) / steps   # ms per step
 
 
+def bf16_compare(args, peak):
+    """The 100k-context, batch-1 decode step with the whole history in a BF16 paged cache against the
+    same step over the INT2 pool, in one process on the same GPU (the pages' batch-1 speed-up over BF16,
+    "评估结果" Fig. 5, measured at kernel level).  Both arms append one token per step."""
+    import numpy as np
+    import torch
+    import bit_rotated_kv_02_gb300 as ok
+    import synth
+    lib = ok.lib()
+    steps, warm = max(3, min(args.steps, 2000)), max(3, min(args.warmup, 50))
+    n_bf = 4                                      # 410 MB of KV per layer: every step reads HBM
+    per_layer = -(-(steps + warm) // n_bf) + 8
+    pages = -(-(L_CTX + per_layer) // PAGE)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5151)
+    chan = torch.from_numpy(synth.outlier_channels(2024, HKV, D, 4).astype(np.int64)).cuda()
+    caches = []
+    for _ in range(n_bf):
+        Cc = ok.BF16Cache(1, HQ, HKV, pages, pages)
+        Cc.set_page_table(torch.randperm(pages, generator=gen, device="cuda").to(torch.int32)[None])
+        ok.oscar_bf16_prefill(Cc, 0, _gpu_kv(gen, L_CTX, HKV, chan), _gpu_kv(gen, L_CTX, HKV, chan))
+        caches.append(Cc)
+    q = (torch.randn((1, HQ, D), generator=gen, device="cuda") * 3).to(torch.bfloat16)
+    kn, vn = _gpu_kv(gen, 1, HKV, chan), _gpu_kv(gen, 1, HKV, chan)
+    out = torch.empty((1, HQ, D), dtype=torch.float32, device="cuda")
+    ws = torch.empty(ok.oscar_bf16_decode_workspace_size(caches[0]), dtype=torch.uint8, device="cuda")
+    EVERY = 8
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(-(-steps // EVERY))]
+    for e2 in evs:
+        for e in e2:
+            e.record()
+
+    def bf_step(i, ev=None):
+        if ev is not None:
+            lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
+        ok.oscar_bf16_decode_step(caches[i % n_bf], kn, vn, q, out=out, ws=ws)
+
+    for i in range(warm):
+        bf_step(i)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for i in range(steps):
+        bf_step(warm + i, evs[i // EVERY] if i % EVERY == 0 else None)
+    t1.record()
+    torch.cuda.synchronize()
+    bf_ms = t0.elapsed_time(t1) / steps
+    attn_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) * 1e3
+    for Cc in caches:
+        assert Cc.err() == 0, hex(Cc.err())
+    ctx = L_CTX + (steps + warm) / (2 * n_bf)        # mean tokens held over the timed steps
+    attn_bytes = ctx * HKV * 2 * D * 2 + 4 * math.ceil(ctx / PAGE) + HQ * D * 2
+    del caches, ws
+    torch.cuda.empty_cache()
+    # the INT2 arm: the headline step over the three-segment pool
+    NL = 8
+    layers = setup_layers(NL, -(-(steps + warm) // NL) + 8)
+    ws2 = torch.empty(ok.oscar_decode_workspace_size(layers[0], 0), dtype=torch.uint8, device="cuda")
+    step2 = lambda i: ok.oscar_decode_step(layers[i % NL], kn, vn, q, out=out, ws=ws2)
+    for i in range(warm):
+        step2(i)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(steps):
+        step2(warm + i)
+    t1.record()
+    torch.cuda.synchronize()
+    int2_ms = t0.elapsed_time(t1) / steps
+    achieved = attn_bytes / (attn_us * 1e-6) / 1e9
+    return [{"metric": "decode step, BF16 paged cache vs INT2 pool: KV tokens/s", "workload":
+             "qwen3-8b-layer decode, 100k context, batch 1: BF16 paged history vs OSCAR INT2 pool",
+             "value": L_CTX / (bf_ms * 1e-3), "unit": "KV tokens/s", "ms_per_step": bf_ms, "steps": steps,
+             "int2_ms_per_step": int2_ms, "int2_value": L_CTX / (int2_ms * 1e-3),
+             "speedup_int2_over_bf16": bf_ms / int2_ms,
+             "config": {"num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D, "page_tokens": PAGE,
+                        "l2": f"{n_bf} rotating BF16 caches of {attn_bytes / 1e6:.0f} MB (> L2)"},
+             "roofline": {"bound": "hbm", "kernel": "bf::attn_kernel (BF16 paged history)", "achieved": achieved,
+                          "peak": peak, "unit": "GB/s", "frac": achieved / peak, "mean_launch_us": attn_us,
+                          "algorithmic_bytes_per_launch": attn_bytes, "timed_launches": len(evs),
+                          "sampling": f"every {EVERY}th step of the timed region"},
+             "gpu_launches": steps * 3}]
+
+
 def other_workload(args):
     import numpy as np
     import torch
@@ -267,6 +351,8 @@ def other_workload(args):
     except (OSError, ValueError):
         pass
     peak = peaks.get("hbm_gbs") or 6800.0
+    if args.workload == "bf16-compare":
+        return bf16_compare(args, peak)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4242)
     lines = []

@@ -25,7 +25,9 @@ DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT = 1, 2, 
 __all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
            "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_demote", "oscar_append_kv",
            "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events",
-           "oscar_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "lib"]
+           "oscar_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "lib", "BF16Cache", "oscar_bf16_prefill",
+           "oscar_bf16_append_kv", "oscar_bf16_decode_workspace_size", "oscar_bf16_decode_attention",
+           "oscar_bf16_decode_step"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 PROFILE_HISTORY, PROFILE_DEMOTE = 0, 1
 
@@ -224,4 +226,76 @@ def oscar_decode_attention_noalloc(pool: Pool, q, out, softmax_scale=None, strea
     scale = 1.0 / math.sqrt(pool.d) if softmax_scale is None else float(softmax_scale)
     _lib.check(lib().oscar_decode_attention_noalloc(pool.ref, _p(q), _p(out), scale, _s(stream)),
                "oscar_decode_attention_noalloc")
+    return out
+
+
+# ---- BF16 paged cache: the baseline INT2 decoding is compared against ----------------------------------
+class BF16Cache:
+    """Device storage of a BF16 paged KV cache plus its C struct (see include/oscar.h)."""
+
+    def __init__(self, batch, num_q_heads, num_kv_heads, num_pages, max_pages, device="cuda", head_dim=HEAD_DIM):
+        dev = torch.device(device)
+        self.B, self.Hq, self.Hkv, self.d = batch, num_q_heads, num_kv_heads, head_dim
+        self.num_pages, self.max_pages = num_pages, max_pages
+        self.k_pages = torch.zeros((num_pages, num_kv_heads, PAGE, head_dim), dtype=torch.bfloat16, device=dev)
+        self.v_pages = torch.zeros_like(self.k_pages)
+        self.page_table = torch.full((batch, max_pages), -1, dtype=torch.int32, device=dev)
+        self.seq_len = torch.zeros(batch, dtype=torch.int32, device=dev)
+        self.err_word = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.struct = _lib.oscar_bf16_cache(
+            batch, num_q_heads, num_kv_heads, head_dim, num_pages, max_pages,
+            *(t.data_ptr() for t in (self.k_pages, self.v_pages, self.page_table, self.seq_len, self.err_word)))
+
+    @property
+    def ref(self):
+        return C.byref(self.struct)
+
+    def set_page_table(self, pt):
+        self.page_table.copy_(torch.as_tensor(pt, dtype=torch.int32).reshape(self.page_table.shape))
+
+    def err(self) -> int:
+        return int(self.err_word.item()) & 0xffffffff
+
+
+def oscar_bf16_prefill(cache: BF16Cache, seq: int, k, v, stream=None):
+    """Tokens [0, len) of sequence `seq` from bf16 k, v [len][Hkv][128]."""
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v")
+    _lib.check(lib().oscar_bf16_prefill(cache.ref, seq, k.shape[0], _p(k), _p(v), _s(stream)), "oscar_bf16_prefill")
+
+
+def oscar_bf16_append_kv(cache: BF16Cache, k_new, v_new, stream=None):
+    _dev(k_new, torch.bfloat16, "k_new")
+    _dev(v_new, torch.bfloat16, "v_new")
+    _lib.check(lib().oscar_bf16_append_kv(cache.ref, _p(k_new), _p(v_new), _s(stream)), "oscar_bf16_append_kv")
+
+
+def oscar_bf16_decode_workspace_size(cache: BF16Cache) -> int:
+    n = C.c_size_t(0)
+    _lib.check(lib().oscar_bf16_decode_workspace_size(cache.ref, C.byref(n)), "oscar_bf16_decode_workspace_size")
+    return n.value
+
+
+def oscar_bf16_decode_attention(cache: BF16Cache, q, out=None, softmax_scale=None, ws=None, stream=None):
+    """fp32 out [B][Hq][128] of bf16 q [B][Hq][128] over the BF16 cache."""
+    _dev(q, torch.bfloat16, "q")
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    if ws is None:
+        ws = torch.empty(oscar_bf16_decode_workspace_size(cache), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(cache.d) if softmax_scale is None else float(softmax_scale)
+    _lib.check(lib().oscar_bf16_decode_attention(cache.ref, _p(q), _p(out), scale, _p(ws), ws.numel(), _s(stream)),
+               "oscar_bf16_decode_attention")
+    return out
+
+
+def oscar_bf16_decode_step(cache: BF16Cache, k_new, v_new, q, out=None, softmax_scale=None, ws=None, stream=None):
+    """Append k_new/v_new bf16 [B][Hkv][128], then attention of q bf16 [B][Hq][128]; returns fp32 out."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (q, "q")):
+        _dev(t, torch.bfloat16, n)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+    if ws is None:
+        ws = torch.empty(oscar_bf16_decode_workspace_size(cache), dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(cache.d) if softmax_scale is None else float(softmax_scale)
+    _lib.check(lib().oscar_bf16_decode_step(cache.ref, _p(k_new), _p(v_new), _p(q), _p(out), scale, _p(ws),
+                                            ws.numel(), _s(stream)), "oscar_bf16_decode_step")
     return out

@@ -31,8 +31,16 @@ class oscar_pool(C.Structure):
                 ("clip_v", C.c_void_p), ("err", C.c_void_p), ("sync", C.c_void_p)]
 
 
+class oscar_bf16_cache(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("num_q_heads", C.c_int32), ("num_kv_heads", C.c_int32),
+                ("head_dim", C.c_int32), ("num_pages", C.c_int32), ("max_pages", C.c_int32),
+                ("k_pages", C.c_void_p), ("v_pages", C.c_void_p), ("page_table", C.c_void_p),
+                ("seq_len", C.c_void_p), ("err", C.c_void_p)]
+
+
 P, I32, I64, SZ, F32, F64 = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float, C.c_double
 PP = C.POINTER(oscar_pool)
+PC = C.POINTER(oscar_bf16_cache)
 SIGNATURES = {
     "oscar_last_error_string": ([], C.c_char_p),
     "oscar_version": ([], C.c_char_p),
@@ -50,6 +58,11 @@ SIGNATURES = {
     "oscar_profile_events": ([I32, P, P], C.c_int),
     "oscar_decode_attention_noalloc": ([PP, P, P, F32, P], C.c_int),
     "oscar_decode_step": ([PP, P, P, P, P, F32, P, SZ, P], C.c_int),
+    "oscar_bf16_prefill": ([PC, I32, I64, P, P, P], C.c_int),
+    "oscar_bf16_append_kv": ([PC, P, P, P], C.c_int),
+    "oscar_bf16_decode_workspace_size": ([PC, C.POINTER(C.c_size_t)], C.c_int),
+    "oscar_bf16_decode_attention": ([PC, P, P, F32, P, SZ, P], C.c_int),
+    "oscar_bf16_decode_step": ([PC, P, P, P, P, F32, P, SZ, P], C.c_int),
 }
 
 _LIB = None

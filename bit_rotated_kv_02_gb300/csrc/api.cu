@@ -75,6 +75,31 @@ oscar_status_t check_pool(const oscar_pool *pool, PoolArgs &a) {
   return OSCAR_OK;
 }
 
+oscar_status_t check_cache(const oscar_bf16_cache *cache, CacheArgs &a) {
+  if (cache == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  const oscar_bf16_cache &c = *cache;
+  if (c.head_dim != OSCAR_HEAD_DIM) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d (only 128)", c.head_dim);
+  if (c.batch <= 0 || c.num_kv_heads <= 0 || c.num_q_heads <= 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "batch/heads must be positive");
+  if (c.num_q_heads % c.num_kv_heads != 0)
+    return fail(OSCAR_ERR_INVALID_ARG, "num_q_heads %d not a multiple of num_kv_heads %d", c.num_q_heads, c.num_kv_heads);
+  const int G = c.num_q_heads / c.num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(OSCAR_ERR_UNSUPPORTED, "GQA ratio %d (1, 2, 4 or 8)", G);
+  if (c.num_pages <= 0 || c.max_pages <= 0) return fail(OSCAR_ERR_INVALID_ARG, "page counts must be positive");
+  if ((int64_t)c.max_pages * OSCAR_PAGE_TOKENS > (int64_t)1 << 30)
+    return fail(OSCAR_ERR_INVALID_ARG, "max_pages %d too large", c.max_pages);
+  if ((int64_t)c.num_pages * c.num_kv_heads * OSCAR_PAGE_TOKENS >= (int64_t)1 << 31)
+    return fail(OSCAR_ERR_INVALID_ARG, "num_pages * Hkv * 64 must stay below 2^31");
+  if (c.k_pages == nullptr || c.v_pages == nullptr || c.page_table == nullptr || c.seq_len == nullptr ||
+      c.err == nullptr)
+    return fail(OSCAR_ERR_INVALID_ARG, "cache pointer is NULL");
+  if ((reinterpret_cast<uintptr_t>(c.k_pages) | reinterpret_cast<uintptr_t>(c.v_pages)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "cache page arrays must be 16-byte aligned");
+  a.B = c.batch; a.Hq = c.num_q_heads; a.Hkv = c.num_kv_heads; a.num_pages = c.num_pages; a.max_pages = c.max_pages;
+  a.k_pages = c.k_pages; a.v_pages = c.v_pages; a.page_table = c.page_table; a.seq_len = c.seq_len; a.err = c.err;
+  return OSCAR_OK;
+}
+
 int auto_splits(const PoolArgs &a) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -269,6 +294,71 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
   return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws),
                                     static_cast<cudaStream_t>(stream)),
                      "decode_step");
+}
+
+oscar_status_t oscar_bf16_prefill(const oscar_bf16_cache *cache, int32_t seq, int64_t len, const oscar_bf16 *k,
+                                  const oscar_bf16 *v, oscar_stream_t stream) {
+  CacheArgs a;
+  oscar_status_t st = check_cache(cache, a);
+  if (st != OSCAR_OK) return st;
+  if (seq < 0 || seq >= a.B) return fail(OSCAR_ERR_INVALID_ARG, "seq %d outside [0, %d)", seq, a.B);
+  if (len < 0 || len > (int64_t)a.max_pages * OSCAR_PAGE_TOKENS)
+    return fail(OSCAR_ERR_INVALID_ARG, "len %lld outside [0, max_pages*64]", (long long)len);
+  if (len > 0 && (k == nullptr || v == nullptr)) return fail(OSCAR_ERR_INVALID_ARG, "k/v NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  return cuda_status(launch_bf16_prefill(a, seq, (int)len, k, v, static_cast<cudaStream_t>(stream)), "bf16_prefill");
+}
+
+oscar_status_t oscar_bf16_append_kv(const oscar_bf16_cache *cache, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
+                                    oscar_stream_t stream) {
+  CacheArgs a;
+  oscar_status_t st = check_cache(cache, a);
+  if (st != OSCAR_OK) return st;
+  if (k_new == nullptr || v_new == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "k_new/v_new NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  return cuda_status(launch_bf16_append(a, k_new, v_new, static_cast<cudaStream_t>(stream)), "bf16_append_kv");
+}
+
+oscar_status_t oscar_bf16_decode_workspace_size(const oscar_bf16_cache *cache, size_t *bytes) {
+  CacheArgs a;
+  oscar_status_t st = check_cache(cache, a);
+  if (st != OSCAR_OK) return st;
+  if (bytes == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = bf16_ws_bytes(a);
+  return OSCAR_OK;
+}
+
+static oscar_status_t bf16_decode(const oscar_bf16_cache *cache, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
+                                  const oscar_bf16 *q, float *out, float softmax_scale, void *ws, size_t ws_bytes,
+                                  oscar_stream_t stream, const char *what) {
+  CacheArgs a;
+  oscar_status_t st = check_cache(cache, a);
+  if (st != OSCAR_OK) return st;
+  if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
+  if ((reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+    return fail(OSCAR_ERR_INVALID_ARG, "q and out must be 4-byte aligned");
+  if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  const size_t need = bf16_ws_bytes(a);
+  if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  return cuda_status(launch_bf16_decode(a, q, out, softmax_scale, static_cast<float *>(ws),
+                                        static_cast<cudaStream_t>(stream), k_new, v_new),
+                     what);
+}
+
+oscar_status_t oscar_bf16_decode_attention(const oscar_bf16_cache *cache, const oscar_bf16 *q, float *out,
+                                           float softmax_scale, void *ws, size_t ws_bytes, oscar_stream_t stream) {
+  return bf16_decode(cache, nullptr, nullptr, q, out, softmax_scale, ws, ws_bytes, stream, "bf16_decode_attention");
+}
+
+oscar_status_t oscar_bf16_decode_step(const oscar_bf16_cache *cache, const oscar_bf16 *k_new,
+                                      const oscar_bf16 *v_new, const oscar_bf16 *q, float *out,
+                                      float softmax_scale, void *ws, size_t ws_bytes, oscar_stream_t stream) {
+  if (k_new == nullptr || v_new == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "k_new/v_new NULL");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  return bf16_decode(cache, k_new, v_new, q, out, softmax_scale, ws, ws_bytes, stream, "bf16_decode_step");
 }
 
 }  // extern "C"

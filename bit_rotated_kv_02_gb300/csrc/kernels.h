@@ -1,6 +1,8 @@
 // Launchers shared between the API layer and the kernel translation units (internal).
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -66,6 +68,25 @@ cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, f
 // Append + demote + query rotation in one kernel, then attention and merge (group size 128).
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
                            float *out, float sm_scale, float *ws, cudaStream_t s);
+
+// quant_tc.cu: cuTensorMapEncodeTiled from the driver (nullptr if the driver lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// decode_bf16.cu (the BF16 paged cache that INT2 decoding is compared against)
+struct CacheArgs {
+  int B, Hq, Hkv, num_pages, max_pages;
+  uint16_t *k_pages, *v_pages;  // bf16 [num_pages][Hkv][64][D]
+  int32_t *page_table, *seq_len;
+  uint32_t *err;
+};
+int bf16_attn_ctas(const CacheArgs &c);
+size_t bf16_ws_bytes(const CacheArgs &c);
+// k_new != nullptr: append the new token first (one more launch, chained).
+cudaError_t launch_bf16_decode(const CacheArgs &c, const uint16_t *q, float *out, float sm_scale, float *ws,
+                               cudaStream_t s, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr);
+cudaError_t launch_bf16_append(const CacheArgs &c, const uint16_t *k_new, const uint16_t *v_new, cudaStream_t s);
+cudaError_t launch_bf16_prefill(const CacheArgs &c, int seq, int len, const uint16_t *k, const uint16_t *v,
+                                cudaStream_t s);
 
 // rotation.cu
 size_t rotation_ws_bytes(int d);

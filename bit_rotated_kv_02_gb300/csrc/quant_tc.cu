@@ -668,6 +668,8 @@ __global__ void __launch_bounds__(THREADS, 1) quant_tc_kernel(const __grid_const
   }
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void *p = nullptr;
@@ -679,6 +681,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   }();
   return fn;
 }
+
+namespace {
 
 template <int G>
 cudaError_t launch_g(const CUtensorMap &map, const QArgs &a, int grid, cudaStream_t s) {

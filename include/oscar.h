@@ -254,6 +254,66 @@ oscar_status_t oscar_profile_events(int32_t which, void *start, void *stop);
 oscar_status_t oscar_decode_attention_noalloc(const oscar_pool *pool, const oscar_bf16 *q, float *out,
                                               float softmax_scale, oscar_stream_t stream);
 
+/*
+ * BF16 paged KV cache: the comparison baseline ("超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化",
+ * section "评估结果", Fig. 5, and the arXiv listing's Abstract: batch-1 decoding at 100k context is up
+ * to about 3x faster with the INT2 history than with the history kept in BF16, because fewer KV bytes
+ * are read).  Every token of a sequence is kept in BF16, in 64-token pages, as a paged serving engine
+ * keeps it; these calls let both sides of that comparison run on the same GPU.
+ * Layouts (row-major, innermost last):
+ *   k_pages, v_pages   bf16  [num_pages][Hkv][64][d]   16-byte aligned; token t of sequence b sits at
+ *                            page page_table[b][t / 64], row t % 64
+ *   page_table         int32 [batch][max_pages]
+ *   seq_len            int32 [batch]   tokens held, 0 <= seq_len <= max_pages * 64
+ *   err                uint32 [1]      device error word (OSCAR_DEVERR_* bits)
+ * Limits: head_dim 128, Hq/Hkv in {1, 2, 4, 8}, num_pages * Hkv * 64 < 2^31.
+ */
+typedef struct oscar_bf16_cache {
+  int32_t batch, num_q_heads, num_kv_heads, head_dim;
+  int32_t num_pages, max_pages;
+  oscar_bf16 *k_pages, *v_pages;
+  int32_t *page_table;
+  int32_t *seq_len;
+  uint32_t *err;
+} oscar_bf16_cache;
+
+/*
+ * Bulk prefill of one sequence: k, v bf16 [len][Hkv][d] (16-byte aligned) -> tokens [0, len) of
+ * sequence `seq` through page_table[seq]; sets seq_len[seq] = len.  page_table[seq] must hold
+ * ceil(len / 64) valid pages (an entry outside [0, num_pages) skips that page and sets
+ * OSCAR_DEVERR_PAGE_INDEX).
+ */
+oscar_status_t oscar_bf16_prefill(const oscar_bf16_cache *cache, int32_t seq, int64_t len, const oscar_bf16 *k,
+                                  const oscar_bf16 *v, oscar_stream_t stream);
+
+/*
+ * Append one token per sequence: k_new, v_new bf16 [batch][Hkv][d] (16-byte aligned) are written at
+ * position seq_len[b] (page page_table[b][seq_len / 64], row seq_len % 64); then seq_len[b] += 1.
+ * A full sequence (seq_len == max_pages * 64) sets OSCAR_DEVERR_HISTORY_FULL, a page-table entry
+ * outside the pool OSCAR_DEVERR_PAGE_INDEX; that sequence is left unchanged.
+ */
+oscar_status_t oscar_bf16_append_kv(const oscar_bf16_cache *cache, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
+                                    oscar_stream_t stream);
+
+/*
+ * Decode attention over the BF16 cache: out[b][h] = sum over the seq_len[b] tokens of
+ * softmax(q·k * softmax_scale) * v, query head h reading KV head h / (Hq/Hkv); an empty sequence
+ * gives zeros.
+ *   q     bf16 [batch][Hq][d] (4-byte aligned);  out  fp32 [batch][Hq][d]
+ *   ws    workspace of at least oscar_bf16_decode_workspace_size() bytes (split partials)
+ */
+oscar_status_t oscar_bf16_decode_workspace_size(const oscar_bf16_cache *cache, size_t *bytes);
+oscar_status_t oscar_bf16_decode_attention(const oscar_bf16_cache *cache, const oscar_bf16 *q, float *out,
+                                           float softmax_scale, void *ws, size_t ws_bytes, oscar_stream_t stream);
+
+/*
+ * One decode step over the BF16 cache: oscar_bf16_append_kv then oscar_bf16_decode_attention, with
+ * the same results, launched as one chain.
+ */
+oscar_status_t oscar_bf16_decode_step(const oscar_bf16_cache *cache, const oscar_bf16 *k_new,
+                                      const oscar_bf16 *v_new, const oscar_bf16 *q, float *out,
+                                      float softmax_scale, void *ws, size_t ws_bytes, oscar_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -80,3 +80,40 @@ def test_prefill_and_rotation_validation(lib):
     assert lib.oscar_make_rotation_workspace_size(128) >= 128 * 128 * 8
     assert lib.oscar_calib_covariance_v(100, 2, 128, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, 1 << 30, None) == 1
     assert lib.oscar_append_kv(C.byref(p), None, FAKE, None) == 1
+
+
+def _cache(**kw):
+    c = _lib.oscar_bf16_cache()
+    c.batch, c.num_q_heads, c.num_kv_heads, c.head_dim, c.num_pages, c.max_pages = 2, 8, 2, 128, 16, 8
+    for name, _ in _lib.oscar_bf16_cache._fields_[6:]:
+        setattr(c, name, 0x10000)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2), (dict(num_q_heads=7), 1), (dict(num_q_heads=32), 2), (dict(batch=0), 1),
+    (dict(num_pages=0), 1), (dict(k_pages=None), 1), (dict(seq_len=None), 1), (dict(v_pages=0x10008), 1),
+    (dict(num_pages=1 << 24), 1),
+])
+def test_bf16_cache_validation(lib, kw, status):
+    c = _cache(**kw)
+    assert lib.oscar_bf16_append_kv(C.byref(c), FAKE, FAKE, None) == status
+    assert lib.oscar_last_error_string()
+
+
+def test_bf16_cache_call_validation(lib):
+    c = _cache()
+    n = C.c_size_t(0)
+    assert lib.oscar_bf16_decode_workspace_size(C.byref(c), C.byref(n)) == 0 and n.value > 0
+    assert lib.oscar_bf16_decode_attention(C.byref(c), FAKE, FAKE, 0.088, None, 0, None) == 3
+    assert lib.oscar_bf16_decode_attention(C.byref(c), FAKE, FAKE, 0.088, FAKE, n.value - 1, None) == 3
+    assert lib.oscar_bf16_decode_attention(C.byref(c), FAKE, FAKE, 0.0, FAKE, n.value, None) == 1
+    assert lib.oscar_bf16_decode_attention(C.byref(c), None, FAKE, 0.088, FAKE, n.value, None) == 1
+    assert lib.oscar_bf16_decode_step(C.byref(c), None, FAKE, FAKE, FAKE, 0.088, FAKE, n.value, None) == 1
+    assert lib.oscar_bf16_decode_step(C.byref(c), C.c_void_p(0x10008), FAKE, FAKE, FAKE, 0.088, FAKE, n.value,
+                                      None) == 1
+    assert lib.oscar_bf16_prefill(C.byref(c), 2, 10, FAKE, FAKE, None) == 1          # seq out of range
+    assert lib.oscar_bf16_prefill(C.byref(c), 0, 8 * 64 + 1, FAKE, FAKE, None) == 1  # longer than max_pages*64
+    assert lib.oscar_bf16_prefill(C.byref(c), 0, 10, None, FAKE, None) == 1
