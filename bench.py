@@ -311,7 +311,7 @@ def bf16_compare(args, peak):
     attn_bytes = ctx * HKV * 2 * D * 2 + 4 * math.ceil(ctx / PAGE) + HQ * D * 2
     del caches, ws
     torch.cuda.empty_cache()
-    # the INT2 arm: the headline step over the three-segment pool
+    # the INT2 arm: the headline step over the three-segment pool (4 launches per step)
     NL = 8
     layers = setup_layers(NL, -(-(steps + warm) // NL) + 8)
     ws2 = torch.empty(ok.oscar_decode_workspace_size(layers[0], 0), dtype=torch.uint8, device="cuda")
@@ -624,11 +624,12 @@ def main():
                          "timed_launches": len(hist_ms), "sampling": f"every {EVERY}th step of the timed region"},
             "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
                        statistics.mean(dem_ms) * 1e3,
-                       "note": "append + demote + query rotation kernel, 1 token x 8 KV heads x K/V per launch"},
+                       "note": "append + demote kernel (side stream, alongside the attention), 1 token x 8 KV "
+                               "heads x K/V per launch"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 3,   # append + demote + q rotation, attention, merge
+            "gpu_launches": args.steps * 4,   # append + demote, q rotation, attention, merge
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -280,8 +280,8 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
   oscar_status_t st = check_pool(pool, a);
   if (st != OSCAR_OK) return st;
   if (k_new == nullptr || v_new == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "k_new/v_new NULL");
-  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 7u)
-    return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 8-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
   if (a.g != OSCAR_HEAD_DIM) {

@@ -6,18 +6,23 @@
 // "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache Quantization", Abstract: a
 // custom INT2 attention kernel compatible with paged KV-cache serving.
 //
-// Three launches:
-//   qrot_kernel   q_rot = q · R_k for every query head (row-vector convention), fp32.
+// Launches:
+//   qrot_kernel   q_rot = q · R_k for every query head (row-vector convention), fp32, and per (sequence,
+//                 KV head) the history consumers' query fragments (MMA B operands, score factors).
 //   attn_kernel   BF16 CTAs (first block indices): 64 sink or recent tokens each, plain FMA, one
 //                 partial per chunk.  History CTAs: the flattened (sequence, KV head, page) space is
-//                 cut into equal contiguous ranges, one per CTA; a producer warp streams up to two
+//                 cut into equal contiguous ranges, one per CTA; a producer warp streams up to four
 //                 pages of one segment per ring stage (codes and scale/zero rows) into shared memory
-//                 with 1-D bulk async copies; four consumer warps each score one 16-token tile of
-//                 every page of the stage with warp MMAs (m16n8k16, f16 inputs, f32 accumulate) and
-//                 accumulate P·V the same way, with a lazily rescaled online softmax; one
-//                 (m, l, o_rot) partial per head is written per (CTA, segment).
+//                 with 1-D bulk async copies; four consumer warps each process one whole page per
+//                 stage with warp MMAs (m16n8k16, f16 inputs, f32 accumulate) for Q.K and P.V, with a
+//                 lazily rescaled online softmax; one (m, l, o_rot) partial per head is written per
+//                 (CTA, segment).
 //   merge_kernel  LSE-combines a segment's partials, un-rotates the history part (o · R_v^T),
 //                 adds the BF16 part and normalises.
+// The decode step (oscar_decode_step) adds the demotion kernel on a side stream: the attention kernel
+// reads only what the step leaves unchanged (the history before the step, the window slots other than
+// the new token's, which it takes from k_new / v_new), so it runs alongside the demotion; the merge
+// follows both, adds the demoted token and advances the pool counters.
 //
 // Exactness of the tensor-core arithmetic: a 2-bit code c placed in the low mantissa bits of an
 // fp16 with a zero exponent field is the subnormal c * 4^k * 2^-24 (k = its bit position / 2), so
@@ -51,7 +56,46 @@ struct Args {
   int n_hist;          // history CTAs (block indices n_bf .. n_bf + n_hist - 1)
   int n_bf;            // BF16 CTAs (block indices 0 .. n_bf - 1)
   float *part;         // partial slots [*][G][PART_STRIDE]
+  const uint32_t *frag;  // per (sequence, KV head): the consumers' query fragments (qrot_kernel)
+  // decode-step form: the pool counters still hold the state before the step (its demotion kernel
+  // runs concurrently and leaves them unchanged); the BF16 CTAs attend the window after the step's
+  // append and take the new token from k_new / v_new, the history CTAs the pages before the step.
+  int step;
+  const uint16_t *k_new, *v_new;  // [B][Hkv][D] bf16
 };
+
+// The step's pool state after its demotion and append, from the counters before the step; the same
+// decisions as the demotion kernel (demote when the window is full and the target page is valid;
+// a demotion that cannot be stored blocks the append too).
+struct StepState {
+  bool ok;        // counters valid
+  bool demote;    // the oldest window token moves to history position hist_len
+  bool append;    // the new token is stored
+  bool to_sink;   // ... into the sink (else into the window)
+  int slen, hl, rs, rl;        // before
+  int nslen, nhl, nrs, nrl;    // after
+};
+__device__ __forceinline__ StepState step_state(const PoolArgs &p, int b) {
+  StepState st;
+  st.slen = p.sink_len[b]; st.hl = p.hist_len[b]; st.rs = p.recent_start[b]; st.rl = p.recent_len[b];
+  st.ok = st.slen >= 0 && st.slen <= SINK && st.hl >= 0 && st.rs >= 0 && st.rs < RECENT && st.rl >= 0 &&
+          st.rl <= RECENT;
+  const bool want = st.ok && st.rl == RECENT;
+  st.demote = false;
+  if (want && st.hl / PAGE < p.max_pages) {
+    const int page = p.page_table[(size_t)b * p.max_pages + st.hl / PAGE];
+    st.demote = page >= 0 && page < p.num_pages;
+  }
+  st.append = st.ok && !(want && !st.demote);
+  st.nslen = st.slen; st.nhl = st.hl; st.nrs = st.rs; st.nrl = st.rl;
+  if (st.demote) { st.nhl = st.hl + 1; st.nrs = (st.rs + 1) % RECENT; st.nrl = st.rl - 1; }
+  st.to_sink = st.append && st.nslen < SINK && st.nhl == 0 && st.nrl == 0;
+  if (st.append) {
+    if (st.to_sink) st.nslen += 1;
+    else st.nrl += 1;
+  }
+  return st;
+}
 
 __device__ __forceinline__ int npages_of(const PoolArgs &p, int b) {
   int hl = p.hist_len[b];
@@ -159,9 +203,7 @@ struct Smem {
   uint64_t full[NSTAGE][STAGE_PAGES], empty[NSTAGE][STAGE_PAGES];  // one pair per page slot
   uint64_t csync;                                                    // consumer-warp barrier
   int meta_seg[NSTAGE], meta_ntok[NSTAGE][STAGE_PAGES], meta_flags[NSTAGE];  // flags: 1 last, 2 abort
-  float qr[G][D];
-  float kfac[G], zfac[G];
-  int sigma[G];
+  float qr[G][D];  // BF16 CTAs: the queries
   float wm[CONSUMER_WARPS][G], wl[CONSUMER_WARPS][G], wz[CONSUMER_WARPS][G];
   float wo[CONSUMER_WARPS][G][D];
   float pbuf[CONSUMER_WARPS][G][16];
@@ -169,15 +211,29 @@ struct Smem {
   int b0, kvh0, local0, np0, hl0;
 };
 
+// Query fragments of one (sequence, KV head) as the history consumers use them: per MMA lane, the B
+// operands bq[nt][j][hb] (NT * 16 words) and the score factors kf[nt], zf[nt] of the lane's accumulator
+// columns, stored word-major ([word][32 lanes]) so that a warp loads each word coalesced.
+template <int G>
+__host__ __device__ constexpr int frag_words() { return Smem<G>::NT * 18; }
+
 // ---------------------------------------------------------------------------------------------
 // q_rot = q . R_k for the G query heads of one (sequence, KV head): grid B * Hkv, 512 threads; thread
 // (c, quarter) sums rows 16k .. 16k+15 for k = 2 quarter, 2 quarter + 1 of column c, and the eight
 // partial sums are added as ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) — the order the demotion
 // kernel uses when it rotates the queries in oscar_decode_step, so both paths give the same bits.
+// It also writes the consumers' query fragments (frag_words): per head the exponent sigma with
+// amax(q_rot) * 2^sigma < 2^14, kf = 2^(24 - sigma) * log2(e) * softmax_scale and zf = sum(q_rot) *
+// log2(e) * softmax_scale, and per lane the q_rot values of its B operands, pre-scaled by 2^sigma and by
+// 4^-k for the code placed at bit 2k of its 16-bit lane, split into two fp16 terms.
 template <int G>
-__global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot) {
+__global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot, uint32_t *frag,
+                                                   float sm_log2) {
+  constexpr int NT = Smem<G>::NT;
   __shared__ float qs[G][D];
   __shared__ float part[8][G][D];
+  __shared__ int s_sig[8];
+  __shared__ float s_kf[8], s_zf[8];
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
@@ -201,10 +257,67 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
   __syncthreads();
   if (qt == 0)
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-      qrot[((size_t)b * p.Hq + kvh * G + h) * D + c] =
-          ((part[0][h][c] + part[1][h][c]) + (part[2][h][c] + part[3][h][c])) +
-          ((part[4][h][c] + part[5][h][c]) + (part[6][h][c] + part[7][h][c]));
+    for (int h = 0; h < G; ++h) {
+      const float v = ((part[0][h][c] + part[1][h][c]) + (part[2][h][c] + part[3][h][c])) +
+                      ((part[4][h][c] + part[5][h][c]) + (part[6][h][c] + part[7][h][c]));
+      qrot[((size_t)b * p.Hq + kvh * G + h) * D + c] = v;
+      qs[h][c] = v;  // q is no longer needed
+    }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    const int h = warp;
+    float amax = 0.f, sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float v = qs[h][lane + 32 * k];
+      amax = fmaxf(amax, fabsf(v));
+      sum += v;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, o));
+      sum += __shfl_xor_sync(FULL, sum, o);
+    }
+    if (lane == 0) {
+      int e = 0;
+      if (amax > 0.f) frexpf(amax, &e);
+      const int sig = (amax > 0.f) ? 14 - e : 0;  // amax * 2^sig < 2^14
+      s_sig[h] = sig;
+      s_kf[h] = pow2f(24 - sig) * sm_log2;
+      s_zf[h] = sum * sm_log2;
+    }
+  }
+  __syncthreads();
+  if (warp < NT) {
+    const int nt = warp, gq = lane >> 2, t = lane & 3;
+    uint32_t *fr = frag + (size_t)s * frag_words<G>() * 32 + lane;
+    const int h = 4 * nt + (gq >> 1), split = gq & 1;
+    const bool live = h < G;
+    const float s2 = live ? pow2f(s_sig[h]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int i = 2 * j + hb;  // register index of the token's 16 (word i/8, slot i%8)
+        const int wi = i >> 3, k = i & 7;
+        const int ch_lo = 32 * t + 16 * wi + k, ch_hi = ch_lo + 8;
+        const float f = code_factor_inv(k) * s2;
+        float v[2];
+        const int chs[2] = {ch_lo, ch_hi};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float x = live ? qs[min(h, G - 1)][chs[e]] * f : 0.f;
+          const float hi = __half2float(__float2half_rn(x));
+          v[e] = split == 0 ? hi : x - hi;
+        }
+        fr[(nt * 16 + i) * 32] = pack_half2(v[0], v[1]);
+      }
+    }
+    const int hc = min(4 * nt + t, G - 1);  // accumulator column pair (2t, 2t+1) = head 4 nt + t
+    fr[(NT * 16 + nt) * 32] = __float_as_uint(s_kf[hc]);
+    fr[(NT * 16 + NT + nt) * 32] = __float_as_uint(s_zf[hc]);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -218,7 +331,18 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float *slot = a.part + ((size_t)a.n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5 + chunk) * G * PART_STRIDE;
   if (warp >= CONSUMER_WARPS) return;
-  int slen = p.sink_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
+  int slen, rs, rl;
+  int new_at = -1;  // step form: the chunk-local index of the new token (read from k_new / v_new)
+  if (a.step) {
+    const StepState st = step_state(p, b);
+    slen = st.nslen; rs = st.nrs; rl = st.nrl;
+    if (st.append) {
+      if (st.to_sink) new_at = chunk == 0 ? st.slen : -1;
+      else if (chunk > 0) new_at = st.nrl - 1 - (chunk - 1) * 64;
+    }
+  } else {
+    slen = p.sink_len[b]; rs = p.recent_start[b]; rl = p.recent_len[b];
+  }
   slen = max(0, min(slen, SINK)); rs = max(0, min(rs, RECENT - 1)); rl = max(0, min(rl, RECENT));
   const int n = (chunk == 0) ? slen : max(0, min(64, rl - (chunk - 1) * 64));
   for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
@@ -228,6 +352,10 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
   const uint16_t *vb = chunk == 0 ? p.sink_v + ((size_t)b * p.Hkv + kvh) * SINK * D
                                   : p.recent_v + ((size_t)b * p.Hkv + kvh) * RECENT * D;
   auto row_of = [&](int i) { return chunk == 0 ? i : (rs + (chunk - 1) * 64 + i) % RECENT; };
+  const uint16_t *kn = a.step ? a.k_new + ((size_t)b * p.Hkv + kvh) * D : nullptr;
+  const uint16_t *vn = a.step ? a.v_new + ((size_t)b * p.Hkv + kvh) * D : nullptr;
+  auto krow = [&](int i) { return i == new_at ? kn : kb + (size_t)row_of(i) * D; };
+  auto vrow = [&](int i) { return i == new_at ? vn : vb + (size_t)row_of(i) * D; };
   // QK: lane -> token (lane & 15) of this warp's 16, channel half (lane >> 4)
   const int tk = 16 * warp + (lane & 15), hf = lane >> 4;
   const bool valid = tk < n;
@@ -235,7 +363,7 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
 #pragma unroll
   for (int h = 0; h < G; ++h) dot[h] = 0.f;
   if (valid) {
-    const uint4 *kr = reinterpret_cast<const uint4 *>(kb + (size_t)row_of(tk) * D + hf * 64);
+    const uint4 *kr = reinterpret_cast<const uint4 *>(krow(tk) + hf * 64);
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = kr[i];
@@ -274,7 +402,7 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const int t2 = 16 * warp + j;
-    vv[j] = t2 < n ? reinterpret_cast<const uint2 *>(vb + (size_t)row_of(t2) * D)[lane] : make_uint2(0, 0);
+    vv[j] = t2 < n ? reinterpret_cast<const uint2 *>(vrow(t2))[lane] : make_uint2(0, 0);
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -351,61 +479,17 @@ __device__ __forceinline__ void reset(WarpState<G> &ws) {
 
 // Segment setup (consumer threads only): load q_rot, derive per-head scaling, build B fragments.
 template <int G>
-__device__ __forceinline__ void setup_segment(const Args &a, Smem<G> &sm, int b, int kvh,
-                                              uint32_t (&bq)[Smem<G>::NT][8][2], uint32_t &par) {
+__device__ __forceinline__ void setup_segment(const Args &a, int b, int kvh, uint32_t (&bq)[Smem<G>::NT][8][2],
+                                              float (&kf)[Smem<G>::NT], float (&zf)[Smem<G>::NT]) {
   constexpr int NT = Smem<G>::NT;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float *src = a.qrot + ((size_t)b * a.p.Hq + kvh * G) * D;
-  for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = src[i];
-  consumer_sync(sm, par, a.p.err);
-  for (int h = warp; h < G; h += CONSUMER_WARPS) {
-    float amax = 0.f, sum = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float v = sm.qr[h][lane + 32 * k];
-      amax = fmaxf(amax, fabsf(v));
-      sum += v;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, o));
-      sum += __shfl_xor_sync(FULL, sum, o);
-    }
-    if (lane == 0) {
-      int e = 0;
-      if (amax > 0.f) frexpf(amax, &e);
-      const int sig = (amax > 0.f) ? 14 - e : 0;  // amax * 2^sig < 2^14
-      sm.sigma[h] = sig;
-      sm.kfac[h] = pow2f(24 - sig) * a.sm_log2;
-      sm.zfac[h] = sum * a.sm_log2;
-    }
-  }
-  consumer_sync(sm, par, a.p.err);
-  const int gq = lane >> 2, t = lane & 3;
+  if (a.step) pdl_wait();  // the step's query rotation (the previous kernel on this stream) has completed
+  const uint32_t *fr = a.frag + (size_t)(b * a.p.Hkv + kvh) * frag_words<G>() * 32 + (threadIdx.x & 31);
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    const int h = 4 * nt + (gq >> 1), split = gq & 1;
-    const bool live = h < G;
-    const float s2 = live ? pow2f(sm.sigma[h]) : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const int i = 2 * j + hb;             // register index of the token's 16 (word i/8, slot i%8)
-        const int wi = i >> 3, k = i & 7;
-        const int ch_lo = 32 * t + 16 * wi + k, ch_hi = ch_lo + 8;
-        const float f = code_factor_inv(k) * s2;
-        float v[2];
-        const int chs[2] = {ch_lo, ch_hi};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float x = live ? sm.qr[h][chs[e]] * f : 0.f;
-          const float hi = __half2float(__float2half_rn(x));
-          v[e] = split == 0 ? hi : x - hi;
-        }
-        bq[nt][j][hb] = pack_half2(v[0], v[1]);
-      }
-    }
+    for (int i = 0; i < 16; ++i) bq[nt][i >> 1][i & 1] = fr[(nt * 16 + i) * 32];
+    kf[nt] = __uint_as_float(fr[(NT * 16 + nt) * 32]);
+    zf[nt] = __uint_as_float(fr[(NT * 16 + NT + nt) * 32]);
   }
 }
 
@@ -465,56 +549,69 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
-// One page in one consumer warp: all 64 tokens (four 16-token tiles); ntok = valid tokens (1..64).
-// Lane (g, t) owns the rows g + 8j (j = 0..7: tile j/2, row half j%2) of the QK accumulators for head
-// column t; the softmax weights are formed in that layout, split into fp16 hi + lo and transposed
-// with movmatrix into the B operand of the P.V products, whose A operand pairs tokens (2t, 2t+1).
-template <int G, bool FULL>
-__device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, const Smem<G> &sm, WarpState<G> &ws,
-                                          const uint32_t (&bq)[Smem<G>::NT][8][2]) {
+// One page in one consumer warp: all 64 tokens as four 16-row MMA tiles; ntok = valid tokens (1..64).
+// MMA row 16 mt + g (+ 8) of tile mt holds token 8 g + 2 mt (+ 1), so lane (g, t) owns the eight
+// consecutive tokens 8 g .. 8 g + 7 (its accumulator rows j = 2 mt + e) and reads their scale/zero
+// rows with one 16-byte load per array.  The softmax weights are formed in the QK accumulator layout
+// (column pair 2t, 2t+1 = head t's hi and lo query terms), split into fp16 hi + lo and transposed with
+// movmatrix into the B operand of the P.V products, whose A operand therefore takes, for k-index
+// pairs (2t, 2t+1) and (2t+8, 2t+9) of tile mt, the tokens 16 t + 2 mt (+ 8) and 16 t + 2 mt + 1 (+ 8).
+// Rows past ntok are masked: score -inf, value scale and zero 0 (their codes are finite integers).
+template <int G>
+__device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState<G> &ws,
+                                          const uint32_t (&bq)[Smem<G>::NT][8][2], const float (&kf_)[Smem<G>::NT],
+                                          const float (&zf_)[Smem<G>::NT]) {
   constexpr int NT = Smem<G>::NT;
   constexpr bool ALL_LIVE = (G % 4) == 0;
   const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
-  // ---- QK: A = K codes (tokens 16mt + g, 16mt + g + 8; lane t owns channels 32t .. 32t+31) ----
+  // ---- QK: A = K codes (lane t owns channels 32t .. 32t+31 of its two tokens per tile) ----
   float S[4][NT][4];
-  const uint8_t *kc = pb + OFF_KC + gq * 32 + 8 * t;
+  const uint8_t *kc = pb + OFF_KC + gq * 256 + 8 * t;
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
-    if (FULL || 16 * mt < ntok) {
-      const uint2 ka = *reinterpret_cast<const uint2 *>(kc + (16 * mt) * 32);
-      const uint2 kb = *reinterpret_cast<const uint2 *>(kc + (16 * mt + 8) * 32);
-      uint32_t T0[16], T1[16];
-      unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
-      unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
+    const uint2 ka = *reinterpret_cast<const uint2 *>(kc + 64 * mt);
+    const uint2 kb = *reinterpret_cast<const uint2 *>(kc + 64 * mt + 32);
+    uint32_t T0[16], T1[16];
+    unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
+    unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          mma16816(S[mt][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+      for (int j = 0; j < 8; ++j)
+        mma16816(S[mt][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+  }
+  // ---- scale / zero of the lane's tokens 8g .. 8g+7 ----
+  const uint4 ks4 = *reinterpret_cast<const uint4 *>(pb + OFF_KS + 16 * gq);
+  const uint4 kz4 = *reinterpret_cast<const uint4 *>(pb + OFF_KZ + 16 * gq);
+  const uint4 vs4 = *reinterpret_cast<const uint4 *>(pb + OFF_VS + 16 * gq);
+  const uint4 vz4 = *reinterpret_cast<const uint4 *>(pb + OFF_VZ + 16 * gq);
+  const int nvalid = ntok - 8 * gq;  // rows j < nvalid are tokens of the page
+  float ks[8], kz[8], vs[8], vz[8];
+  {
+    const uint32_t kw[4] = {ks4.x, ks4.y, ks4.z, ks4.w}, zw[4] = {kz4.x, kz4.y, kz4.z, kz4.w};
+    const uint32_t vw[4] = {vs4.x, vs4.y, vs4.z, vs4.w}, uw[4] = {vz4.x, vz4.y, vz4.z, vz4.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ks[2 * i] = __uint_as_float(kw[i] << 16); ks[2 * i + 1] = __uint_as_float(kw[i] & 0xffff0000u);
+      kz[2 * i] = __uint_as_float(zw[i] << 16); kz[2 * i + 1] = __uint_as_float(zw[i] & 0xffff0000u);
+      vs[2 * i] = __uint_as_float(vw[i] << 16); vs[2 * i + 1] = __uint_as_float(vw[i] & 0xffff0000u);
+      vz[2 * i] = __uint_as_float(uw[i] << 16); vz[2 * i + 1] = __uint_as_float(uw[i] & 0xffff0000u);
     }
   }
-  // ---- per-row scale / zero of the lane's 8 rows ----
-  const uint16_t *Ks = reinterpret_cast<const uint16_t *>(pb + OFF_KS) + gq;
-  const uint16_t *Kz = reinterpret_cast<const uint16_t *>(pb + OFF_KZ) + gq;
-  const uint16_t *Vs = reinterpret_cast<const uint16_t *>(pb + OFF_VS) + gq;
-  const uint16_t *Vz = reinterpret_cast<const uint16_t *>(pb + OFF_VZ) + gq;
-  float ks[8], kz[8], vs[8], vz[8];
+  if (nvalid < 8) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const bool valid = FULL || gq + 8 * j < ntok;
-    ks[j] = bf16_to_f32(Ks[8 * j]);
-    kz[j] = bf16_to_f32(Kz[8 * j]);
-    vs[j] = valid ? bf16_to_f32(Vs[8 * j]) : 0.f;
-    vz[j] = valid ? bf16_to_f32(Vz[8 * j]) : 0.f;
+    for (int j = 0; j < 8; ++j)
+      if (j >= nvalid) { vs[j] = 0.f; vz[j] = 0.f; }
   }
   // ---- weight scaling exponent tau: weights p * vs * 2^tau stay below 2^14 ----
+  // (a warp vote on the lane maxima; the cross-lane maximum is formed only when tau must change)
   float vmax = fmaxf(max3f(vs[0], vs[1], vs[2]), max3f(max3f(vs[3], vs[4], vs[5]), vs[6], vs[7]));
-  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 4));
-  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 8));
-  vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 16));
-  if (vmax >= ws.tau_lim && vmax > 0.f) {
+  if (__any_sync(FULL, vmax >= ws.tau_lim && vmax > 0.f)) {
+    vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 4));
+    vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 8));
+    vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 16));
     int e;
     frexpf(vmax, &e);
     const int tnew = max(-100, min(100, WEXP - e));
@@ -537,27 +634,32 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, const Sme
   for (int nt = 0; nt < NT; ++nt) {
     const int h = ALL_LIVE ? 4 * nt + t : min(4 * nt + t, G - 1);
     const bool live_h = ALL_LIVE || 4 * nt + t < G;
-    const float kf = sm.kfac[h], zf = sm.zfac[h];
+    const float kf = kf_[nt], zf = zf_[nt];
+    (void)h;
     float sc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int mt = j >> 1, e = j & 1;
-      sc[j] = (FULL || gq + 8 * j < ntok) ? fmaf((S[mt][nt][2 * e] + S[mt][nt][2 * e + 1]) * ks[j], kf, kz[j] * zf)
-                                          : -INFINITY;
+      const float v = fmaf((S[mt][nt][2 * e] + S[mt][nt][2 * e + 1]) * ks[j], kf, kz[j] * zf);
+      sc[j] = j < nvalid ? v : -INFINITY;
     }
+    // lazy rescaling: the head's maximum is formed across lanes only when some row exceeds the
+    // reference by more than 2^LAZY (a warp vote on the lane maxima decides)
     float tmax = fmaxf(max3f(sc[0], sc[1], sc[2]), max3f(max3f(sc[3], sc[4], sc[5]), sc[6], sc[7]));
-    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 4));
-    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 8));
-    tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 16));
-    if (tmax > ws.m2[nt] + (float)LAZY) {
-      const float alpha = (ws.m2[nt] == -INFINITY) ? 0.f : fast_exp2(ws.m2[nt] - tmax);
-      ws.l[nt] *= alpha;
-      ws.oz[nt] *= alpha;
+    if (__any_sync(FULL, tmax > ws.m2[nt] + (float)LAZY)) {
+      tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 4));
+      tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, 16));
+      if (tmax > ws.m2[nt] + (float)LAZY) {
+        const float alpha = (ws.m2[nt] == -INFINITY) ? 0.f : fast_exp2(ws.m2[nt] - tmax);
+        ws.l[nt] *= alpha;
+        ws.oz[nt] *= alpha;
 #pragma unroll
-      for (int m8 = 0; m8 < 8; ++m8)
+        for (int m8 = 0; m8 < 8; ++m8)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) ws.O[nt][m8][r] *= alpha;
-      ws.m2[nt] = tmax;
+          for (int r = 0; r < 4; ++r) ws.O[nt][m8][r] *= alpha;
+        ws.m2[nt] = tmax;
+      }
     }
     // p * 2^tau = exp2(score - (m - tau)); l and the zero-point sum take p itself
     const float mref = ws.m2[nt] - (float)ws.tau;
@@ -569,8 +671,8 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, const Sme
       lsum += pr;
       zsum = fmaf(pr, vz[j], zsum);
       const float w = live_h ? pr * vs[j] : 0.f;
-      const __half hh = __float2half_rn(w);
-      wp[j] = pack_half2(__half2float(hh), w - __half2float(hh));  // (hi, lo)
+      const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
+      wp[j] = pack_half2(hi, w - hi);                                      // (hi, lo)
     }
     ws.l[nt] = fmaf(lsum, untau, ws.l[nt]);
     ws.oz[nt] = fmaf(zsum, untau, ws.oz[nt]);
@@ -580,13 +682,12 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, const Sme
       bw[nt][mt][1] = movmatrix_trans(wp[2 * mt + 1]);
     }
   }
-  // ---- P.V per tile: A = V codes^T (tokens 2t, 2t+1 | 2t+8, 2t+9; group g: channels 16g .. 16g+15) ----
-  const uint32_t *vrow = reinterpret_cast<const uint32_t *>(pb + OFF_VC) + gq + 2 * t * 8;
+  // ---- P.V per tile: A = V codes^T (group g: channels 16g .. 16g+15, one 32-bit word per token) ----
+  const uint32_t *vrow = reinterpret_cast<const uint32_t *>(pb + OFF_VC) + 16 * t * 8 + gq;
 #pragma unroll
   for (int mt = 0; mt < 4; ++mt) {
-    if (!(FULL || 16 * mt < ntok)) continue;
-    const uint32_t *vr = vrow + 16 * mt * 8;
-    const uint32_t xa = vr[0], xb = vr[8], xc = vr[64], xd = vr[72];
+    const uint32_t xa = vrow[16 * mt], xb = vrow[64 + 16 * mt];           // tokens 16t+2mt, 16t+8+2mt
+    const uint32_t xc = vrow[16 * mt + 8], xd = vrow[64 + 16 * mt + 8];   // the same + 1
     uint32_t VA[16], VB[16];
     unpack16(prmt(xa, xb, 0x5410), VA, 0); unpack16(prmt(xa, xb, 0x7632), VA, 8);
     unpack16(prmt(xc, xd, 0x5410), VB, 0); unpack16(prmt(xc, xd, 0x7632), VB, 8);
@@ -702,10 +803,11 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   WarpState<G> ws;
   reset(ws);
   uint32_t bq[NT][8][2];
+  float kf[NT], zf[NT];
   // the first segment's query setup needs no pages: it overlaps the first bulk copies
   int cur = sm.b0 * p.Hkv + sm.kvh0, stage = 0;
   ws.csync_par = 0;
-  setup_segment(a, sm, sm.b0, sm.kvh0, bq, ws.csync_par);
+  setup_segment<G>(a, sm.b0, sm.kvh0, bq, kf, zf);
   uint32_t phase = 0;
   while (true) {
     if (!mbar_wait_bounded(&sm.full[stage][warp], phase)) {
@@ -718,12 +820,11 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     if (seg != cur) {
       if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
       cur = seg;
-      setup_segment(a, sm, seg / p.Hkv, seg % p.Hkv, bq, ws.csync_par);
+      setup_segment<G>(a, seg / p.Hkv, seg % p.Hkv, bq, kf, zf);
     }
     const int ntok = sm.meta_ntok[stage][warp];
     const uint8_t *pb = sm.ring[stage] + warp * PAGE_BYTES;
-    if (ntok == PAGE) page_pass<G, true>(pb, ntok, sm, ws, bq);
-    else if (ntok > 0) page_pass<G, false>(pb, ntok, sm, ws, bq);
+    if (ntok > 0) page_pass<G>(pb, ntok, ws, bq, kf, zf);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage][warp]);
     if (flags & 1) break;
@@ -736,7 +837,11 @@ template <int G>
 __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
-  pdl_wait();
+  // Step form: nothing this kernel reads is written by the step's demotion kernel (pool counters, page
+  // tables, history pages before the step, the window slots the BF16 CTAs read, q and R_k), so it runs
+  // alongside it; every thread waits for it before the grid may complete, so that the merge that
+  // follows sees the demoted token and q_rot.
+  if (!a.step) pdl_wait();
   pdl_trigger();
   if ((int)blockIdx.x < a.n_bf) bf16_role<G>(a, sm);
   else hist_role<G>(a, sm, (int)blockIdx.x - a.n_bf);
@@ -753,17 +858,52 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
 constexpr int MT = 512;
 constexpr int MAXPARTS = 1040;
 template <int G>
-__global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out) {
+// Step form (qrot != NULL): the pool counters still hold the state before the step; the token the
+// step demoted (history position hist_len) enters as one more partial (m = its score, l = 1, o = its
+// dequantized rotated value), and the last CTA of a sequence to finish (arrival counter pool.sync[b])
+// advances the counters to the state after the step.
+__global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
+                                                   const float *qrot, float sm_log2) {
   constexpr int OV = 36;  // partials per slice issued at once (4 slices: 144 partials)
   __shared__ float wgt[MAXPARTS], lsum[MAXPARTS];
   __shared__ float red[MT / 32];
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
   __shared__ long long s_pref, s_total;
+  __shared__ float s_md;
+  __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
+  const bool step = qrot != nullptr;
+  StepState st{};
+  float od = 0.f;  // step form: the demoted token's dequantized rotated value at channel ch
+  if (step) {
+    st = step_state(p, b);
+    if (st.demote) {
+      const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
+                         st.hl % PAGE;
+      if (warp == 0) {
+        const float4 q4 = reinterpret_cast<const float4 *>(qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
+        const uint32_t cb = p.codes_k[row * (D / 4) + lane];  // channels 4 lane .. 4 lane + 3
+        float dc = q4.x * (float)(cb & 3u) + q4.y * (float)((cb >> 2) & 3u) + q4.z * (float)((cb >> 4) & 3u) +
+                   q4.w * (float)((cb >> 6) & 3u);
+        float sq = (q4.x + q4.y) + (q4.z + q4.w);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          dc += __shfl_xor_sync(FULL, dc, o);
+          sq += __shfl_xor_sync(FULL, sq, o);
+        }
+        if (lane == 0)
+          s_md = sm_log2 * fmaf(bf16_to_f32(p.scale_k[row]), dc, bf16_to_f32(p.zero_k[row]) * sq);
+      }
+      const uint32_t cv = (p.codes_v[row * (D / 4) + ch / 4] >> (2 * (ch & 3))) & 3u;
+      od = fmaf((float)cv, bf16_to_f32(p.scale_v[row]), bf16_to_f32(p.zero_v[row]));
+    } else if (tid == 0) {
+      s_md = -INFINITY;
+    }
+  }
   if (warp == 0) {
     long long total;
     int bb, kk, ll;
@@ -819,6 +959,8 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   float M = red[0];
 #pragma unroll
   for (int w = 1; w < MT / 32; ++w) M = fmaxf(M, red[w]);
+  const float md = step ? s_md : -INFINITY;
+  M = fmaxf(M, md);
   __syncthreads();
   float ls = 0.f;
   for (int i = tid; i < nparts; i += MT) {
@@ -833,8 +975,10 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   float L = 0.f;
 #pragma unroll
   for (int w = 0; w < MT / 32; ++w) L += red[w];
+  const float ed = md == -INFINITY ? 0.f : exp2f(md - M);
+  L += ed;
   // weighted sums: history partials (rotated space) and BF16 partials (original space) apart
-  float acc = 0.f, accb = 0.f;
+  float acc = sl == 0 ? ed * od : 0.f, accb = 0.f;
 #pragma unroll
   for (int k = 0; k < OV; ++k) {
     const int i = sl + 4 * k;
@@ -865,6 +1009,24 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   if (sl == 0) {
     const float o = Osl[0][ch] + (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
     out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
+  }
+  if (!step) return;
+  // every CTA of the sequence has read the counters before it arrives; the last one advances them
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    s_last = atomicAdd(p.sync + b, 1) == (int)(gridDim.x * gridDim.y) - 1;
+  }
+  __syncthreads();
+  if (s_last && tid == 0) {
+    __threadfence();
+    if (st.ok && (st.demote || st.append)) {
+      p.sink_len[b] = st.nslen;
+      p.hist_len[b] = st.nhl;
+      p.recent_start[b] = st.nrs;
+      p.recent_len[b] = st.nrl;
+    }
+    p.sync[b] = 0;
   }
 }
 
@@ -911,7 +1073,27 @@ int v1_hist_ctas(const PoolArgs &p) {
 size_t v1_ws_bytes(const PoolArgs &p) {
   const int G = p.Hq / p.Hkv;
   const size_t slots = (size_t)v1_hist_ctas(p) + (size_t)p.B * p.Hkv * 6;
-  return (size_t)p.B * p.Hq * D * sizeof(float) + slots * G * PART_STRIDE * sizeof(float);
+  const size_t frag = (size_t)p.B * p.Hkv * (G > 4 ? 36 : 18) * 32 * sizeof(uint32_t);
+  return (size_t)p.B * p.Hq * D * sizeof(float) + frag + slots * G * PART_STRIDE * sizeof(float);
+}
+
+// A non-blocking side stream and a fork/join event pair per host thread and device (created on first
+// use, kept for the life of the process).
+static cudaError_t side_stream(cudaStream_t &s, cudaEvent_t &fork, cudaEvent_t &join) {
+  struct Side { cudaStream_t s = nullptr; cudaEvent_t fork = nullptr, join = nullptr; };
+  thread_local Side side[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  Side &x = side[dev];
+  if (x.s == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  s = x.s; fork = x.fork; join = x.join;
+  return cudaSuccess;
 }
 
 // k_new != NULL: the step form (append + demote + query rotation fused in the demote kernel);
@@ -923,24 +1105,44 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.p = p;
   a.q = q;
   a.qrot = ws;
-  a.part = ws + (size_t)p.B * p.Hq * D;
+  uint32_t *frag = reinterpret_cast<uint32_t *>(ws + (size_t)p.B * p.Hq * D);
+  a.frag = frag;
+  a.part = reinterpret_cast<float *>(frag + (size_t)p.B * p.Hkv * v1::frag_words<G>() * 32);
   a.sm_log2 = sm_scale * 1.4426950408889634f;
   a.n_hist = v1_hist_ctas(p);
+  if (k_new != nullptr) {  // leave the demotion kernel's CTAs their slots (each displaces two of ours)
+    const int r = 4 * p.B * p.Hkv;
+    a.n_hist = a.n_hist - (r < a.n_hist / 4 ? r : a.n_hist / 4);
+  }
   const int nbf = p.B * p.Hkv * 5;
   a.n_bf = nbf;
   const int smem = (int)sizeof(v1::Smem<G>);
   cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  if (k_new != nullptr) {
-    if ((e = launch_demote(p, nullptr, 2, k_new, v_new, s, q, ws)) != cudaSuccess) return e;
-  } else if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws)) != cudaSuccess) {
-    return e;
+  // Step form: the demotion kernel (counters left unchanged), the query rotation and the attention
+  // kernel run alongside one another; the merge adds the demoted token and advances the counters.
+  a.step = k_new != nullptr;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  // Step form: the demotion runs on a side stream forked from and joined back into the caller's
+  // stream, alongside the query rotation and the attention kernel; the merge follows both.
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (a.step) {
+    if ((e = side_stream(side, fork, join)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(side, fork, 0)) != cudaSuccess) return e;
+    if ((e = launch_demote(p, nullptr, 3, k_new, v_new, side)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(join, side)) != cudaSuccess) return e;
   }
+  if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2)) !=
+      cudaSuccess)
+    return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
+  if (a.step && (e = cudaStreamWaitEvent(s, join, 0)) != cudaSuccess) return e;
   return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), 0, s, p, (const float *)a.part, a.n_hist,
-                    out);
+                    out, a.step ? (const float *)ws : nullptr, a.sm_log2);
 }
 
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,

@@ -48,7 +48,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // quantize.cu
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
-                          const uint16_t *v_new, cudaStream_t s, const uint16_t *q = nullptr, float *qrot = nullptr);
+                          const uint16_t *v_new, cudaStream_t s);
 cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride, const float *R32,
                                  const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
                                  const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s);
@@ -65,7 +65,8 @@ cudaError_t launch_decode(const PoolArgs &p, const uint16_t *q, float *out, floa
 size_t v1_ws_bytes(const PoolArgs &p);
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
                              cudaStream_t s);
-// Append + demote + query rotation in one kernel, then attention and merge (group size 128).
+// The decode step for group size 128: the demotion (on a side stream) alongside the query rotation and
+// the attention kernel, then the merge.
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
                            float *out, float sm_scale, float *ws, cudaStream_t s);
 

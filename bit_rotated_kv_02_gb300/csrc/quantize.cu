@@ -19,20 +19,15 @@ namespace oscar {
 // the last CTA to arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival
 // counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
-// mode 2: as mode 0, then append k_new/v_new.  With q != NULL the K CTA also writes the rotated queries
-// q_rot = q . R_k of its KV head's query heads (the decode step's query rotation, fused here because
-// this CTA already holds R_k in registers), summed in the order of v1::qrot_kernel.
+// mode 2: as mode 0, then append k_new/v_new; mode 3: as mode 2 but the counters are left unchanged
+// (the decode step's merge kernel advances them once every reader of the step is done).
 constexpr int DEMOTE_WARPS = 8, DEMOTE_ROWS = D / DEMOTE_WARPS;  // 16 rows of R per warp
 constexpr int RS_LD = D + 4;  // padded row stride of the shared copy of R (16-byte rows, 4-way reads)
 constexpr size_t DEMOTE_SMEM = (size_t)D * RS_LD * sizeof(float);
 __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const int32_t *mask, int mode,
-                                                            const uint16_t *k_new, const uint16_t *v_new,
-                                                            const uint16_t *q, float *qrot) {
-  constexpr int GMAX = 8;
+                                                            const uint16_t *k_new, const uint16_t *v_new) {
   __shared__ float xs[D];
   __shared__ float pacc[DEMOTE_WARPS][32][4], psab[DEMOTE_WARPS][32][4];
-  __shared__ float qsm[GMAX][D];
-  __shared__ float4 qpart[DEMOTE_WARPS][GMAX][32];
   __shared__ int s_ok;
   extern __shared__ float4 rs4[];  // this CTA's R, row stride RS_LD floats, for the Dot2 tier
   pdl_wait();
@@ -48,15 +43,10 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
 #pragma unroll
     for (int i = 0; i < DEMOTE_ROWS; ++i) rs4[(DEMOTE_ROWS * warp + i) * (RS_LD / 4) + lane] = rrow[i];
   }
-  // the appended token's row (mode 2; warp 0), also independent of the counters
+  // the appended token's row (modes 2 and 3; warp 0), also independent of the counters
   uint2 newrow = make_uint2(0u, 0u);
-  if (mode == 2 && warp == 0)
+  if (mode >= 2 && warp == 0)
     newrow = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[lane];
-  // fused query rotation (q != NULL): q of the G query heads of this KV head
-  const int G = p.Hq / p.Hkv;
-  if (q != nullptr && kv == 0)
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-      qsm[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + (size_t)kvh * G) * D + i]);
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
   const bool want = counters_ok && ((mode == 1) ? (mask[b] != 0 && rl > 0) : (rl == RECENT));
@@ -126,39 +116,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
-  if (q != nullptr && kv == 0) {
-    // q_rot[h] = q[h] . R_k: warp w sums rows 16w .. 16w+15 (already in registers)
-    for (int h = 0; h < G; ++h) {
-      float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int i = 0; i < DEMOTE_ROWS; ++i) {
-        const float qi = qsm[h][DEMOTE_ROWS * warp + i];
-        acc4.x = fmaf(qi, rrow[i].x, acc4.x);
-        acc4.y = fmaf(qi, rrow[i].y, acc4.y);
-        acc4.z = fmaf(qi, rrow[i].z, acc4.z);
-        acc4.w = fmaf(qi, rrow[i].w, acc4.w);
-      }
-      qpart[warp][h][lane] = acc4;
-    }
-  }
-  __syncthreads();
-  if (q != nullptr && kv == 0) {
-    for (int h = warp; h < G; h += DEMOTE_WARPS) {
-      float4 pr[DEMOTE_WARPS];
-#pragma unroll
-      for (int w = 0; w < DEMOTE_WARPS; ++w) pr[w] = qpart[w][h][lane];
-      // ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)), as v1::qrot_kernel
-      auto t8 = [&](float a0, float a1, float a2, float a3, float a4, float a5, float a6, float a7) {
-        return ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
-      };
-      reinterpret_cast<float4 *>(qrot + ((size_t)b * p.Hq + (size_t)kvh * G + h) * D)[lane] = make_float4(
-          t8(pr[0].x, pr[1].x, pr[2].x, pr[3].x, pr[4].x, pr[5].x, pr[6].x, pr[7].x),
-          t8(pr[0].y, pr[1].y, pr[2].y, pr[3].y, pr[4].y, pr[5].y, pr[6].y, pr[7].y),
-          t8(pr[0].z, pr[1].z, pr[2].z, pr[3].z, pr[4].z, pr[5].z, pr[6].z, pr[7].z),
-          t8(pr[0].w, pr[1].w, pr[2].w, pr[3].w, pr[4].w, pr[5].w, pr[6].w, pr[7].w));
-    }
-  }
-  const bool append = mode == 2 && counters_ok && !blocked;
+  const bool append = mode >= 2 && counters_ok && !blocked;
   int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
   if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
   if (append && warp == 0) {
@@ -174,6 +132,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     if (nslen < SINK && nhl == 0 && nrl == 0) nslen += 1;
     else nrl += 1;
   }
+  if (mode == 3) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -212,12 +171,11 @@ __global__ void set_counters_kernel(PoolArgs p, int b, int slen, int hl, int rl)
 
 // ---- launchers ------------------------------------------------------------------------------
 cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, const uint16_t *k_new,
-                          const uint16_t *v_new, cudaStream_t s, const uint16_t *q, float *qrot) {
+                          const uint16_t *v_new, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(demote_append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEMOTE_SMEM);
   if (e != cudaSuccess) return e;
   profile_begin(OSCAR_PROFILE_DEMOTE, s);
-  e = launch_pdl(demote_append_kernel, dim3(2 * p.Hkv, p.B), dim3(256), DEMOTE_SMEM, s, p, mask, mode, k_new, v_new, q,
-                 qrot);
+  e = launch_pdl(demote_append_kernel, dim3(2 * p.Hkv, p.B), dim3(256), DEMOTE_SMEM, s, p, mask, mode, k_new, v_new);
   profile_end(OSCAR_PROFILE_DEMOTE, s);
   return e;
 }

@@ -91,8 +91,10 @@ def test_decode_after_appends():
 
 @pytest.mark.parametrize("G,g", [(4, 128), (8, 128), (2, 32)])
 def test_decode_step_matches_oracle_and_separate_calls(G, g):
-    """oscar_decode_step (append + demote + query rotation fused for group 128) gives the oracle's result
-    at every step, and exactly what oscar_append_kv followed by oscar_decode_attention gives."""
+    """oscar_decode_step gives the oracle's result at every step and, up to float32 rounding, what
+    oscar_append_kv followed by oscar_decode_attention gives (for group 128 the step's attention runs
+    alongside its demotion and takes the demoted token as a partial of its own); both leave the pool
+    byte for byte as the oracle does."""
     seed, Hkv = 640 + G + g, 2
     Hq = G * Hkv
     O, P, q = _setup([330, 1100], Hq, Hkv, g, seed, extra_pages=2)
@@ -107,12 +109,14 @@ def test_decode_step_matches_oracle_and_separate_calls(G, g):
         out = ok.oscar_decode_step(P, kd, vd, qd)
         ok.oscar_append_kv(P2, kd, vd)
         out2 = ok.oscar_decode_attention(P2, qd)
-        assert torch.equal(out, out2)
-        if t % 7 == 0:
+        torch.testing.assert_close(out, out2, rtol=1e-5, atol=1e-4)
+        if t % 7 == 0 or t == 19:
             helpers.assert_attention_close(out.cpu().numpy(), O.decode(qt))
+            helpers.assert_pools_equal(O, P)
     torch.cuda.synchronize()
     helpers.assert_pools_equal(O, P)
-    assert P.err() == 0
+    helpers.assert_pools_equal(O, P2)
+    assert P.err() == 0 and P2.err() == 0
 
 
 def test_100k_context_sampled_heads():
