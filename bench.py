@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed", "bf16-compare"],
+    ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed", "bf16-compare",
+                                           "shared-prefix"],
                     default="decode100k",
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -340,6 +341,57 @@ def bf16_compare(args, peak):
              "gpu_launches": steps * 3}]
 
 
+def shared_prefix(args, peak):
+    """Decode step throughput against the fraction of history pages shared by every sequence of the
+    batch (a common prompt prefix held once through the page tables: the prefix-cache use of the paged
+    history, "评估结果" Fig. 6).  16 sequences x 32k context, Qwen3-8B layer shapes."""
+    import numpy as np
+    import torch
+    import bit_rotated_kv_02_gb300 as ok
+    import synth
+    B, L, Hq, Hkv = 16, 32_768, HQ, HKV
+    hist = L - SINK - RECENT
+    steps = max(3, min(args.steps, 300))
+    warm = max(3, min(args.warmup, 20))
+    own = -(-(hist + steps + warm + 8) // PAGE)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(6161)
+    chan = torch.from_numpy(synth.outlier_channels(2024, Hkv, D, 4).astype(np.int64)).cuda()
+    Rk, Rv = _gpu_rotations(ok, Hkv, D, 100), _gpu_rotations(ok, Hkv, D, 200)
+    clip = torch.full((Hkv,), 0.9)
+    lines = []
+    for frac in (0.0, 0.5, 0.9):
+        share = int(frac * (hist // PAGE))
+        P = ok.Pool(B, Hq, Hkv, 128, B * own, own, Rk, Rv, clip, clip)
+        pt = torch.randperm(B * own, generator=gen, device="cuda").to(torch.int32).reshape(B, own)
+        pt[1:, :share] = pt[0, :share]
+        P.set_page_table(pt)
+        K0, V0 = _gpu_kv(gen, L, Hkv, chan), _gpu_kv(gen, L, Hkv, chan)
+        ok.oscar_prefill_pool(P, 0, K0, V0)
+        for b in range(1, B):
+            K, V = _gpu_kv(gen, L, Hkv, chan), _gpu_kv(gen, L, Hkv, chan)
+            n = SINK + share * PAGE
+            K[:n], V[:n] = K0[:n], V0[:n]
+            ok.oscar_prefill_pool_shared(P, b, K, V, share)
+        del K0, V0
+        q = (torch.randn((B, Hq, D), generator=gen, device="cuda") * 3).to(torch.bfloat16)
+        kn, vn = _gpu_kv(gen, B, Hkv, chan), _gpu_kv(gen, B, Hkv, chan)
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        ws = torch.empty(ok.oscar_decode_workspace_size(P), dtype=torch.uint8, device="cuda")
+        ms = _time(lambda: ok.oscar_decode_step(P, kn, vn, q, out=out, ws=ws), steps, warm)
+        assert P.err() == 0, hex(P.err())
+        per_tok = Hkv * 2 * (D // 4 + 4)
+        unique = (hist + (B - 1) * (hist - share * PAGE)) * per_tok + B * (SINK + RECENT) * Hkv * 2 * D * 2
+        lines.append({"metric": "decode step with shared prefix pages: KV tokens/s", "workload":
+                      f"qwen3-8b-layer decode, batch {B} x 32k context, {share} of {hist // PAGE} history pages shared",
+                      "shared_fraction": share / (hist // PAGE), "value": B * L / (ms * 1e-3), "unit": "KV tokens/s",
+                      "ms_per_step": ms, "steps": steps, "unique_bytes_per_step": unique,
+                      "unique_gbs": unique / (ms * 1e-3) / 1e9, "unique_frac_of_peak": unique / (ms * 1e-3) / 1e9 / peak})
+        del P, ws
+        torch.cuda.empty_cache()
+    return lines
+
+
 def other_workload(args):
     import numpy as np
     import torch
@@ -353,6 +405,8 @@ def other_workload(args):
     peak = peaks.get("hbm_gbs") or 6800.0
     if args.workload == "bf16-compare":
         return bf16_compare(args, peak)
+    if args.workload == "shared-prefix":
+        return shared_prefix(args, peak)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4242)
     lines = []

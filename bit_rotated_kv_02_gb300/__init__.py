@@ -23,7 +23,7 @@ ROT_HAAR, ROT_COVARIANCE = 0, 1
 DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 __all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
-           "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_demote", "oscar_append_kv",
+           "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_prefill_pool_shared", "oscar_demote", "oscar_append_kv",
            "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events",
            "oscar_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "lib", "BF16Cache", "oscar_bf16_prefill",
            "oscar_bf16_append_kv", "oscar_bf16_decode_workspace_size", "oscar_bf16_decode_attention",
@@ -164,6 +164,15 @@ def oscar_prefill_pool(pool: Pool, seq: int, k, v, stats=None, stream=None):
     _dev(v, torch.bfloat16, "v")
     _lib.check(lib().oscar_prefill_pool(pool.ref, seq, k.shape[0], _p(k), _p(v), _p(stats), _s(stream)),
                "oscar_prefill_pool")
+
+
+def oscar_prefill_pool_shared(pool: Pool, seq: int, k, v, shared_pages: int, stats=None, stream=None):
+    """Prefill whose first `shared_pages` history pages are already in the pool (shared prefix pages that
+    the sequence's page table points at); they are not written."""
+    _dev(k, torch.bfloat16, "k")
+    _dev(v, torch.bfloat16, "v")
+    _lib.check(lib().oscar_prefill_pool_shared(pool.ref, seq, k.shape[0], _p(k), _p(v), shared_pages, _p(stats),
+                                               _s(stream)), "oscar_prefill_pool_shared")
 
 
 def oscar_demote(pool: Pool, mask=None, stream=None):

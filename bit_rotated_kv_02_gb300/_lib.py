@@ -51,6 +51,7 @@ SIGNATURES = {
     "oscar_calib_covariance_v": ([I64, I32, I32, P, P, P, F64, P, P, SZ, P], C.c_int),
     "oscar_quantize_kv": ([I64, I32, I32, I32, P, P, P, P, P, P, P, P], C.c_int),
     "oscar_prefill_pool": ([PP, I32, I64, P, P, P, P], C.c_int),
+    "oscar_prefill_pool_shared": ([PP, I32, I64, P, P, I32, P, P], C.c_int),
     "oscar_demote": ([PP, P, P], C.c_int),
     "oscar_append_kv": ([PP, P, P, P], C.c_int),
     "oscar_decode_workspace_size": ([PP, I32, C.POINTER(C.c_size_t)], C.c_int),

@@ -217,6 +217,27 @@ oscar_status_t oscar_prefill_pool(const oscar_pool *pool, int32_t seq, int64_t l
   return cuda_status(launch_prefill(a, seq, len, k, v, stats, static_cast<cudaStream_t>(stream)), "prefill_pool");
 }
 
+oscar_status_t oscar_prefill_pool_shared(const oscar_pool *pool, int32_t seq, int64_t len, const oscar_bf16 *k,
+                                         const oscar_bf16 *v, int32_t shared_pages, uint32_t *stats,
+                                         oscar_stream_t stream) {
+  PoolArgs a;
+  oscar_status_t st = check_pool(pool, a);
+  if (st != OSCAR_OK) return st;
+  if (seq < 0 || seq >= a.B) return fail(OSCAR_ERR_INVALID_ARG, "seq %d outside [0, %d)", seq, a.B);
+  if (len < 0) return fail(OSCAR_ERR_INVALID_ARG, "negative length");
+  const int64_t hist = len > OSCAR_SINK_TOKENS + OSCAR_RECENT_TOKENS ? len - OSCAR_SINK_TOKENS - OSCAR_RECENT_TOKENS : 0;
+  if (hist > (int64_t)a.max_pages * OSCAR_PAGE_TOKENS)
+    return fail(OSCAR_ERR_INVALID_ARG, "history of %lld tokens exceeds max_pages*64", (long long)hist);
+  if (shared_pages < 0 || (int64_t)shared_pages * OSCAR_PAGE_TOKENS > hist)
+    return fail(OSCAR_ERR_INVALID_ARG, "shared_pages %d outside [0, %lld] (whole history pages only)", shared_pages,
+                (long long)(hist / OSCAR_PAGE_TOKENS));
+  if (len > 0 && (k == nullptr || v == nullptr)) return fail(OSCAR_ERR_INVALID_ARG, "k/v NULL");
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  return cuda_status(launch_prefill(a, seq, len, k, v, stats, static_cast<cudaStream_t>(stream), shared_pages),
+                     "prefill_pool_shared");
+}
+
 oscar_status_t oscar_demote(const oscar_pool *pool, const int32_t *mask, oscar_stream_t stream) {
   PoolArgs a;
   oscar_status_t st = check_pool(pool, a);

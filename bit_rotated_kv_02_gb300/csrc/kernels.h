@@ -53,7 +53,7 @@ cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, i
                                  const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
                                  const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s);
 cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
-                           cudaStream_t s);
+                           cudaStream_t s, int skip = 0);
 
 // decode.cu
 constexpr int PART_STRIDE = D + 4;  // one partial: o[128], m, l, pad

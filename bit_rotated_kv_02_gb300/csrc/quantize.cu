@@ -180,8 +180,10 @@ cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, cons
   return e;
 }
 
+// skip: the first `skip` history pages are already in place (shared with another sequence's identical
+// prefix through the page table) and are neither quantized nor written.
 cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
-                           cudaStream_t s) {
+                           cudaStream_t s, int skip) {
   const int ns = (int)(L < SINK ? L : SINK);
   const int64_t rest = L - ns;
   const int nr = (int)(rest < RECENT ? rest : RECENT);
@@ -199,12 +201,14 @@ cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *
                                                      p.recent_v + (size_t)b * p.Hkv * RECENT * D, RECENT);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (nh > 0) {
-    const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
-    e = launch_quantize_rows(nh, p.Hkv, p.g, k + (size_t)ns * stride, stride, p.R_k, p.clip_k, p.codes_k, p.scale_k,
+  const int64_t first = (int64_t)skip * PAGE;  // history rows [first, nh) are written
+  if (nh > first) {
+    const int32_t *pt = p.page_table + (size_t)b * p.max_pages + skip;
+    const int64_t n = nh - first, x0 = (int64_t)ns + first;
+    e = launch_quantize_rows(n, p.Hkv, p.g, k + (size_t)x0 * stride, stride, p.R_k, p.clip_k, p.codes_k, p.scale_k,
                              p.zero_k, pt, p.num_pages, p.err, stats, s);
     if (e != cudaSuccess) return e;
-    e = launch_quantize_rows(nh, p.Hkv, p.g, v + (size_t)ns * stride, stride, p.R_v, p.clip_v, p.codes_v, p.scale_v,
+    e = launch_quantize_rows(n, p.Hkv, p.g, v + (size_t)x0 * stride, stride, p.R_v, p.clip_v, p.codes_v, p.scale_v,
                              p.zero_v, pt, p.num_pages, p.err, stats, s);
     if (e != cudaSuccess) return e;
   }

@@ -168,6 +168,20 @@ oscar_status_t oscar_prefill_pool(const oscar_pool *pool, int32_t seq, int64_t l
                                   const oscar_bf16 *v, uint32_t *stats, oscar_stream_t stream);
 
 /*
+ * Bulk prefill of a sequence whose prompt starts with the same tokens as a sequence already in the
+ * pool (a shared prefix: the paged, prefix-cache-compatible history of the Abstract and of "OSCAR 的
+ * 设计"; "评估结果" Fig. 6 measures the prefix-cache hit ratio).  As oscar_prefill_pool, except that
+ * the first `shared_pages` history pages are taken as already in place: page_table[seq][0 ..
+ * shared_pages) points at pages written for the other sequence (the same physical pages), and those
+ * pages are neither quantized nor written.  Only whole pages can be shared (shared_pages * 64 <=
+ * history length); demotions write only at and after the history length, so shared pages are never
+ * written again.  k and v still hold all `len` tokens (the sink and recent window are per sequence).
+ */
+oscar_status_t oscar_prefill_pool_shared(const oscar_pool *pool, int32_t seq, int64_t len, const oscar_bf16 *k,
+                                         const oscar_bf16 *v, int32_t shared_pages, uint32_t *stats,
+                                         oscar_stream_t stream);
+
+/*
  * Demotion ("OSCAR 的设计": the oldest recent token is rotated, clipped, quantized and packed by a
  * fused kernel and demoted into the INT2 history).
  * For every sequence whose recent window is full (recent_len == 256) — or, if mask (device int32

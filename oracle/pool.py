@@ -63,22 +63,24 @@ class Pool:
         self.codes_k[page, kvh, row], self.scale_k[page, kvh, row], self.zero_k[page, kvh, row] = pk[0], sk[0], zk[0]
         self.codes_v[page, kvh, row], self.scale_v[page, kvh, row], self.zero_v[page, kvh, row] = pv[0], sv[0], zv[0]
 
-    def prefill(self, b, K_bits, V_bits, heads=None):
+    def prefill(self, b, K_bits, V_bits, heads=None, shared_pages=0):
         """K_bits, V_bits: bf16 [L][Hkv][d] of one sequence; fills its three segments (history of the
-        KV heads in `heads` only, when given: each head's history is independent of the others)."""
+        KV heads in `heads` only, when given: each head's history is independent of the others).
+        shared_pages: the first history pages are already in place (the page table points at pages
+        another sequence with the same prefix filled) and are not written."""
         L = K_bits.shape[0]
         ns = min(L, SINK)
         nr = min(max(L - SINK, 0), RECENT)
         nh = L - ns - nr
         self.sink_k[b, :, :ns] = K_bits[:ns].transpose(1, 0, 2)
         self.sink_v[b, :, :ns] = V_bits[:ns].transpose(1, 0, 2)
-        t = np.arange(nh)
+        t = np.arange(shared_pages * PAGE, nh)
         pages, rows = self.page_table[b, t // PAGE], t % PAGE
         for kvh in (range(self.Hkv) if heads is None else heads):
             for X, R, clip, codes, scale, zero in (
                     (K_bits, self.R_k, self.clip_k, self.codes_k, self.scale_k, self.zero_k),
                     (V_bits, self.R_v, self.clip_v, self.codes_v, self.scale_v, self.zero_v)):
-                pc, sc, zc = quant.quantize_vectors_many(X[ns:ns + nh, kvh], R[kvh], clip[kvh], self.g)
+                pc, sc, zc = quant.quantize_vectors_many(X[ns + t, kvh], R[kvh], clip[kvh], self.g)
                 codes[pages, kvh, rows], scale[pages, kvh, rows], zero[pages, kvh, rows] = pc, sc, zc
         self.recent_k[b, :, :nr] = K_bits[ns + nh:].transpose(1, 0, 2)
         self.recent_v[b, :, :nr] = V_bits[ns + nh:].transpose(1, 0, 2)

@@ -99,3 +99,37 @@ def test_demote_mask_moves_exactly_flagged_sequences():
     P.demote(np.array([0, 1]))
     assert (P.hist_len[0], P.recent_len[0]) == (80, 256)
     assert (P.hist_len[1], P.recent_len[1], P.recent_start[1]) == (1, 235, 1)
+
+
+def test_shared_prefix_pages_equal_private_copies():
+    """Two sequences with the same first 64 * P history tokens: the second one's page table points at
+    the first one's prefix pages (written once).  Its decode equals, exactly, that of a pool where it has
+    private pages holding the same tokens; sharing pages whose tokens differ would change it."""
+    d, P, L = 32, 3, 320 + 64 * 5 + 10          # 5 full history pages + 10 tokens
+    shared = synth.outlier_kv(11, L, 1, d, np.array([[2]]))
+    tail = synth.outlier_kv(12, L, 1, d, np.array([[2]]))
+    K1 = np.concatenate([shared[:64 + 64 * P], tail[64 + 64 * P:]])
+    V0 = synth.outlier_kv(13, L, 1, d, np.array([[2]]))
+    V1 = np.concatenate([V0[:64 + 64 * P], tail[64 + 64 * P:][:, :, ::-1]])
+    q = synth.outlier_q(14, 2, 2, 1, d, np.array([[2]]))
+
+    def make(share):
+        Pl = _make(2, 2, 1, d, 16, 12)
+        pt = np.full((2, 12), -1, np.int32)
+        pt[:, :6] = np.arange(12, dtype=np.int32).reshape(2, 6)
+        if share:
+            pt[1, :P] = pt[0, :P]
+        Pl.page_table[:] = pt
+        Pl.prefill(0, shared, V0)
+        Pl.prefill(1, K1, V1, shared_pages=P if share else 0)
+        return Pl
+
+    A, B = make(True), make(False)
+    np.testing.assert_array_equal(A.decode(q), B.decode(q))
+    # the pages seq 1 would have written for its prefix are byte-identical to the shared ones
+    for name in ("codes_k", "codes_v", "scale_k", "zero_k", "scale_v", "zero_v"):
+        arr = getattr(B, name)
+        np.testing.assert_array_equal(arr[:P], arr[6:6 + P])
+    bad = make(True)
+    bad.prefill(0, tail, V0)                     # the prefix pages now hold other tokens
+    assert np.abs(bad.decode(q)[1] - A.decode(q)[1]).max() > 1e-3
