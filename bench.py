@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed", "bf16-compare",
-                                           "shared-prefix"],
+                                           "shared-prefix", "quality"],
                     default="decode100k",
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -392,6 +392,34 @@ def shared_prefix(args, peak):
     return lines
 
 
+def quality_workload(args):
+    """Attention quality of the four variants of the pages' Fig. 1 (naive INT2, Hadamard-only, clip-only,
+    OSCAR) on one Qwen3-8B-shaped layer (32 query / 8 KV heads): calibration-style synthetic activations
+    (anisotropic spectrum, four outlier channels per KV head: x4 in q, x10 in K and V), 2,048 calibration
+    tokens, one decode query per head over 4,416 tokens of context."""
+    import numpy as np
+    import torch
+    import synth
+    from bit_rotated_kv_02_gb300 import quality
+    T, L, G = 2048, 4416, HQ // HKV
+    ch = synth.outlier_channels(77, HKV, D, 4)
+    Qs = synth.calib_samples(78, T + 1, HQ, D, ch, heads_per_channel_set=G, factor=4.0)
+    KV = [synth.calib_samples(79 + h, T + L, 2, D, ch[h:h + 1], heads_per_channel_set=2, factor=10.0)
+          for h in range(HKV)]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16).cuda()
+    K = dev(np.stack([kv[:, 0] for kv in KV], 1))
+    V = dev(np.stack([kv[:, 1] for kv in KV], 1))
+    Qd = dev(Qs)
+    lines = []
+    for name, (Rk, Rv, c) in quality.variants(Qd[:T], K[:T], V[:T]).items():
+        kl, err = quality.measure(K[T:], V[T:], Qd[T], Rk, Rv, [c] * HKV, [c] * HKV)
+        lines.append({"metric": "attention quality vs exact BF16 attention (score KL, relative output error)",
+                      "variant": name, "score_kl": kl, "output_rel_sq_error": err, "clip": c,
+                      "workload": "qwen3-8b-layer, calibration-style synthetic activations, 4,416-token context",
+                      "data": "synthetic"})
+    return lines
+
+
 def other_workload(args):
     import numpy as np
     import torch
@@ -407,6 +435,8 @@ def other_workload(args):
         return bf16_compare(args, peak)
     if args.workload == "shared-prefix":
         return shared_prefix(args, peak)
+    if args.workload == "quality":
+        return quality_workload(args)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4242)
     lines = []

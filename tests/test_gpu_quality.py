@@ -1,0 +1,84 @@
+"""GPU: the attention-quality harness ("超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化", section
+"OSCAR 的动机", Fig. 1) against the float64 oracle.
+
+With the same rotations and clip ratios on both sides the pools hold the same codes, so the harness's
+score KL and output error must equal the oracle's up to the decode kernel's float32 rounding; the
+library-built variants must rank as the oracle's do on the calibration-style recipe.
+"""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+import synth
+from oracle import pool as opool
+from oracle import quality as oquality
+from oracle import rotation as orot
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+
+D, G, HKV, T, L = 128, 4, 2, 2048, 320 + 640
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+
+
+def _data(seed):
+    ch = synth.outlier_channels(seed, HKV, D, 4)
+    Qs = synth.calib_samples(seed + 1, T + 1, G * HKV, D, ch, heads_per_channel_set=G, factor=4.0)
+    KV = [synth.calib_samples(seed + 2 + h, T + L, 2, D, ch[h:h + 1], heads_per_channel_set=2, factor=10.0)
+          for h in range(HKV)]
+    K = np.stack([kv[:, 0] for kv in KV], 1)
+    V = np.stack([kv[:, 1] for kv in KV], 1)
+    return Qs[:T], K[:T], V[:T], K[T:], V[T:], Qs[T]
+
+
+def _oracle_rotations(Qc, Kc, Vc):
+    f = lambda b: synth.bf16_bits_to_f32(b).astype(np.float64)
+    HP = orot.to_f32(orot.hadamard(D) @ orot.bitrev_matrix(D))
+    Rk = np.stack([orot.to_f32(orot.rotation_from_covariance(orot.covariance_k(f(Qc[:, h * G:(h + 1) * G]))))
+                   for h in range(HKV)])
+    Rv = np.stack([orot.to_f32(orot.rotation_from_covariance(
+        orot.covariance_v(f(Qc[:, h * G:(h + 1) * G]), f(Kc[:, h]), f(Vc[:, h])))) for h in range(HKV)])
+    I = np.stack([np.eye(D, dtype=np.float32)] * HKV)
+    return {"naive_int2": (I, I, 1.0), "hadamard_only": (np.stack([HP] * HKV),) * 2 + (1.0,),
+            "clip_only": (I, I, 0.9), "oscar": (Rk, Rv, 0.9)}
+
+
+def _oracle_metrics(K, V, q, Rk, Rv, c):
+    pages = -(-(L - 320) // 64)
+    P = opool.Pool(1, G * HKV, HKV, D, 128, pages, pages, Rk, Rv, [c] * HKV, [c] * HKV)
+    P.page_table[0] = np.arange(pages, dtype=np.int32)
+    P.prefill(0, K, V)
+    return oquality.metrics(P, 0, K, V, q)
+
+
+def test_harness_equals_oracle_with_the_same_rotations():
+    from bit_rotated_kv_02_gb300 import quality
+    Qc, Kc, Vc, K, V, q = _data(900)
+    Kd, Vd, qd = helpers.to_dev_bf16(K), helpers.to_dev_bf16(V), helpers.to_dev_bf16(q)
+    for name, (Rk, Rv, c) in _oracle_rotations(Qc, Kc, Vc).items():
+        kl, err = quality.measure(Kd, Vd, qd, torch.from_numpy(Rk).cuda(), torch.from_numpy(Rv).cuda(),
+                                  [c] * HKV, [c] * HKV)
+        okl, oerr = _oracle_metrics(K, V, q, Rk, Rv, c)
+        assert kl == pytest.approx(okl, rel=1e-6, abs=1e-9), name
+        assert err == pytest.approx(oerr, rel=1e-3), name
+
+
+def test_hadamard_variant_is_the_oracle_hadamard_bitrev():
+    from bit_rotated_kv_02_gb300 import quality
+    R = quality.hadamard_rotation(1)[0].cpu().numpy()
+    np.testing.assert_allclose(R, orot.to_f32(orot.hadamard(D) @ orot.bitrev_matrix(D)), rtol=0, atol=1e-8)
+
+
+def test_library_variants_rank_as_in_fig1():
+    from bit_rotated_kv_02_gb300 import quality
+    Qc, Kc, Vc, K, V, q = _data(910)
+    dev = lambda x: helpers.to_dev_bf16(x)
+    res = {name: quality.measure(dev(K), dev(V), dev(q), Rk, Rv, [c] * HKV, [c] * HKV)
+           for name, (Rk, Rv, c) in quality.variants(dev(Qc), dev(Kc), dev(Vc)).items()}
+    assert res["oscar"][1] < res["hadamard_only"][1] < res["naive_int2"][1]
+    assert res["oscar"][0] < res["naive_int2"][0] and res["hadamard_only"][0] < res["naive_int2"][0]
