@@ -312,7 +312,7 @@ def bf16_compare(args, peak):
     attn_bytes = ctx * HKV * 2 * D * 2 + 4 * math.ceil(ctx / PAGE) + HQ * D * 2
     del caches, ws
     torch.cuda.empty_cache()
-    # the INT2 arm: the headline step over the three-segment pool (4 launches per step)
+    # the INT2 arm: the headline step over the three-segment pool (3 launches per step)
     NL = 8
     layers = setup_layers(NL, -(-(steps + warm) // NL) + 8)
     ws2 = torch.empty(ok.oscar_decode_workspace_size(layers[0], 0), dtype=torch.uint8, device="cuda")
@@ -575,7 +575,8 @@ def main():
         return
 
     NL = args.layers
-    total = args.warmup + args.steps + args.e2e_steps
+    DEM_N = 200  # appends timed on their own after the run
+    total = args.warmup + args.steps + args.e2e_steps + DEM_N
     per_layer = -(-total // NL)
     layers = setup_layers(NL, per_layer + 8)
     dev = torch.device("cuda")
@@ -598,7 +599,6 @@ def main():
         P = layers[l]
         if ev is not None:
             lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
-            lib.oscar_profile_events(1, C.c_void_p(ev[2].cuda_event), C.c_void_p(ev[3].cuda_event))
         j = i % NQ
         st = lib.oscar_decode_step(P.ref, C.c_void_p(kn[j].data_ptr()), C.c_void_p(vn[j].data_ptr()),
                                    C.c_void_p(qs[j].data_ptr()), C.c_void_p(outs[l].data_ptr()), scale,
@@ -636,7 +636,6 @@ def main():
     clk = clocks.stop(wall0, time.time())
     ms = t_start.elapsed_time(t_stop)
     hist_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dem_ms = [e[2].elapsed_time(e[3]) for e in evs]
     ms = max_over_ranks(ms)
     for P in layers:
         if P.err() != 0:
@@ -665,6 +664,16 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     e2e_ms = max_over_ranks(e2e_ms)
+    # the demotion + append kernel on its own (oscar_append_kv: one token per step, window full)
+    e0.record()
+    for i in range(DEM_N):
+        ok.oscar_append_kv(layers[i % NL], dk, dv)
+    e1.record()
+    torch.cuda.synchronize()
+    dem_ms = e0.elapsed_time(e1) / DEM_N
+    for P in layers:
+        if P.err() != 0:
+            raise RuntimeError(f"device error flags {P.err():#x}")
 
     # algorithmic bytes of the history kernel per launch (codes + scale/zero + page table + q)
     hist_tokens_avg = (tokens / args.steps) - SINK - RECENT
@@ -706,14 +715,13 @@ def main():
                                                                        "decode_v1.cu")),
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3,
                          "timed_launches": len(hist_ms), "sampling": f"every {EVERY}th step of the timed region"},
-            "demote": {"tokens_per_s": 1.0 / (statistics.mean(dem_ms) * 1e-3), "mean_launch_us":
-                       statistics.mean(dem_ms) * 1e3,
-                       "note": "append + demote kernel (side stream, alongside the attention), 1 token x 8 KV "
-                               "heads x K/V per launch"},
+            "demote": {"tokens_per_s": 1.0 / (dem_ms * 1e-3), "mean_call_us": dem_ms * 1e3,
+                       "note": "oscar_append_kv (demotion + append kernel), timed on its own after the run; in "
+                               "the decode step the merge kernel performs the demotion"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 4,   # append + demote, q rotation, attention, merge
+            "gpu_launches": args.steps * 3,   # q rotation, attention, merge (+ demotion and append)
             "clocks": clk,
             "cpu_baseline": cpu,
         }

@@ -19,10 +19,10 @@
 //                 (CTA, segment).
 //   merge_kernel  LSE-combines a segment's partials, un-rotates the history part (o · R_v^T),
 //                 adds the BF16 part and normalises.
-// The decode step (oscar_decode_step) adds the demotion kernel on a side stream: the attention kernel
-// reads only what the step leaves unchanged (the history before the step, the window slots other than
-// the new token's, which it takes from k_new / v_new), so it runs alongside the demotion; the merge
-// follows both, adds the demoted token and advances the pool counters.
+// The decode step (oscar_decode_step) uses the same three launches: the attention kernel reads only what
+// the step leaves unchanged (the history before the step, the window slots other than the new token's,
+// which it takes from k_new / v_new); the merge kernel performs the demotion (overlapping the attention's
+// tail), adds the demoted token, stores the new token and advances the pool counters.
 //
 // Exactness of the tensor-core arithmetic: a 2-bit code c placed in the low mantissa bits of an
 // fp16 with a zero exponent field is the subnormal c * 4^k * 2^-24 (k = its bit position / 2), so
@@ -69,6 +69,7 @@ struct Args {
 // a demotion that cannot be stored blocks the append too).
 struct StepState {
   bool ok;        // counters valid
+  bool want;      // the window is full: its oldest token is due for demotion
   bool demote;    // the oldest window token moves to history position hist_len
   bool append;    // the new token is stored
   bool to_sink;   // ... into the sink (else into the window)
@@ -81,6 +82,7 @@ __device__ __forceinline__ StepState step_state(const PoolArgs &p, int b) {
   st.ok = st.slen >= 0 && st.slen <= SINK && st.hl >= 0 && st.rs >= 0 && st.rs < RECENT && st.rl >= 0 &&
           st.rl <= RECENT;
   const bool want = st.ok && st.rl == RECENT;
+  st.want = want;
   st.demote = false;
   if (want && st.hl / PAGE < p.max_pages) {
     const int page = p.page_table[(size_t)b * p.max_pages + st.hl / PAGE];
@@ -857,53 +859,88 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
 // that each R_v row is read as one contiguous 512-byte run.
 constexpr int MT = 512;
 constexpr int MAXPARTS = 1040;
+// Decode-step form (k_new != NULL): the merge also performs the step's demotion and append.  The pool
+// counters still hold the state before the step (the attention kernel read them); before its
+// griddepcontrol.wait the CTA rotates, clips and quantizes the window's oldest K and V vectors of its
+// KV head (when the window is full) — all inputs of that are state the step's earlier kernels leave
+// unchanged, so the work overlaps the attention kernel's tail.  The demoted token then enters the
+// merge as one more partial (m = its score, l = 1, o = its dequantized rotated value).  The CTA of
+// query head 0 stores the demoted codes into the history; the last CTA of a sequence to finish (arrival
+// counter pool.sync[b]; every CTA has read the window by then) stores the new token into the sink or
+// the window and advances the counters.  Warps 0-7 rotate the K vector, warps 8-15 the V vector, each
+// warp 16 rows of R held in registers, as the demotion kernel does.
 template <int G>
-// Step form (qrot != NULL): the pool counters still hold the state before the step; the token the
-// step demoted (history position hist_len) enters as one more partial (m = its score, l = 1, o = its
-// dequantized rotated value), and the last CTA of a sequence to finish (arrival counter pool.sync[b])
-// advances the counters to the state after the step.
-__global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
-                                                   const float *qrot, float sm_log2) {
+__global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
+                                                   const float *qrot, float sm_log2, const uint16_t *k_new,
+                                                   const uint16_t *v_new) {
   constexpr int OV = 36;  // partials per slice issued at once (4 slices: 144 partials)
+  constexpr int DW = 8, DR = D / DW;  // demotion: 8 warps per vector, 16 rows of R each
   __shared__ float wgt[MAXPARTS], lsum[MAXPARTS];
   __shared__ float red[MT / 32];
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
   __shared__ long long s_pref, s_total;
   __shared__ float s_md;
   __shared__ int s_last;
-  pdl_wait();
-  pdl_trigger();
+  __shared__ float xdem[2][D];
+  __shared__ float pacc[2][DW][32][4], psab[2][DW][32][4];
+  __shared__ uint8_t dcodes[2][D / 4];
+  __shared__ uint16_t dscale[2], dzero[2];
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
-  const bool step = qrot != nullptr;
+  const bool step = k_new != nullptr;
   StepState st{};
-  float od = 0.f;  // step form: the demoted token's dequantized rotated value at channel ch
   if (step) {
     st = step_state(p, b);
     if (st.demote) {
-      const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
-                         st.hl % PAGE;
-      if (warp == 0) {
-        const float4 q4 = reinterpret_cast<const float4 *>(qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
-        const uint32_t cb = p.codes_k[row * (D / 4) + lane];  // channels 4 lane .. 4 lane + 3
-        float dc = q4.x * (float)(cb & 3u) + q4.y * (float)((cb >> 2) & 3u) + q4.z * (float)((cb >> 4) & 3u) +
-                   q4.w * (float)((cb >> 6) & 3u);
-        float sq = (q4.x + q4.y) + (q4.z + q4.w);
+      const int kv = warp / DW, w8 = warp % DW;
+      const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
+      float4 rrow[DR];
+      const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(DR * w8) * (D / 4) + lane;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          dc += __shfl_xor_sync(FULL, dc, o);
-          sq += __shfl_xor_sync(FULL, sq, o);
-        }
-        if (lane == 0)
-          s_md = sm_log2 * fmaf(bf16_to_f32(p.scale_k[row]), dc, bf16_to_f32(p.zero_k[row]) * sq);
+      for (int i = 0; i < DR; ++i) rrow[i] = R4[i * (D / 4)];
+      if (w8 == 0) {
+        const uint2 xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
+                                                         (((size_t)b * p.Hkv + kvh) * RECENT + st.rs) * D)[lane];
+        xdem[kv][4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
+        xdem[kv][4 * lane + 1] = bf16_to_f32(xw.x >> 16);
+        xdem[kv][4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
+        xdem[kv][4 * lane + 3] = bf16_to_f32(xw.y >> 16);
       }
-      const uint32_t cv = (p.codes_v[row * (D / 4) + ch / 4] >> (2 * (ch & 3))) & 3u;
-      od = fmaf((float)cv, bf16_to_f32(p.scale_v[row]), bf16_to_f32(p.zero_v[row]));
-    } else if (tid == 0) {
-      s_md = -INFINITY;
+      __syncthreads();
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < DR; ++i) {
+        const float xi = xdem[kv][DR * w8 + i], ax = fabsf(xi);
+        acc[0] = fmaf(xi, rrow[i].x, acc[0]);
+        acc[1] = fmaf(xi, rrow[i].y, acc[1]);
+        acc[2] = fmaf(xi, rrow[i].z, acc[2]);
+        acc[3] = fmaf(xi, rrow[i].w, acc[3]);
+        sab[0] = fmaf(ax, fabsf(rrow[i].x), sab[0]);
+        sab[1] = fmaf(ax, fabsf(rrow[i].y), sab[1]);
+        sab[2] = fmaf(ax, fabsf(rrow[i].z), sab[2]);
+        sab[3] = fmaf(ax, fabsf(rrow[i].w), sab[3]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { pacc[kv][w8][lane][k] = acc[k]; psab[kv][w8][lane][k] = sab[k]; }
+      __syncthreads();
+      if (w8 == 0) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float a8 = 0.f, s8 = 0.f;
+#pragma unroll
+          for (int w = 0; w < DW; ++w) { a8 += pacc[kv][w][lane][k]; s8 += psab[kv][w][lane][k]; }
+          acc[k] = a8;
+          sab[k] = s8;
+        }
+        QuantStats qst{0, 0, 0};
+        quantize_from_dots(xdem[kv], Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcodes[kv],
+                           &dscale[kv], &dzero[kv], qst);
+      }
     }
   }
+  // Everything up to here and the partials' location and the R_v rows below read only state that the
+  // attention kernel does not write (pool counters, R_v), so they overlap its tail.
   if (warp == 0) {
     long long total;
     int bb, kk, ll;
@@ -932,6 +969,47 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
   const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
   const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
   auto slot = [&](int i) { return i < nh ? hp + (size_t)i * stride : bp + (size_t)(i - nh) * stride; };
+  // R_v rows c = warp + 16 k (k < 8), lane's four columns 4 lane .. 4 lane + 3
+  constexpr int UW = MT / 32, UPW = D / UW;
+  float4 rv[UPW];
+#pragma unroll
+  for (int k = 0; k < UPW; ++k)
+    rv[k] = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + warp + UW * k) * D)[lane];
+  pdl_wait();
+  pdl_trigger();
+  float od = 0.f;  // step form: the demoted token's dequantized rotated value at channel ch
+  if (step) {
+    __syncthreads();  // the demoted codes are in shared memory
+    if (st.demote) {
+      if (warp == 0) {
+        const float4 q4 = reinterpret_cast<const float4 *>(qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
+        const uint32_t cb = dcodes[0][lane];  // channels 4 lane .. 4 lane + 3
+        float dc = q4.x * (float)(cb & 3u) + q4.y * (float)((cb >> 2) & 3u) + q4.z * (float)((cb >> 4) & 3u) +
+                   q4.w * (float)((cb >> 6) & 3u);
+        float sq = (q4.x + q4.y) + (q4.z + q4.w);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          dc += __shfl_xor_sync(FULL, dc, o);
+          sq += __shfl_xor_sync(FULL, sq, o);
+        }
+        if (lane == 0) s_md = sm_log2 * fmaf(bf16_to_f32(dscale[0]), dc, bf16_to_f32(dzero[0]) * sq);
+      }
+      const uint32_t cv = (dcodes[1][ch / 4] >> (2 * (ch & 3))) & 3u;
+      od = fmaf((float)cv, bf16_to_f32(dscale[1]), bf16_to_f32(dzero[1]));
+      if (h == 0 && tid < 2 * (D / 4)) {  // store the demoted K and V codes, scale and zero in the history
+        const int kv = tid / (D / 4), byte = tid % (D / 4);
+        const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
+                           st.hl % PAGE;
+        (kv == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + byte] = dcodes[kv][byte];
+        if (byte == 0) {
+          (kv == 0 ? p.scale_k : p.scale_v)[row] = dscale[kv];
+          (kv == 0 ? p.zero_k : p.zero_v)[row] = dzero[kv];
+        }
+      }
+    } else if (tid == 0) {
+      s_md = -INFINITY;
+    }
+  }
   float mx = -INFINITY;
   for (int i = tid; i < nparts; i += MT) {
     const float *q = slot(i);
@@ -946,12 +1024,6 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
     const int i = sl + 4 * k;
     ov[k] = i < nparts ? slot(i)[ch] : 0.f;
   }
-  // R_v rows c = warp + 16 k (k < 8), lane's four columns 4 lane .. 4 lane + 3
-  constexpr int UW = MT / 32, UPW = D / UW;
-  float4 rv[UPW];
-#pragma unroll
-  for (int k = 0; k < UPW; ++k)
-    rv[k] = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + warp + UW * k) * D)[lane];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
   if (lane == 0) red[warp] = mx;
@@ -1011,15 +1083,30 @@ __global__ void __launch_bounds__(MT) merge_kernel(PoolArgs p, const float *part
     out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
   }
   if (!step) return;
-  // every CTA of the sequence has read the counters before it arrives; the last one advances them
+  // every CTA of the sequence has read the counters and the window before it arrives; the last one
+  // stores the new token of every KV head and advances the counters
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     s_last = atomicAdd(p.sync + b, 1) == (int)(gridDim.x * gridDim.y) - 1;
   }
   __syncthreads();
-  if (s_last && tid == 0) {
-    __threadfence();
+  if (!s_last) return;
+  __threadfence();
+  if (st.append) {
+    for (int i = tid; i < p.Hkv * 2 * (D / 4); i += MT) {  // 8-byte pieces of the K and V rows
+      const int kh = i / (2 * (D / 4)), kv = (i / (D / 4)) & 1, j = i % (D / 4);
+      uint16_t *dst = st.to_sink
+          ? (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kh) * SINK + st.slen) * D
+          : (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kh) * RECENT + (st.nrs + st.nrl - 1) % RECENT) * D;
+      reinterpret_cast<uint2 *>(dst)[j] =
+          reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kh) * D)[j];
+    }
+  }
+  if (tid == 0) {
+    if (!st.ok) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
+    else if (st.want && !st.demote)
+      atomicOr(p.err, st.hl / PAGE >= p.max_pages ? OSCAR_DEVERR_HISTORY_FULL : OSCAR_DEVERR_PAGE_INDEX);
     if (st.ok && (st.demote || st.append)) {
       p.sink_len[b] = st.nslen;
       p.hist_len[b] = st.nhl;
@@ -1077,25 +1164,6 @@ size_t v1_ws_bytes(const PoolArgs &p) {
   return (size_t)p.B * p.Hq * D * sizeof(float) + frag + slots * G * PART_STRIDE * sizeof(float);
 }
 
-// A non-blocking side stream and a fork/join event pair per host thread and device (created on first
-// use, kept for the life of the process).
-static cudaError_t side_stream(cudaStream_t &s, cudaEvent_t &fork, cudaEvent_t &join) {
-  struct Side { cudaStream_t s = nullptr; cudaEvent_t fork = nullptr, join = nullptr; };
-  thread_local Side side[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  Side &x = side[dev];
-  if (x.s == nullptr) {
-    if ((e = cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-  }
-  s = x.s; fork = x.fork; join = x.join;
-  return cudaSuccess;
-}
-
 // k_new != NULL: the step form (append + demote + query rotation fused in the demote kernel);
 // otherwise the query rotation runs as its own kernel.
 template <int G>
@@ -1124,25 +1192,16 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.step = k_new != nullptr;
   a.k_new = k_new;
   a.v_new = v_new;
-  // Step form: the demotion runs on a side stream forked from and joined back into the caller's
-  // stream, alongside the query rotation and the attention kernel; the merge follows both.
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  if (a.step) {
-    if ((e = side_stream(side, fork, join)) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(fork, s)) != cudaSuccess || (e = cudaStreamWaitEvent(side, fork, 0)) != cudaSuccess) return e;
-    if ((e = launch_demote(p, nullptr, 3, k_new, v_new, side)) != cudaSuccess) return e;
-    if ((e = cudaEventRecord(join, side)) != cudaSuccess) return e;
-  }
+  // Step form: the attention reads only state the step leaves unchanged; the merge performs the
+  // demotion (overlapping the attention's tail), the append and the counter update.
   if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2)) !=
       cudaSuccess)
     return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
-  if (a.step && (e = cudaStreamWaitEvent(s, join, 0)) != cudaSuccess) return e;
   return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), 0, s, p, (const float *)a.part, a.n_hist,
-                    out, a.step ? (const float *)ws : nullptr, a.sm_log2);
+                    out, (const float *)ws, a.sm_log2, k_new, v_new);
 }
 
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,

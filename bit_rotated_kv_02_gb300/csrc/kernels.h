@@ -65,8 +65,8 @@ cudaError_t launch_decode(const PoolArgs &p, const uint16_t *q, float *out, floa
 size_t v1_ws_bytes(const PoolArgs &p);
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
                              cudaStream_t s);
-// The decode step for group size 128: the demotion (on a side stream) alongside the query rotation and
-// the attention kernel, then the merge.
+// The decode step for group size 128: the query rotation, the attention kernel and the merge, which
+// performs the demotion and the append.
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
                            float *out, float sm_scale, float *ws, cudaStream_t s);
 

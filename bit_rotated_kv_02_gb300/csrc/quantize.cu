@@ -19,8 +19,7 @@ namespace oscar {
 // the last CTA to arrive (arrival counter pool.sync[b]) updates the counters and returns the arrival
 // counter to zero.
 // mode 0: demote where recent_len == 256; mode 1: demote where mask[b] != 0 && recent_len > 0;
-// mode 2: as mode 0, then append k_new/v_new; mode 3: as mode 2 but the counters are left unchanged
-// (the decode step's merge kernel advances them once every reader of the step is done).
+// mode 2: as mode 0, then append k_new/v_new.
 constexpr int DEMOTE_WARPS = 8, DEMOTE_ROWS = D / DEMOTE_WARPS;  // 16 rows of R per warp
 constexpr int RS_LD = D + 4;  // padded row stride of the shared copy of R (16-byte rows, 4-way reads)
 constexpr size_t DEMOTE_SMEM = (size_t)D * RS_LD * sizeof(float);
@@ -43,9 +42,9 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
 #pragma unroll
     for (int i = 0; i < DEMOTE_ROWS; ++i) rs4[(DEMOTE_ROWS * warp + i) * (RS_LD / 4) + lane] = rrow[i];
   }
-  // the appended token's row (modes 2 and 3; warp 0), also independent of the counters
+  // the appended token's row (mode 2; warp 0), also independent of the counters
   uint2 newrow = make_uint2(0u, 0u);
-  if (mode >= 2 && warp == 0)
+  if (mode == 2 && warp == 0)
     newrow = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[lane];
   const int slen = p.sink_len[b], hl = p.hist_len[b], rs = p.recent_start[b], rl = p.recent_len[b];
   const bool counters_ok = slen >= 0 && slen <= SINK && hl >= 0 && rs >= 0 && rs < RECENT && rl >= 0 && rl <= RECENT;
@@ -116,7 +115,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
-  const bool append = mode >= 2 && counters_ok && !blocked;
+  const bool append = mode == 2 && counters_ok && !blocked;
   int nslen = slen, nhl = hl, nrs = rs, nrl = rl;
   if (demote) { nhl = hl + 1; nrs = (rs + 1) % RECENT; nrl = rl - 1; }
   if (append && warp == 0) {
@@ -132,7 +131,6 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
     if (nslen < SINK && nhl == 0 && nrl == 0) nslen += 1;
     else nrl += 1;
   }
-  if (mode == 3) return;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
