@@ -23,14 +23,16 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import attention, quant
+from . import attention, codebook, quant
 
 PAGE, SINK, RECENT = 64, 64, 256
 
 
 class Pool:
     def __init__(self, batch, num_q_heads, num_kv_heads, d, group, num_pages, max_pages,
-                 R_k32, R_v32, clip_k, clip_v):
+                 R_k32, R_v32, clip_k, clip_v, codebook_k=None, codebook_v=None):
+        """codebook_k, codebook_v: float32 [Hkv][4] levels (oracle.codebook), or None for the uniform
+        levels (0, 1, 2, 3)."""
         self.B, self.Hq, self.Hkv, self.d, self.g = batch, num_q_heads, num_kv_heads, d, group
         self.ng = d // group
         self.num_pages, self.max_pages = num_pages, max_pages
@@ -38,6 +40,8 @@ class Pool:
         self.R_v = np.asarray(R_v32, np.float32).reshape(num_kv_heads, d, d)
         self.clip_k = np.asarray(clip_k, np.float32).reshape(num_kv_heads)
         self.clip_v = np.asarray(clip_v, np.float32).reshape(num_kv_heads)
+        self.cb_k = None if codebook_k is None else np.asarray(codebook_k, np.float32).reshape(num_kv_heads, 4)
+        self.cb_v = None if codebook_v is None else np.asarray(codebook_v, np.float32).reshape(num_kv_heads, 4)
         self.sink_k = np.zeros((batch, num_kv_heads, SINK, d), np.uint16)
         self.sink_v = np.zeros_like(self.sink_k)
         self.recent_k = np.zeros((batch, num_kv_heads, RECENT, d), np.uint16)
@@ -58,10 +62,20 @@ class Pool:
     def _store_history(self, b, pos, kvh, k_bits, v_bits):
         page = int(self.page_table[b, pos // PAGE])
         row = pos % PAGE
-        pk, sk, zk = quant.quantize_vectors(k_bits[None, :], self.R_k[kvh], self.clip_k[kvh], self.g)
-        pv, sv, zv = quant.quantize_vectors(v_bits[None, :], self.R_v[kvh], self.clip_v[kvh], self.g)
+        pk, sk, zk = self._quantize(k_bits[None, :], self.R_k[kvh], self.clip_k[kvh], self.cb_k, kvh)
+        pv, sv, zv = self._quantize(v_bits[None, :], self.R_v[kvh], self.clip_v[kvh], self.cb_v, kvh)
         self.codes_k[page, kvh, row], self.scale_k[page, kvh, row], self.zero_k[page, kvh, row] = pk[0], sk[0], zk[0]
         self.codes_v[page, kvh, row], self.scale_v[page, kvh, row], self.zero_v[page, kvh, row] = pv[0], sv[0], zv[0]
+
+    def _quantize(self, X, R, clip, cb, kvh):
+        if cb is None:
+            return quant.quantize_vectors_many(X, R, clip, self.g)
+        return codebook.quantize_vectors_cb(X, R, clip, self.g, cb[kvh])
+
+    def _dequantize(self, packed, scale, zero, cb, kvh):
+        if cb is None:
+            return quant.dequantize(packed, scale, zero, self.g)
+        return codebook.dequantize_cb(packed, scale, zero, self.g, cb[kvh])
 
     def prefill(self, b, K_bits, V_bits, heads=None, shared_pages=0):
         """K_bits, V_bits: bf16 [L][Hkv][d] of one sequence; fills its three segments (history of the
@@ -77,10 +91,10 @@ class Pool:
         t = np.arange(shared_pages * PAGE, nh)
         pages, rows = self.page_table[b, t // PAGE], t % PAGE
         for kvh in (range(self.Hkv) if heads is None else heads):
-            for X, R, clip, codes, scale, zero in (
-                    (K_bits, self.R_k, self.clip_k, self.codes_k, self.scale_k, self.zero_k),
-                    (V_bits, self.R_v, self.clip_v, self.codes_v, self.scale_v, self.zero_v)):
-                pc, sc, zc = quant.quantize_vectors_many(X[ns + t, kvh], R[kvh], clip[kvh], self.g)
+            for X, R, clip, cb, codes, scale, zero in (
+                    (K_bits, self.R_k, self.clip_k, self.cb_k, self.codes_k, self.scale_k, self.zero_k),
+                    (V_bits, self.R_v, self.clip_v, self.cb_v, self.codes_v, self.scale_v, self.zero_v)):
+                pc, sc, zc = self._quantize(X[ns + t, kvh], R[kvh], clip[kvh], cb, kvh)
                 codes[pages, kvh, rows], scale[pages, kvh, rows], zero[pages, kvh, rows] = pc, sc, zc
         self.recent_k[b, :, :nr] = K_bits[ns + nh:].transpose(1, 0, 2)
         self.recent_v[b, :, :nr] = V_bits[ns + nh:].transpose(1, 0, 2)
@@ -122,10 +136,10 @@ class Pool:
         slots = [(rs + i) % RECENT for i in range(nr)]
         t = np.arange(nh)
         pages, rows = self.page_table[b, t // PAGE], t % PAGE
-        hk = quant.dequantize(self.codes_k[pages, kvh, rows], self.scale_k[pages, kvh, rows],
-                              self.zero_k[pages, kvh, rows], self.g)
-        hv = quant.dequantize(self.codes_v[pages, kvh, rows], self.scale_v[pages, kvh, rows],
-                              self.zero_v[pages, kvh, rows], self.g)
+        hk = self._dequantize(self.codes_k[pages, kvh, rows], self.scale_k[pages, kvh, rows],
+                              self.zero_k[pages, kvh, rows], self.cb_k, kvh)
+        hv = self._dequantize(self.codes_v[pages, kvh, rows], self.scale_v[pages, kvh, rows],
+                              self.zero_v[pages, kvh, rows], self.cb_v, kvh)
         return (f(self.sink_k[b, kvh, :ns]), f(self.sink_v[b, kvh, :ns]), hk, hv,
                 f(self.recent_k[b, kvh, slots]), f(self.recent_v[b, kvh, slots]))
 
