@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["decode100k", "batch-sweep", "bulk", "mixed", "bf16-compare",
-                                           "shared-prefix", "quality"],
+                                           "shared-prefix", "quality", "codebook"],
                     default="decode100k",
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -392,6 +392,62 @@ def shared_prefix(args, peak):
     return lines
 
 
+def codebook_compare(args, peak):
+    """The 100k-context, batch-1 decode step over a pool whose history carries Lloyd-Max codebooks
+    (calibrated by the library on the first 4,096 tokens of each layer's keys and values) against the
+    same step over uniform-INT2 pools, round-robin over 4 layers per arm (history larger than L2)."""
+    import numpy as np
+    import torch
+    import bit_rotated_kv_02_gb300 as ok
+    import synth
+    steps, warm = max(3, min(args.steps, 400)), max(3, min(args.warmup, 20))
+    n_layers, hist = 4, L_CTX - SINK - RECENT
+    pages = -(-(hist + (steps + warm) // n_layers + 16) // PAGE)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(7171)
+    chan = torch.from_numpy(synth.outlier_channels(2024, HKV, D, 4).astype(np.int64)).cuda()
+    Rk, Rv = _gpu_rotations(ok, HKV, D, 100), _gpu_rotations(ok, HKV, D, 200)
+    clip = torch.full((HKV,), CLIP)
+    arms = {"uniform": [], "lloyd_max": []}
+    t0 = time.time()
+    for l in range(n_layers):
+        K, V = _gpu_kv(gen, L_CTX, HKV, chan), _gpu_kv(gen, L_CTX, HKV, chan)
+        cbk = ok.oscar_lloyd_max_codebook(K[:4096].contiguous(), Rk.cuda(), clip.cuda())
+        cbv = ok.oscar_lloyd_max_codebook(V[:4096].contiguous(), Rv.cuda(), clip.cuda())
+        pt = torch.randperm(pages, generator=gen, device="cuda").to(torch.int32)[None]
+        for name, cbs in (("uniform", (None, None)), ("lloyd_max", (cbk, cbv))):
+            P = ok.Pool(1, HQ, HKV, GROUP, pages, pages, Rk, Rv, clip, clip, codebook_k=cbs[0], codebook_v=cbs[1])
+            P.set_page_table(pt)
+            ok.oscar_prefill_pool(P, 0, K, V)
+            arms[name].append(P)
+        del K, V
+    torch.cuda.synchronize()
+    calib_s = time.time() - t0
+    q = (torch.randn((1, HQ, D), generator=gen, device="cuda") * 3).to(torch.bfloat16)
+    kn, vn = _gpu_kv(gen, 1, HKV, chan), _gpu_kv(gen, 1, HKV, chan)
+    out = torch.empty((1, HQ, D), dtype=torch.float32, device="cuda")
+    lines = []
+    byts = hist * HKV * 2 * (D // 4 + 4) + (SINK + RECENT) * HKV * 2 * D * 2
+    for name, layers in arms.items():
+        ws = torch.empty(ok.oscar_decode_workspace_size(layers[0]), dtype=torch.uint8, device="cuda")
+        it = [0]
+
+        def step():
+            ok.oscar_decode_step(layers[it[0] % n_layers], kn, vn, q, out=out, ws=ws)
+            it[0] += 1
+        ms = _time(step, steps, warm)
+        for P in layers:
+            assert P.err() == 0, hex(P.err())
+        lines.append({"metric": "decode step (append+demote + attention): KV tokens/s", "variant": name,
+                      "workload": WORKLOAD + (", Lloyd-Max codebooks" if name == "lloyd_max" else ", uniform INT2"),
+                      "value": L_CTX / (ms * 1e-3), "unit": "KV tokens/s", "ms_per_step": ms, "steps": steps,
+                      "step_gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak,
+                      "decode_path": "tensor-core INT2" if name == "uniform" else "CUDA-core codebook levels",
+                      "setup_s_incl_calibration": calib_s})
+        del ws
+    return lines
+
+
 def quality_workload(args):
     """Attention quality of the four variants of the pages' Fig. 1 (naive INT2, Hadamard-only, clip-only,
     OSCAR) on one Qwen3-8B-shaped layer (32 query / 8 KV heads): calibration-style synthetic activations
@@ -411,8 +467,15 @@ def quality_workload(args):
     V = dev(np.stack([kv[:, 1] for kv in KV], 1))
     Qd = dev(Qs)
     lines = []
-    for name, (Rk, Rv, c) in quality.variants(Qd[:T], K[:T], V[:T]).items():
-        kl, err = quality.measure(K[T:], V[T:], Qd[T], Rk, Rv, [c] * HKV, [c] * HKV)
+    vs = quality.variants(Qd[:T], K[:T], V[:T])
+    runs = [(name, Rk, Rv, c, None) for name, (Rk, Rv, c) in vs.items()]
+    Rk, Rv, c = vs["oscar"]
+    # OSCAR's rotation plus Lloyd-Max codebooks calibrated on the same calibration keys and values
+    runs.append(("oscar_lloyd_max", Rk, Rv, c, quality.lloyd_max_codebooks(K[:T], V[:T], Rk, Rv, c)))
+    for name, Rk, Rv, c, cbs in runs:
+        cbk, cbv = (None, None) if cbs is None else cbs
+        kl, err = quality.measure(K[T:], V[T:], Qd[T], Rk, Rv, [c] * HKV, [c] * HKV, codebook_k=cbk,
+                                  codebook_v=cbv)
         lines.append({"metric": "attention quality vs exact BF16 attention (score KL, relative output error)",
                       "variant": name, "score_kl": kl, "output_rel_sq_error": err, "clip": c,
                       "workload": "qwen3-8b-layer, calibration-style synthetic activations, 4,416-token context",
@@ -437,6 +500,8 @@ def other_workload(args):
         return shared_prefix(args, peak)
     if args.workload == "quality":
         return quality_workload(args)
+    if args.workload == "codebook":
+        return codebook_compare(args, peak)
     gen = torch.Generator(device="cuda")
     gen.manual_seed(4242)
     lines = []

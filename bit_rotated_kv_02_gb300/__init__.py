@@ -23,7 +23,7 @@ ROT_HAAR, ROT_COVARIANCE = 0, 1
 DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT = 1, 2, 4, 8
 
 __all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
-           "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_prefill_pool", "oscar_prefill_pool_shared", "oscar_demote", "oscar_append_kv",
+           "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_quantize_kv_codebook", "oscar_lloyd_max_codebook", "oscar_prefill_pool", "oscar_prefill_pool_shared", "oscar_demote", "oscar_append_kv",
            "oscar_decode_workspace_size", "oscar_decode_attention", "oscar_profile_events",
            "oscar_decode_attention_noalloc", "NOALLOC_SCRATCH_BYTES", "lib", "BF16Cache", "oscar_bf16_prefill",
            "oscar_bf16_append_kv", "oscar_bf16_decode_workspace_size", "oscar_bf16_decode_attention",
@@ -110,11 +110,47 @@ def oscar_quantize_kv(x, R32, clip, group_size, codes=None, scale=None, zero=Non
     return codes, scale, zero
 
 
+def oscar_quantize_kv_codebook(x, R32, clip, codebook, group_size=HEAD_DIM, codes=None, scale=None, zero=None,
+                               stats=None, stream=None):
+    """oscar_quantize_kv with the four levels codebook fp32 [Hkv][4] in place of the uniform 0, 1, 2, 3."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(R32, torch.float32, "R32")
+    _dev(clip, torch.float32, "clip")
+    _dev(codebook, torch.float32, "codebook")
+    N, Hkv, d = x.shape
+    ng = d // group_size
+    codes = torch.empty((N, Hkv, d // 4), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scale = torch.empty((N, Hkv, ng), dtype=torch.bfloat16, device=x.device) if scale is None else scale
+    zero = torch.empty((N, Hkv, ng), dtype=torch.bfloat16, device=x.device) if zero is None else zero
+    _lib.check(lib().oscar_quantize_kv_codebook(N, Hkv, d, group_size, _p(x), _p(R32), _p(clip), _p(codebook),
+                                                _p(codes), _p(scale), _p(zero), _p(stats), _s(stream)),
+               "oscar_quantize_kv_codebook")
+    return codes, scale, zero
+
+
+def oscar_lloyd_max_codebook(x, R32, clip, group_size=HEAD_DIM, max_iters=200, codebook=None, ws=None, stream=None):
+    """Lloyd-Max levels fp32 [Hkv][4] per KV head from the calibration rows x bf16 [n][Hkv][128]."""
+    _dev(x, torch.bfloat16, "x")
+    _dev(R32, torch.float32, "R32")
+    _dev(clip, torch.float32, "clip")
+    N, Hkv, d = x.shape
+    codebook = torch.empty((Hkv, 4), dtype=torch.float32, device=x.device) if codebook is None else codebook
+    n = C.c_size_t(0)
+    _lib.check(lib().oscar_lloyd_max_workspace_size(N, Hkv, C.byref(n)), "oscar_lloyd_max_workspace_size")
+    if ws is None:
+        ws = torch.empty(max(n.value, 16), dtype=torch.uint8, device=x.device)
+    _lib.check(lib().oscar_lloyd_max_codebook(N, Hkv, d, group_size, _p(x), _p(R32), _p(clip), max_iters,
+                                              _p(codebook), _p(ws), ws.numel(), _s(stream)),
+               "oscar_lloyd_max_codebook")
+    return codebook
+
+
 class Pool:
-    """Device storage of one layer's three-segment pool plus its C struct (see include/oscar.h)."""
+    """Device storage of one layer's three-segment pool plus its C struct (see include/oscar.h).
+    codebook_k, codebook_v: optional fp32 [Hkv][4] Lloyd-Max levels (None: the uniform INT2 levels)."""
 
     def __init__(self, batch, num_q_heads, num_kv_heads, group_size, num_pages, max_pages, R_k, R_v, clip_k, clip_v,
-                 device="cuda", head_dim=HEAD_DIM):
+                 device="cuda", head_dim=HEAD_DIM, codebook_k=None, codebook_v=None):
         dev = torch.device(device)
         self.B, self.Hq, self.Hkv, self.d, self.g = batch, num_q_heads, num_kv_heads, head_dim, group_size
         self.ng = head_dim // group_size
@@ -137,13 +173,17 @@ class Pool:
         self.clip_v = clip_v.to(dev, torch.float32).contiguous()
         self.err_word = z(1, dt=torch.int32)
         self.sync = z(batch, dt=torch.int32)
+        cbk = lambda cb: None if cb is None else torch.as_tensor(cb, dtype=torch.float32).to(dev).reshape(
+            num_kv_heads, 4).contiguous()
+        self.codebook_k, self.codebook_v = cbk(codebook_k), cbk(codebook_v)
         self.struct = _lib.oscar_pool(
             batch, num_q_heads, num_kv_heads, head_dim, group_size, num_pages, max_pages,
             *(t.data_ptr() for t in (self.sink_k, self.sink_v, self.recent_k, self.recent_v, self.codes_k,
                                      self.codes_v, self.scale_k, self.zero_k, self.scale_v, self.zero_v,
                                      self.page_table, self.sink_len, self.hist_len, self.recent_start,
                                      self.recent_len, self.R_k, self.R_v, self.clip_k, self.clip_v, self.err_word,
-                                     self.sync)))
+                                     self.sync)),
+            *(None if t is None else t.data_ptr() for t in (self.codebook_k, self.codebook_v)))
 
     @property
     def ref(self):

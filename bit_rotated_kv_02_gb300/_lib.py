@@ -28,7 +28,8 @@ class oscar_pool(C.Structure):
                 ("scale_v", C.c_void_p), ("zero_v", C.c_void_p), ("page_table", C.c_void_p),
                 ("sink_len", C.c_void_p), ("hist_len", C.c_void_p), ("recent_start", C.c_void_p),
                 ("recent_len", C.c_void_p), ("R_k", C.c_void_p), ("R_v", C.c_void_p), ("clip_k", C.c_void_p),
-                ("clip_v", C.c_void_p), ("err", C.c_void_p), ("sync", C.c_void_p)]
+                ("clip_v", C.c_void_p), ("err", C.c_void_p), ("sync", C.c_void_p),
+                ("codebook_k", C.c_void_p), ("codebook_v", C.c_void_p)]
 
 
 class oscar_bf16_cache(C.Structure):
@@ -50,6 +51,9 @@ SIGNATURES = {
     "oscar_calib_covariance_v_workspace_size": ([I64, I32, I32], SZ),
     "oscar_calib_covariance_v": ([I64, I32, I32, P, P, P, F64, P, P, SZ, P], C.c_int),
     "oscar_quantize_kv": ([I64, I32, I32, I32, P, P, P, P, P, P, P, P], C.c_int),
+    "oscar_quantize_kv_codebook": ([I64, I32, I32, I32, P, P, P, P, P, P, P, P, P], C.c_int),
+    "oscar_lloyd_max_workspace_size": ([I64, I32, C.POINTER(C.c_size_t)], C.c_int),
+    "oscar_lloyd_max_codebook": ([I64, I32, I32, I32, P, P, P, I32, P, P, C.c_size_t, P], C.c_int),
     "oscar_prefill_pool": ([PP, I32, I64, P, P, P, P], C.c_int),
     "oscar_prefill_pool_shared": ([PP, I32, I64, P, P, I32, P, P], C.c_int),
     "oscar_demote": ([PP, P, P], C.c_int),

@@ -71,7 +71,10 @@ oscar_status_t check_pool(const oscar_pool *pool, PoolArgs &a) {
   a.codes_k = p.codes_k; a.codes_v = p.codes_v; a.scale_k = p.scale_k; a.zero_k = p.zero_k;
   a.scale_v = p.scale_v; a.zero_v = p.zero_v; a.page_table = p.page_table; a.sink_len = p.sink_len;
   a.hist_len = p.hist_len; a.recent_start = p.recent_start; a.recent_len = p.recent_len;
+  if ((reinterpret_cast<uintptr_t>(p.codebook_k) | reinterpret_cast<uintptr_t>(p.codebook_v)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "pool codebooks must be 16-byte aligned");
   a.R_k = p.R_k; a.R_v = p.R_v; a.clip_k = p.clip_k; a.clip_v = p.clip_v; a.err = p.err; a.sync = p.sync;
+  a.cb_k = p.codebook_k; a.cb_v = p.codebook_v;
   return OSCAR_OK;
 }
 
@@ -201,6 +204,55 @@ oscar_status_t oscar_quantize_kv(int64_t n_tokens, int32_t num_kv_heads, int32_t
                      "quantize_kv");
 }
 
+oscar_status_t oscar_quantize_kv_codebook(int64_t n_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t group_size, const oscar_bf16 *x, const float *R32,
+                                          const float *clip, const float *codebook, uint8_t *codes,
+                                          oscar_bf16 *scale, oscar_bf16 *zero, uint32_t *stats,
+                                          oscar_stream_t stream) {
+  if (head_dim != OSCAR_HEAD_DIM) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d (only 128)", head_dim);
+  if (!supported_group(group_size)) return fail(OSCAR_ERR_UNSUPPORTED, "group_size %d", group_size);
+  if (n_tokens < 0 || num_kv_heads <= 0) return fail(OSCAR_ERR_INVALID_ARG, "bad sizes");
+  if (n_tokens == 0) return OSCAR_OK;
+  if (x == nullptr || R32 == nullptr || clip == nullptr || codebook == nullptr || codes == nullptr ||
+      scale == nullptr || zero == nullptr)
+    return fail(OSCAR_ERR_INVALID_ARG, "NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(R32) | reinterpret_cast<uintptr_t>(codes) |
+       reinterpret_cast<uintptr_t>(codebook)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "x, R32, codebook and codes must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(scale) | reinterpret_cast<uintptr_t>(zero)) & 7u)
+    return fail(OSCAR_ERR_INVALID_ARG, "scale and zero must be 8-byte aligned");
+  return cuda_status(launch_quantize_rows_cb(n_tokens, num_kv_heads, group_size, x, (int64_t)num_kv_heads * head_dim,
+                                             R32, clip, codebook, codes, scale, zero, nullptr, 0, nullptr, stats,
+                                             static_cast<cudaStream_t>(stream)),
+                     "quantize_kv_codebook");
+}
+
+oscar_status_t oscar_lloyd_max_workspace_size(int64_t n, int32_t num_kv_heads, size_t *bytes) {
+  if (bytes == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "bytes is NULL");
+  if (n < 0 || num_kv_heads <= 0) return fail(OSCAR_ERR_INVALID_ARG, "bad sizes");
+  *bytes = lloyd_ws_bytes(n, num_kv_heads);
+  return OSCAR_OK;
+}
+
+oscar_status_t oscar_lloyd_max_codebook(int64_t n, int32_t num_kv_heads, int32_t head_dim, int32_t group_size,
+                                        const oscar_bf16 *x, const float *R32, const float *clip,
+                                        int32_t max_iters, float *codebook, void *ws, size_t ws_bytes,
+                                        oscar_stream_t stream) {
+  if (head_dim != OSCAR_HEAD_DIM) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d (only 128)", head_dim);
+  if (!supported_group(group_size)) return fail(OSCAR_ERR_UNSUPPORTED, "group_size %d", group_size);
+  if (n < 0 || num_kv_heads <= 0 || max_iters < 0) return fail(OSCAR_ERR_INVALID_ARG, "bad sizes");
+  if (codebook == nullptr || (n > 0 && (x == nullptr || R32 == nullptr || clip == nullptr)))
+    return fail(OSCAR_ERR_INVALID_ARG, "NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(R32) | reinterpret_cast<uintptr_t>(ws)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "x, R32 and ws must be 16-byte aligned");
+  const size_t need = lloyd_ws_bytes(n, num_kv_heads);
+  if (need > 0 && (ws == nullptr || ws_bytes < need))
+    return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
+  return cuda_status(launch_lloyd_max(n, num_kv_heads, group_size, x, R32, clip, max_iters, codebook, ws,
+                                      static_cast<cudaStream_t>(stream)),
+                     "lloyd_max_codebook");
+}
+
 oscar_status_t oscar_prefill_pool(const oscar_pool *pool, int32_t seq, int64_t len, const oscar_bf16 *k,
                                   const oscar_bf16 *v, uint32_t *stats, oscar_stream_t stream) {
   PoolArgs a;
@@ -257,13 +309,19 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
   return cuda_status(launch_demote(a, nullptr, 2, k_new, v_new, static_cast<cudaStream_t>(stream)), "append_kv");
 }
 
+// Whole-vector groups with the uniform levels decode on the tensor-core path (codes as exact small
+// integers in the MMA); other group sizes and codebook pools on the CUDA-core path.
+static bool tensor_core_path(const PoolArgs &a) {
+  return a.g == OSCAR_HEAD_DIM && a.cb_k == nullptr && a.cb_v == nullptr;
+}
+
 oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_splits, size_t *bytes) {
   PoolArgs a;
   oscar_status_t st = check_pool(pool, a);
   if (st != OSCAR_OK) return st;
   if (bytes == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "bytes is NULL");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
-  if (a.g == OSCAR_HEAD_DIM) {
+  if (tensor_core_path(a)) {
     *bytes = v1_ws_bytes(a);
   } else {
     const int s = num_splits == 0 ? auto_splits(a) : num_splits;
@@ -280,7 +338,7 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
-  if (a.g == OSCAR_HEAD_DIM) {
+  if (tensor_core_path(a)) {
     const size_t need = v1_ws_bytes(a);
     if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
     if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
@@ -305,7 +363,7 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
     return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
-  if (a.g != OSCAR_HEAD_DIM) {
+  if (!tensor_core_path(a)) {
     if ((st = oscar_append_kv(pool, k_new, v_new, stream)) != OSCAR_OK) return st;
     return oscar_decode_attention(pool, q, out, softmax_scale, 0, ws, ws_bytes, stream);
   }

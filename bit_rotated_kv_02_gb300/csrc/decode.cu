@@ -26,6 +26,10 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+__device__ __forceinline__ float level(uint32_t code, float4 l) {
+  return code < 2 ? (code == 0 ? l.x : l.y) : (code == 2 ? l.z : l.w);
+}
+
 // Online-softmax update of one 32-token chunk for G heads; scores s[h] are lane-local (one token per
 // lane), o[h][k] are lane-local output channels 4*lane+k.  p values go to pbuf[h][lane].
 template <int G>
@@ -124,6 +128,9 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
   }
   const int t0 = split * pps * PAGE;
   const int t1 = min(t0 + pps * PAGE, hl);
+  // dequantization levels of this KV head (the uniform 0, 1, 2, 3 without a codebook)
+  const float4 lk = p.cb_k != nullptr ? reinterpret_cast<const float4 *>(p.cb_k)[kvh] : make_float4(0.f, 1.f, 2.f, 3.f);
+  const float4 lv = p.cb_v != nullptr ? reinterpret_cast<const float4 *>(p.cb_v)[kvh] : make_float4(0.f, 1.f, 2.f, 3.f);
   const int32_t *pt = p.page_table + (size_t)b * p.max_pages;
 
   float m[G], l[G], o[G][4];
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
       for (int w = 0; w < 8; ++w) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float cf = (float)((words[w] >> (2 * j)) & 3u);
+          const float cf = level((words[w] >> (2 * j)) & 3u, lk);
           const int c = 16 * w + j;
 #pragma unroll
           for (int h = 0; h < G; ++h) r[h] = fmaf(cf, qr[c][h], r[h]);
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
       const float z = bf16_to_f32(p.zero_v[row * ng + gi]);
       float v[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = fmaf((float)((byte >> (2 * k)) & 3u), sc, z);
+      for (int k = 0; k < 4; ++k) v[k] = fmaf(level((byte >> (2 * k)) & 3u, lv), sc, z);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float pj = pbuf[warp][h][j];

@@ -935,7 +935,7 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
         }
         QuantStats qst{0, 0, 0};
         quantize_from_dots(xdem[kv], Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcodes[kv],
-                           &dscale[kv], &dzero[kv], qst);
+                           &dscale[kv], &dzero[kv], qst);  // the step's merge serves uniform pools only
       }
     }
   }

@@ -52,8 +52,17 @@ cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, cons
 cudaError_t launch_quantize_rows(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride, const float *R32,
                                  const float *clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
                                  const int32_t *pt, int num_pages, uint32_t *err, uint32_t *stats, cudaStream_t s);
+// The same with codebook levels cb [Hkv][4] (CUDA-core rotation; the tensor-core kernel serves the uniform levels).
+cudaError_t launch_quantize_rows_cb(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride,
+                                    const float *R32, const float *clip, const float *cb, uint8_t *codes,
+                                    uint16_t *scale, uint16_t *zero, const int32_t *pt, int num_pages, uint32_t *err,
+                                    uint32_t *stats, cudaStream_t s);
 cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
                            cudaStream_t s, int skip = 0);
+// codebook.cu: Lloyd-Max levels [Hkv][4] from calibration rows x [n][Hkv][D] (workspace: lloyd_ws_bytes).
+size_t lloyd_ws_bytes(int64_t n, int Hkv);
+cudaError_t launch_lloyd_max(int64_t n, int Hkv, int g, const uint16_t *x, const float *R32, const float *clip,
+                             int iters, float *cb_out, void *ws, cudaStream_t s);
 
 // decode.cu
 constexpr int PART_STRIDE = D + 4;  // one partial: o[128], m, l, pad

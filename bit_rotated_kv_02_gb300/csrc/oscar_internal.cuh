@@ -32,6 +32,7 @@ struct PoolArgs {
   const float *R_k, *R_v, *clip_k, *clip_v;
   uint32_t *err;
   int32_t *sync;
+  const float *cb_k, *cb_v;  // [Hkv][4] codebook levels, or nullptr for the uniform levels 0, 1, 2, 3
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
@@ -47,6 +48,19 @@ __device__ __forceinline__ int code_of(float x, float zero, float scale, bool va
   if (!valid) return 0;
   const float t = __fdiv_rn(__fsub_rn(x, zero), scale);
   return (int)fminf(fmaxf(rintf(t), 0.0f), 3.0f);   // rintf: nearest, ties to even
+}
+
+// Codebook quantizer: the level l_i nearest to t = (x - zero) / scale, ties to the even index, from the
+// float32 midpoints m = (m_0, m_1, m_2), m_i = (l_i + l_{i+1}) / 2: code = #{i : t > m_i} + (t == m_1).
+// The uniform levels (0, 1, 2, 3) give clamp(rint(t), 0, 3).  Monotone in x for scale > 0.
+__device__ __forceinline__ float3 level_midpoints(const float *cb) {
+  return make_float3(__fmul_rn(__fadd_rn(cb[0], cb[1]), 0.5f), __fmul_rn(__fadd_rn(cb[1], cb[2]), 0.5f),
+                     __fmul_rn(__fadd_rn(cb[2], cb[3]), 0.5f));
+}
+__device__ __forceinline__ int code_of_levels(float x, float zero, float scale, bool valid, float3 m) {
+  if (!valid) return 0;
+  const float t = __fdiv_rn(__fsub_rn(x, zero), scale);
+  return (t > m.x) + (t > m.y) + (t > m.z) + (t == m.y);
 }
 
 // ---- exact rotated element --------------------------------------------------------------
@@ -235,10 +249,11 @@ static __device__ __noinline__ float2 dot2_interval_xs(const float *xs, const fl
 // when both ends of the element's interval give the same code.
 // R: the rotation in global memory (float64 / integer tier); R2, ld2: the same values for the Dot2
 // tier (a shared-memory copy with row stride ld2, or R itself with ld2 = 128).
+// cb: the four codebook levels of this (KV head, K/V), or nullptr for the uniform levels.
 __device__ inline void quantize_from_dots(const float *xs, const float *R, const float *R2, int ld2,
                                           const float (&acc)[4], const float (&sab)[4], float clip, int g,
                                           uint8_t *codes_out, uint16_t *scale_out, uint16_t *zero_out,
-                                          QuantStats &st) {
+                                          QuantStats &st, const float *cb = nullptr) {
   const int lane = threadIdx.x & 31;
   const int gl = g / 4;  // lanes per group (8, 16 or 32)
   // gamma_128 = 7.6294e-6; 8e-6 also covers the rounding of sab itself; 1e-37 covers underflow.
@@ -318,13 +333,15 @@ __device__ inline void quantize_from_dots(const float *xs, const float *R, const
   }
   const float zf = bf16_to_f32(z), sf = bf16_to_f32(s);
   const bool valid = sf != 0.0f && isfinite(sf);
+  const float3 mids = cb != nullptr ? level_midpoints(cb) : make_float3(0.f, 0.f, 0.f);
+  auto code_at = [&](float x) { return cb != nullptr ? code_of_levels(x, zf, sf, valid, mids) : code_of(x, zf, sf, valid); };
   int code[4];
   for (int tier = 0; tier < 3; ++tier) {
     bool need[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      code[k] = code_of(lo[k], zf, sf, valid);
-      need[k] = code[k] != code_of(hi[k], zf, sf, valid);
+      code[k] = code_at(lo[k]);
+      need[k] = code[k] != code_at(hi[k]);
     }
     if (tier == 2 || !__any_sync(FULL, need[0] || need[1] || need[2] || need[3])) break;
     evaluate(need, tier);

@@ -4,6 +4,8 @@
 // first written into the recent window; as decoding advances the oldest recent token is rotated,
 // clipped, quantized and packed by a fused kernel and demoted into the INT2 history; sink and
 // recent stay BF16.
+#include <algorithm>
+
 #include "oscar_internal.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -108,10 +110,11 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
       const float clip = (kv == 0 ? p.clip_k : p.clip_v)[kvh];
       const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
       QuantStats st{0, 0, 0};
+      const float *cb = kv == 0 ? p.cb_k : p.cb_v;
       quantize_from_dots(xs, Rw, reinterpret_cast<const float *>(rs4), RS_LD, acc, sab, clip, p.g,
                          (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
                          (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
-                         st);
+                         st, cb != nullptr ? cb + 4 * kvh : nullptr);
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
@@ -150,6 +153,59 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Rotate / clip / quantize / pack with a codebook (the Lloyd-Max levels of this (KV head, K or V); the
+// tensor-core bulk kernel serves the uniform levels): grid (ctas per head, Hkv), 256 threads.  The CTA
+// holds R of its KV head in shared memory (padded rows); warp w quantizes rows r = 8 blockIdx.x + w,
+// stepping by 8 gridDim.x: dots by FMA over the 128 rows of R (lane: 4 columns), then quantize_from_dots
+// with the codebook, its compensated-dot tier reading the shared copy of R.  Output rows as in
+// launch_quantize_rows (dense, or through the page table).
+__global__ void __launch_bounds__(256, 1) quantize_rows_cb_kernel(int64_t n, int Hkv, int g, const uint16_t *x,
+                                                                int64_t x_row_stride, const float *R32,
+                                                                const float *clip, const float *cb, uint8_t *codes,
+                                                                uint16_t *scale, uint16_t *zero, const int32_t *pt,
+                                                                int num_pages, uint32_t *err, uint32_t *stats) {
+  extern __shared__ float4 rs4[];  // R of this head, row stride RS_LD floats
+  __shared__ float xs[DEMOTE_WARPS][D];
+  const int h = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float *Rw = R32 + (size_t)h * D * D;
+  for (int i = threadIdx.x; i < D * (D / 4); i += blockDim.x)
+    rs4[(i / (D / 4)) * (RS_LD / 4) + (i % (D / 4))] = reinterpret_cast<const float4 *>(Rw)[i];
+  __syncthreads();
+  const float *Rs = reinterpret_cast<const float *>(rs4);
+  const float c = clip[h];
+  const int ng = D / g;
+  QuantStats st{0, 0, 0};
+  for (int64_t r = (int64_t)blockIdx.x * DEMOTE_WARPS + warp; r < n; r += (int64_t)gridDim.x * DEMOTE_WARPS) {
+    size_t drow;
+    if (pt == nullptr) {
+      drow = (size_t)r * Hkv + h;
+    } else {
+      const int page = pt[r / PAGE];
+      if (page < 0 || page >= num_pages) {
+        if (lane == 0 && err != nullptr) atomicOr(err, OSCAR_DEVERR_PAGE_INDEX);
+        continue;
+      }
+      drow = ((size_t)page * Hkv + h) * PAGE + (size_t)(r % PAGE);
+    }
+    load_vec_to_smem(x + (size_t)r * x_row_stride + (size_t)h * D, xs[warp]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) {
+      const float xi = xs[warp][i], ax = fabsf(xi);
+      const float4 rv = rs4[i * (RS_LD / 4) + lane];
+      acc[0] = fmaf(xi, rv.x, acc[0]); acc[1] = fmaf(xi, rv.y, acc[1]);
+      acc[2] = fmaf(xi, rv.z, acc[2]); acc[3] = fmaf(xi, rv.w, acc[3]);
+      sab[0] = fmaf(ax, fabsf(rv.x), sab[0]); sab[1] = fmaf(ax, fabsf(rv.y), sab[1]);
+      sab[2] = fmaf(ax, fabsf(rv.z), sab[2]); sab[3] = fmaf(ax, fabsf(rv.w), sab[3]);
+    }
+    quantize_from_dots(xs[warp], Rw, Rs, RS_LD, acc, sab, c, g, codes + drow * (D / 4), scale + drow * ng,
+                       zero + drow * ng, st, cb + 4 * h);
+    __syncwarp();
+  }
+  flush_stats(stats, st);
+}
+
 // Copy token rows [t0, t0+n) of x [L][Hkv][D] into dst [Hkv][cap][D] rows [0, n) of one sequence.
 __global__ void copy_rows_kernel(const uint16_t *x, int64_t t0, int n, int Hkv, uint16_t *dst, int cap) {
   const int kvh = blockIdx.y;
@@ -180,6 +236,23 @@ cudaError_t launch_demote(const PoolArgs &p, const int32_t *mask, int mode, cons
 
 // skip: the first `skip` history pages are already in place (shared with another sequence's identical
 // prefix through the page table) and are neither quantized nor written.
+cudaError_t launch_quantize_rows_cb(int64_t n, int Hkv, int g, const uint16_t *x, int64_t x_row_stride,
+                                    const float *R32, const float *clip, const float *cb, uint8_t *codes,
+                                    uint16_t *scale, uint16_t *zero, const int32_t *pt, int num_pages, uint32_t *err,
+                                    uint32_t *stats, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(quantize_rows_cb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DEMOTE_SMEM);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (n + DEMOTE_WARPS - 1) / DEMOTE_WARPS;
+  const int per_head = (int)std::min<int64_t>(want, std::max(1, 2 * sms / Hkv));
+  quantize_rows_cb_kernel<<<dim3(per_head, Hkv), 256, DEMOTE_SMEM, s>>>(n, Hkv, g, x, x_row_stride, R32, clip, cb,
+                                                                       codes, scale, zero, pt, num_pages, err, stats);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *k, const uint16_t *v, uint32_t *stats,
                            cudaStream_t s, int skip) {
   const int ns = (int)(L < SINK ? L : SINK);
@@ -203,11 +276,17 @@ cudaError_t launch_prefill(const PoolArgs &p, int b, int64_t L, const uint16_t *
   if (nh > first) {
     const int32_t *pt = p.page_table + (size_t)b * p.max_pages + skip;
     const int64_t n = nh - first, x0 = (int64_t)ns + first;
-    e = launch_quantize_rows(n, p.Hkv, p.g, k + (size_t)x0 * stride, stride, p.R_k, p.clip_k, p.codes_k, p.scale_k,
-                             p.zero_k, pt, p.num_pages, p.err, stats, s);
+    e = p.cb_k != nullptr
+            ? launch_quantize_rows_cb(n, p.Hkv, p.g, k + (size_t)x0 * stride, stride, p.R_k, p.clip_k, p.cb_k,
+                                      p.codes_k, p.scale_k, p.zero_k, pt, p.num_pages, p.err, stats, s)
+            : launch_quantize_rows(n, p.Hkv, p.g, k + (size_t)x0 * stride, stride, p.R_k, p.clip_k, p.codes_k,
+                                   p.scale_k, p.zero_k, pt, p.num_pages, p.err, stats, s);
     if (e != cudaSuccess) return e;
-    e = launch_quantize_rows(n, p.Hkv, p.g, v + (size_t)x0 * stride, stride, p.R_v, p.clip_v, p.codes_v, p.scale_v,
-                             p.zero_v, pt, p.num_pages, p.err, stats, s);
+    e = p.cb_v != nullptr
+            ? launch_quantize_rows_cb(n, p.Hkv, p.g, v + (size_t)x0 * stride, stride, p.R_v, p.clip_v, p.cb_v,
+                                      p.codes_v, p.scale_v, p.zero_v, pt, p.num_pages, p.err, stats, s)
+            : launch_quantize_rows(n, p.Hkv, p.g, v + (size_t)x0 * stride, stride, p.R_v, p.clip_v, p.codes_v,
+                                   p.scale_v, p.zero_v, pt, p.num_pages, p.err, stats, s);
     if (e != cudaSuccess) return e;
   }
   set_counters_kernel<<<1, 1, 0, s>>>(p, b, ns, (int)nh, nr);

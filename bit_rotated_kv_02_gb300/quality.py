@@ -15,7 +15,8 @@ kernels); the exact attention, the dequantization of the stored history for p_ha
 are plain float64 tensor arithmetic on the same device (measurement, not part of the decode path).
 
 Variants (rotation R, clip ratio c): naive INT2 (I, 1), Hadamard-only (H . P, 1), clip-only (I, c),
-OSCAR (U . H . P with U from the calibration covariances, c).
+OSCAR (U . H . P with U from the calibration covariances, c); OSCAR's rotation may further carry
+Lloyd-Max codebooks calibrated on the same keys and values (the closing comparison with TurboQuant).
 """
 from __future__ import annotations
 
@@ -24,7 +25,8 @@ import math
 import torch
 
 from . import (HEAD_DIM, PAGE, RECENT, SINK, ROT_COVARIANCE, ROT_HAAR, Pool, oscar_calib_covariance_k,
-               oscar_calib_covariance_v, oscar_decode_attention, oscar_make_rotation, oscar_prefill_pool)
+               oscar_calib_covariance_v, oscar_decode_attention, oscar_lloyd_max_codebook, oscar_make_rotation,
+               oscar_prefill_pool)
 
 
 def identity_rotation(num_kv_heads: int, device="cuda") -> torch.Tensor:
@@ -59,7 +61,9 @@ def _dequant_history(P: Pool, kvh: int, which: str) -> torch.Tensor:
     pages, rows = P.page_table[0, t // PAGE].long(), t % PAGE
     codes = getattr(P, "codes_" + which)[pages, kvh, rows]                      # u8 [hl][d/4]
     shifts = torch.arange(4, device=codes.device, dtype=torch.uint8) * 2
-    c = ((codes[..., None] >> shifts) & 3).reshape(hl, HEAD_DIM).double()      # channel 4b+i: byte b, bits 2i
+    c = ((codes[..., None] >> shifts) & 3).reshape(hl, HEAD_DIM)               # channel 4b+i: byte b, bits 2i
+    cb = getattr(P, "codebook_" + which)
+    c = c.double() if cb is None else cb[kvh].double()[c.long()]               # level of each code
     scale = getattr(P, "scale_" + which)[pages, kvh, rows].double()            # [hl][d/g]
     zero = getattr(P, "zero_" + which)[pages, kvh, rows].double()
     g = HEAD_DIM // scale.shape[1]
@@ -67,10 +71,10 @@ def _dequant_history(P: Pool, kvh: int, which: str) -> torch.Tensor:
 
 
 def measure(K: torch.Tensor, V: torch.Tensor, q: torch.Tensor, R_k: torch.Tensor, R_v: torch.Tensor, clip_k,
-            clip_v, group_size: int = HEAD_DIM, softmax_scale=None):
+            clip_v, group_size: int = HEAD_DIM, softmax_scale=None, codebook_k=None, codebook_v=None):
     """(mean score KL, relative output error) of one sequence of tokens K, V (bf16 [L][Hkv][d], CUDA)
-    stored in an INT2 pool with rotations R_k, R_v (fp32 [Hkv][d][d]) and clip ratios clip_k, clip_v
-    ([Hkv]), for the queries q (bf16 [Hq][d])."""
+    stored in an INT2 pool with rotations R_k, R_v (fp32 [Hkv][d][d]), clip ratios clip_k, clip_v
+    ([Hkv]) and optional codebooks (fp32 [Hkv][4]), for the queries q (bf16 [Hq][d])."""
     L, Hkv, d = K.shape
     Hq = q.shape[0]
     G = Hq // Hkv
@@ -78,7 +82,8 @@ def measure(K: torch.Tensor, V: torch.Tensor, q: torch.Tensor, R_k: torch.Tensor
     pages = max(1, -(-max(L - SINK - RECENT, 0) // PAGE))
     clip_k = torch.as_tensor(clip_k, dtype=torch.float32).reshape(Hkv)
     clip_v = torch.as_tensor(clip_v, dtype=torch.float32).reshape(Hkv)
-    P = Pool(1, Hq, Hkv, group_size, pages, pages, R_k, R_v, clip_k, clip_v, device=K.device)
+    P = Pool(1, Hq, Hkv, group_size, pages, pages, R_k, R_v, clip_k, clip_v, device=K.device, codebook_k=codebook_k,
+             codebook_v=codebook_v)
     P.set_page_table(torch.arange(pages, dtype=torch.int32)[None])
     oscar_prefill_pool(P, 0, K.contiguous(), V.contiguous())
     o_hat = oscar_decode_attention(P, q[None].contiguous(), softmax_scale=scale)[0].double()
@@ -102,6 +107,14 @@ def measure(K: torch.Tensor, V: torch.Tensor, q: torch.Tensor, R_k: torch.Tensor
             num += float(torch.sum((o_hat[h] - o) ** 2))
             den += float(torch.sum(o ** 2))
     return sum(kls) / len(kls), num / den
+
+
+def lloyd_max_codebooks(Kc: torch.Tensor, Vc: torch.Tensor, R_k: torch.Tensor, R_v: torch.Tensor, clip: float = 0.9,
+                        group_size: int = HEAD_DIM):
+    """Per-head Lloyd-Max levels (fp32 [Hkv][4]) of the calibration keys and values under R_k, R_v."""
+    c = torch.full((Kc.shape[1],), float(clip), dtype=torch.float32, device=Kc.device)
+    return (oscar_lloyd_max_codebook(Kc.contiguous(), R_k, c, group_size),
+            oscar_lloyd_max_codebook(Vc.contiguous(), R_v, c, group_size))
 
 
 def variants(Qc, Kc, Vc, clip: float = 0.9):

@@ -73,6 +73,14 @@ typedef void *oscar_stream_t;  /* cudaStream_t */
  *   sink_len, hist_len, recent_start, recent_len   int32 [batch]
  *   R_k, R_v                fp32  [Hkv][d][d]   rotation of keys / values (x_rot = x · R)
  *   clip_k, clip_v          fp32  [Hkv]         clip ratios in (0, 1]
+ *   codebook_k, codebook_v  fp32  [Hkv][4]      optional (NULL = uniform INT2): the four dequantization
+ *                                               levels l0 < l1 < l2 < l3 of a Lloyd-Max codebook in the
+ *                                               group's coordinate t = (x_rot - zero) / scale; a code is the
+ *                                               nearest level (ties to the even code) and dequantizes to
+ *                                               zero + scale * l[code]; 16-byte aligned.  Pools with a
+ *                                               codebook decode on the CUDA-core attention path, and
+ *                                               oscar_decode_step takes them through oscar_demote +
+ *                                               oscar_decode_attention (same results).
  *   err                     uint32 [1]          device error word (OSCAR_DEVERR_* bits)
  *   sync                    int32 [batch]       arrival counters; zero them once before the first
  *                                               call, every call leaves them zero again
@@ -93,6 +101,7 @@ typedef struct oscar_pool {
   const float *clip_k, *clip_v;
   uint32_t *err;
   int32_t *sync;
+  const float *codebook_k, *codebook_v;
 } oscar_pool;
 
 /* Description of the calling thread's last error ("" if none). Never NULL. */
@@ -157,6 +166,36 @@ oscar_status_t oscar_calib_covariance_v(int64_t T, int32_t heads, int32_t d, con
 oscar_status_t oscar_quantize_kv(int64_t n_tokens, int32_t num_kv_heads, int32_t head_dim, int32_t group_size,
                                  const oscar_bf16 *x, const float *R32, const float *clip, uint8_t *codes,
                                  oscar_bf16 *scale, oscar_bf16 *zero, uint32_t *stats, oscar_stream_t stream);
+
+/*
+ * oscar_quantize_kv with a codebook: the same rotation, scale and zero, and for each element the
+ * nearest of the four levels codebook[h][0..3] (float32, strictly increasing) to t = (x_hat - zero) / scale
+ * in float32, ties to the even code (midpoints m_i = (l_i + l_{i+1}) * 0.5 in float32;
+ * code = #{i : t > m_i} + (t == m_1)).  The levels (0, 1, 2, 3) give oscar_quantize_kv's codes.
+ *   codebook fp32 [Hkv][4], 16-byte aligned.  The rotation runs on the CUDA cores.
+ */
+oscar_status_t oscar_quantize_kv_codebook(int64_t n_tokens, int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t group_size, const oscar_bf16 *x, const float *R32,
+                                          const float *clip, const float *codebook, uint8_t *codes,
+                                          oscar_bf16 *scale, oscar_bf16 *zero, uint32_t *stats,
+                                          oscar_stream_t stream);
+
+/*
+ * Lloyd-Max calibration of a 4-level codebook per KV head ("超越TurboQuant！OSCAR：面向真实服务的2-bit
+ * KV Cache量化", closing comparison with TurboQuant: a Lloyd-Max codebook on top of the rotation).
+ * For the calibration rows x bf16 [n][Hkv][d] (keys or values), R32 fp32 [Hkv][d][d], clip fp32 [Hkv]:
+ * every element's t = (x_rot - zero) / scale with the uniform quantizer's bf16 scale and zero (x_rot by
+ * float32 FMA dots; groups with a zero or non-finite scale are left out), then Lloyd's method per head
+ * from the levels (0, 1, 2, 3): cells by the nearest level (ties to the even code, float64 midpoints),
+ * each level moved to its cell's mean (an empty cell keeps its level), until no level moves or
+ * max_iters iterations.  codebook: fp32 [Hkv][4] output.  ws: device scratch of at least
+ * oscar_lloyd_max_workspace_size bytes, 16-byte aligned.  x and R32 16-byte aligned.
+ */
+oscar_status_t oscar_lloyd_max_workspace_size(int64_t n, int32_t num_kv_heads, size_t *bytes);
+oscar_status_t oscar_lloyd_max_codebook(int64_t n, int32_t num_kv_heads, int32_t head_dim, int32_t group_size,
+                                        const oscar_bf16 *x, const float *R32, const float *clip,
+                                        int32_t max_iters, float *codebook, void *ws, size_t ws_bytes,
+                                        oscar_stream_t stream);
 
 /*
  * Bulk prefill of one sequence into the pool: tokens [0, 64) -> sink, [64, len-256) -> history

@@ -27,8 +27,9 @@ def oracle_rotations(seed: int, Hkv: int, d: int = 128):
     return np.stack([orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(seed + h, d))) for h in range(Hkv)])
 
 
-def make_pools(B, Hq, Hkv, g, pages_per_seq, seed, clip_k=None, clip_v=None, extra_pages=0):
-    """(oracle Pool, device Pool) with identical rotations, clips and shuffled page tables."""
+def make_pools(B, Hq, Hkv, g, pages_per_seq, seed, clip_k=None, clip_v=None, extra_pages=0, codebook_k=None,
+               codebook_v=None):
+    """(oracle Pool, device Pool) with identical rotations, clips, codebooks and shuffled page tables."""
     import bit_rotated_kv_02_gb300 as ok
     Rk = oracle_rotations(seed, Hkv)
     Rv = oracle_rotations(seed + 1000, Hkv)
@@ -36,10 +37,11 @@ def make_pools(B, Hq, Hkv, g, pages_per_seq, seed, clip_k=None, clip_v=None, ext
     clip_v = np.full(Hkv, 0.9, np.float32) if clip_v is None else np.asarray(clip_v, np.float32)
     max_pages = max(max(pages_per_seq) + extra_pages, 1)
     pt, num_pages = synth.page_tables(seed, [p + extra_pages for p in pages_per_seq], max_pages)
-    O = opool.Pool(B, Hq, Hkv, 128, g, num_pages, max_pages, Rk, Rv, clip_k, clip_v)
+    O = opool.Pool(B, Hq, Hkv, 128, g, num_pages, max_pages, Rk, Rv, clip_k, clip_v, codebook_k=codebook_k,
+                   codebook_v=codebook_v)
     O.page_table[:] = pt
     P = ok.Pool(B, Hq, Hkv, g, num_pages, max_pages, torch.from_numpy(Rk), torch.from_numpy(Rv),
-                torch.from_numpy(clip_k), torch.from_numpy(clip_v))
+                torch.from_numpy(clip_k), torch.from_numpy(clip_v), codebook_k=codebook_k, codebook_v=codebook_v)
     P.set_page_table(pt)
     return O, P
 
