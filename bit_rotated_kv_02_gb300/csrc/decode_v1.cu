@@ -9,8 +9,8 @@
 // Launches:
 //   qrot_kernel   q_rot = q · R_k for every query head (row-vector convention), fp32, and per (sequence,
 //                 KV head) the history consumers' query fragments (MMA B operands, score factors).
-//   attn_kernel   BF16 CTAs (first block indices): 64 sink or recent tokens each, plain FMA, one
-//                 partial per chunk.  History CTAs: the flattened (sequence, KV head, page) space is
+//   attn_kernel   BF16 CTAs (first block indices): 64 sink or recent tokens each, compensated FMA dot
+//                 products, one partial per chunk.  History CTAs: the flattened (sequence, KV head, page) space is
 //                 cut into equal contiguous ranges, one per CTA; a producer warp streams up to four
 //                 pages of one segment per ring stage (codes and scale/zero rows) into shared memory
 //                 with 1-D bulk async copies; four consumer warps each process one whole page per
@@ -21,14 +21,16 @@
 //                 adds the BF16 part and normalises.
 // The decode step (oscar_decode_step) uses the same three launches: the attention kernel reads only what
 // the step leaves unchanged (the history before the step, the window slots other than the new token's,
-// which it takes from k_new / v_new); the merge kernel performs the demotion (overlapping the attention's
-// tail), adds the demoted token, stores the new token and advances the pool counters.
+// which it takes from k_new / v_new); its sink CTAs, idle long before the history CTAs finish, perform
+// the demotion and write the demoted token as a partial of its own; the merge stores the new token and
+// advances the pool counters.
 //
 // Exactness of the tensor-core arithmetic: a 2-bit code c placed in the low mantissa bits of an
 // fp16 with a zero exponent field is the subnormal c * 4^k * 2^-24 (k = its bit position / 2), so
-// codes enter the MMA exactly with one AND per two codes.  q_rot and the softmax weights are split
-// into two fp16 terms (hi + lo, 22 significant bits), pre-scaled by powers of two (including 4^-k)
-// so that fp16 holds them; scale and zero point are applied in fp32 outside the MMA:
+// codes enter the MMA exactly with one AND per two codes.  q_rot is split into two fp16 terms on a
+// fixed-point grid (so that a token's code sums are exact), the softmax weights into two fp16 terms
+// (hi + lo, 22 significant bits), both pre-scaled by powers of two (including 4^-k) so that fp16 holds
+// them; scale and zero point are applied in fp32 outside the MMA:
 //   score = scale * sum_c code_c q_c + zero * sum_c q_c,   o_rot = sum_t p_t scale_t code_t + sum_t p_t zero_t.
 // Softmax values are kept in base 2 (scores pre-multiplied by log2 e), so partials carry log2 maxima.
 #include "oscar_internal.cuh"
@@ -50,15 +52,15 @@ constexpr int WEXP = 14 - LAZY;    // weights p * scale * 2^tau < 2^14 with tau 
 
 struct Args {
   PoolArgs p;
-  const float *qrot;   // [B][Hq][D]
+  const float *qrot;   // [B][Hq][D] (qrot_kernel)
   const uint16_t *q;   // [B][Hq][D] bf16
   float sm_log2;       // softmax_scale * log2(e)
   int n_hist;          // history CTAs (block indices n_bf .. n_bf + n_hist - 1)
   int n_bf;            // BF16 CTAs (block indices 0 .. n_bf - 1)
   float *part;         // partial slots [*][G][PART_STRIDE]
   const uint32_t *frag;  // per (sequence, KV head): the consumers' query fragments (qrot_kernel)
-  // decode-step form: the pool counters still hold the state before the step (its demotion kernel
-  // runs concurrently and leaves them unchanged); the BF16 CTAs attend the window after the step's
+  // decode-step form: the pool counters still hold the state before the step (the merge kernel that
+  // follows performs the demotion and the append); the BF16 CTAs attend the window after the step's
   // append and take the new token from k_new / v_new, the history CTAs the pages before the step.
   int step;
   const uint16_t *k_new, *v_new;  // [B][Hkv][D] bf16
@@ -220,14 +222,19 @@ template <int G>
 __host__ __device__ constexpr int frag_words() { return Smem<G>::NT * 18; }
 
 // ---------------------------------------------------------------------------------------------
-// q_rot = q . R_k for the G query heads of one (sequence, KV head): grid B * Hkv, 512 threads; thread
-// (c, quarter) sums rows 16k .. 16k+15 for k = 2 quarter, 2 quarter + 1 of column c, and the eight
-// partial sums are added as ((p0 + p1) + (p2 + p3)) + ((p4 + p5) + (p6 + p7)) — the order the demotion
-// kernel uses when it rotates the queries in oscar_decode_step, so both paths give the same bits.
-// It also writes the consumers' query fragments (frag_words): per head the exponent sigma with
-// amax(q_rot) * 2^sigma < 2^14, kf = 2^(24 - sigma) * log2(e) * softmax_scale and zf = sum(q_rot) *
-// log2(e) * softmax_scale, and per lane the q_rot values of its B operands, pre-scaled by 2^sigma and by
-// 4^-k for the code placed at bit 2k of its 16-bit lane, split into two fp16 terms.
+// q_rot = q . R_k for the G query heads of one (sequence, KV head) and the history consumers' query
+// fragments (frag_words per lane): grid B * Hkv, 512 threads.  Thread (c, quarter) sums rows 16k ..
+// 16k+15 for k = 2 quarter, 2 quarter + 1 of column c; the eight partial sums are added pairwise.  Per
+// head the exponent sigma with amax(q_rot) * 2^sigma < 2^14, kf = 2^(24 - sigma) * log2(e) *
+// softmax_scale and zf = sum(q_rot) * log2(e) * softmax_scale, and per lane the q_rot values of its B
+// operands: y = q_rot * 2^sigma split on a fixed-point grid, hi = 8 rint(y / 8) and lo = rint((y - hi) *
+// 256) / 256 (so |y - hi - lo| <= 2^-9 < 2^-23 amax(y)), each scaled by 4^-k for the code placed at bit
+// 2k of its 16-bit lane.  Every product of a code with hi is an integer multiple of 2^-21 and every
+// product with lo a multiple of 2^-32, and 128 of them stay below 2^24 units: the tensor cores' float32
+// sums of a token's code products are exact, whatever their order.
+// The loads of q and R_k (inputs no kernel of the step writes) are issued before the griddepcontrol.wait;
+// the trigger follows the wait, so that the attention kernel, which reads the pool counters at once,
+// starts only after the previous step's merge has completed.
 template <int G>
 __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot, uint32_t *frag,
                                                    float sm_log2) {
@@ -236,15 +243,26 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
   __shared__ float part[8][G][D];
   __shared__ int s_sig[8];
   __shared__ float s_kf[8], s_zf[8];
-  pdl_wait();
-  pdl_trigger();
   const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
   const int tid = threadIdx.x, c = tid & (D - 1), qt = tid >> 7;
-  for (int i = tid; i < G * D; i += 512) qs[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + kvh * G) * D + i]);
   const float *R = p.R_k + (size_t)kvh * D * D + (size_t)(32 * qt) * D + c;
   float r[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) r[i] = R[(size_t)i * D];
+  constexpr int QPT = (G * D + 511) / 512;
+  uint16_t qv[QPT];
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = tid + 512 * k;
+    qv[k] = i < G * D ? q[((size_t)b * p.Hq + kvh * G) * D + i] : 0;
+  }
+  pdl_wait();  // the previous kernel on the stream (the last reader of q_rot and the fragments) has completed
+  pdl_trigger();
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = tid + 512 * k;
+    if (i < G * D) qs[i / D][i % D] = bf16_to_f32(qv[k]);
+  }
   __syncthreads();
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
@@ -304,14 +322,15 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
         const int i = 2 * j + hb;  // register index of the token's 16 (word i/8, slot i%8)
         const int wi = i >> 3, k = i & 7;
         const int ch_lo = 32 * t + 16 * wi + k, ch_hi = ch_lo + 8;
-        const float f = code_factor_inv(k) * s2;
+        const float f = code_factor_inv(k);
         float v[2];
         const int chs[2] = {ch_lo, ch_hi};
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float x = live ? qs[min(h, G - 1)][chs[e]] * f : 0.f;
-          const float hi = __half2float(__float2half_rn(x));
-          v[e] = split == 0 ? hi : x - hi;
+          const float y = live ? qs[min(h, G - 1)][chs[e]] * s2 : 0.f;  // exact: s2 is a power of two
+          const float hi = 8.f * rintf(y * 0.125f);
+          const float lo = rintf((y - hi) * 256.f) * (1.f / 256.f);
+          v[e] = (split == 0 ? hi : lo) * f;
         }
         fr[(nt * 16 + i) * 32] = pack_half2(v[0], v[1]);
       }
@@ -319,6 +338,126 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
     const int hc = min(4 * nt + t, G - 1);  // accumulator column pair (2t, 2t+1) = head 4 nt + t
     fr[(NT * 16 + nt) * 32] = __float_as_uint(s_kf[hc]);
     fr[(NT * 16 + NT + nt) * 32] = __float_as_uint(s_zf[hc]);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode-step demotion, run by the sink CTA of each (sequence, KV head) once its BF16 chunk is done (the
+// history CTAs take far longer): the window's oldest K and V vectors (slot recent_start, unchanged
+// until the merge) are rotated, clipped and quantized exactly as the demotion kernel does, their codes,
+// scale and zero are stored into history row hist_len (which no consumer of this step reads), and the
+// demoted token becomes one more rotated-space partial of every query head of the group: m = its score
+// q_rot . (zero + scale * codes) * log2(e) * softmax_scale (a compensated sum), l = 1, o = its
+// dequantized V.  Without a demotion the slot holds an empty partial.  Warps 0-1 rotate K, warps 2-3 V,
+// each 64 rows of R in four batches of 16 (any summation order: quantize_from_dots bounds it); the
+// scratch lives in the page ring, which BF16 CTAs do not use.
+template <int G>
+__device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int kvh, int seg, const StepState &st) {
+  const PoolArgs &p = a.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float *dslot = a.part + ((size_t)a.n_hist + (size_t)p.B * p.Hkv * 6 + seg) * G * PART_STRIDE;
+  if (!st.demote) {
+    for (int i = tid; i < G * PART_STRIDE; i += 128) dslot[i] = (i % PART_STRIDE) == D ? -INFINITY : 0.f;
+    return;
+  }
+  float *xs = reinterpret_cast<float *>(sm.ring[0]);   // [2][D]: the K and V vectors
+  float *pacc = xs + 2 * D;                            // [4 warps][32 lanes][4]
+  float *psab = pacc + 4 * 32 * 4;
+  uint8_t *dcode = reinterpret_cast<uint8_t *>(psab + 4 * 32 * 4);  // [2][D / 4]
+  uint16_t *dsz = reinterpret_cast<uint16_t *>(dcode + 2 * (D / 4));  // scale K, scale V, zero K, zero V
+  const int kv = warp >> 1, w2 = warp & 1;
+  const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
+  if (w2 == 0) {
+    const uint2 xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
+                                                     (((size_t)b * p.Hkv + kvh) * RECENT + st.rs) * D)[lane];
+    float *dst = xs + kv * D + 4 * lane;
+    dst[0] = bf16_to_f32(xw.x & 0xffffu);
+    dst[1] = bf16_to_f32(xw.x >> 16);
+    dst[2] = bf16_to_f32(xw.y & 0xffffu);
+    dst[3] = bf16_to_f32(xw.y >> 16);
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int bt = 0; bt < 4; ++bt) {
+    const int r0 = 64 * w2 + 16 * bt;
+    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)r0 * (D / 4) + lane;
+    float4 rrow[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) rrow[i] = R4[i * (D / 4)];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float xi = xs[kv * D + r0 + i], ax = fabsf(xi);
+      acc[0] = fmaf(xi, rrow[i].x, acc[0]);
+      acc[1] = fmaf(xi, rrow[i].y, acc[1]);
+      acc[2] = fmaf(xi, rrow[i].z, acc[2]);
+      acc[3] = fmaf(xi, rrow[i].w, acc[3]);
+      sab[0] = fmaf(ax, fabsf(rrow[i].x), sab[0]);
+      sab[1] = fmaf(ax, fabsf(rrow[i].y), sab[1]);
+      sab[2] = fmaf(ax, fabsf(rrow[i].z), sab[2]);
+      sab[3] = fmaf(ax, fabsf(rrow[i].w), sab[3]);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) { pacc[(warp * 32 + lane) * 4 + k] = acc[k]; psab[(warp * 32 + lane) * 4 + k] = sab[k]; }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  if (w2 == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc[k] = pacc[(warp * 32 + lane) * 4 + k] + pacc[((warp + 1) * 32 + lane) * 4 + k];
+      sab[k] = psab[(warp * 32 + lane) * 4 + k] + psab[((warp + 1) * 32 + lane) * 4 + k];
+    }
+    QuantStats qst{0, 0, 0};
+    quantize_from_dots(xs + kv * D, Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g,
+                       dcode + kv * (D / 4), dsz + kv, dsz + 2 + kv, qst);  // codebook pools: CUDA-core path
+  }
+  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  if (tid < 2 * (D / 4)) {  // the demoted K and V codes, scale and zero into history row hist_len
+    const int kv2 = tid / (D / 4), byte = tid % (D / 4);
+    const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
+                       st.hl % PAGE;
+    (kv2 == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + byte] = dcode[kv2 * (D / 4) + byte];
+    if (byte == 0) {
+      (kv2 == 0 ? p.scale_k : p.scale_v)[row] = dsz[kv2];
+      (kv2 == 0 ? p.zero_k : p.zero_v)[row] = dsz[2 + kv2];
+    }
+  }
+  const float sk = bf16_to_f32(dsz[0]), zk = bf16_to_f32(dsz[2]);
+  const float sv = bf16_to_f32(dsz[1]), zv = bf16_to_f32(dsz[3]);
+  for (int i = tid; i < G * D; i += 128) {  // o: the dequantized rotated V, the same for every head
+    const int c = i % D;
+    dslot[(i / D) * PART_STRIDE + c] = fmaf((float)((dcode[D / 4 + c / 4] >> (2 * (c & 3))) & 3u), sv, zv);
+  }
+  pdl_wait();  // the query rotation has completed: its q_rot is read
+  const uint32_t cb = dcode[lane];  // K codes of channels 4 lane .. 4 lane + 3
+  for (int h = warp; h < G; h += 4) {
+    const float4 q4 = reinterpret_cast<const float4 *>(a.qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
+    const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
+    float dc = 0.f, dce = 0.f, sq = 0.f;  // sum of q_rot * code with its rounding errors
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float cf = (float)((cb >> (2 * k)) & 3u);
+      const float pr = qr[k] * cf, pe = fmaf(qr[k], cf, -pr);
+      float t, e2;
+      two_sum_f32(dc, pr, t, e2);
+      dc = t;
+      dce += e2 + pe;
+      sq += qr[k];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float d2 = __shfl_xor_sync(FULL, dc, o);
+      dce += __shfl_xor_sync(FULL, dce, o);
+      float t, e2;
+      two_sum_f32(dc, d2, t, e2);
+      dc = t;
+      dce += e2;
+      sq += __shfl_xor_sync(FULL, sq, o);
+    }
+    if (lane == 0) {
+      dslot[h * PART_STRIDE + D] = a.sm_log2 * fmaf(sk, dc + dce, zk * sq);
+      dslot[h * PART_STRIDE + D + 1] = 1.f;
+    }
   }
 }
 
@@ -335,8 +474,9 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
   if (warp >= CONSUMER_WARPS) return;
   int slen, rs, rl;
   int new_at = -1;  // step form: the chunk-local index of the new token (read from k_new / v_new)
+  StepState st{};
   if (a.step) {
-    const StepState st = step_state(p, b);
+    st = step_state(p, b);
     slen = st.nslen; rs = st.nrs; rl = st.nrl;
     if (st.append) {
       if (st.to_sink) new_at = chunk == 0 ? st.slen : -1;
@@ -361,9 +501,12 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
   // QK: lane -> token (lane & 15) of this warp's 16, channel half (lane >> 4)
   const int tk = 16 * warp + (lane & 15), hf = lane >> 4;
   const bool valid = tk < n;
-  float dot[G];
+  // the products of two bf16 values are exact in float32; their sum carries its rounding errors
+  // (TwoSum), so that the score is the exact dot product rounded about once: logits of several
+  // hundred with two tokens sharing the weight need that accuracy
+  float dot[G], cmp[G];
 #pragma unroll
-  for (int h = 0; h < G; ++h) dot[h] = 0.f;
+  for (int h = 0; h < G; ++h) dot[h] = cmp[h] = 0.f;
   if (valid) {
     const uint4 *kr = reinterpret_cast<const uint4 *>(krow(tk) + hf * 64);
     uint4 w[8];
@@ -377,14 +520,25 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
         const float kv = bf16_to_f32((ws[e >> 1] >> (16 * (e & 1))) & 0xffffu);
         const int c = hf * 64 + 8 * i + e;
 #pragma unroll
-        for (int h = 0; h < G; ++h) dot[h] = fmaf(kv, sm.qr[h][c], dot[h]);
+        for (int h = 0; h < G; ++h) {
+          const float pr = kv * sm.qr[h][c];
+          float t, e2;
+          two_sum_f32(dot[h], pr, t, e2);
+          dot[h] = t;
+          cmp[h] += e2;
+        }
       }
     }
   }
   float m2[G], l[G], o[G][4];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    dot[h] += __shfl_xor_sync(FULL, dot[h], 16);
+    {
+      const float d2 = __shfl_xor_sync(FULL, dot[h], 16), c2 = __shfl_xor_sync(FULL, cmp[h], 16);
+      float t, e2;
+      two_sum_f32(dot[h], d2, t, e2);
+      dot[h] = t + ((cmp[h] + c2) + e2);
+    }
     const float s2 = valid ? dot[h] * a.sm_log2 : -INFINITY;
     float mx = s2;
 #pragma unroll
@@ -440,6 +594,7 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
     slot[h * PART_STRIDE + tid] = O;
     if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
   }
+  if (a.step && chunk == 0) demote_role<G>(a, sm, b, kvh, seg, st);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -839,108 +994,70 @@ template <int G>
 __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
-  // Step form: nothing this kernel reads is written by the step's demotion kernel (pool counters, page
-  // tables, history pages before the step, the window slots the BF16 CTAs read, q and R_k), so it runs
-  // alongside it; every thread waits for it before the grid may complete, so that the merge that
-  // follows sees the demoted token and q_rot.
+  // Step form: nothing this kernel reads is written by the query rotation that precedes it except the
+  // fragments, which the history consumers load after their wait; the rest (pool counters, page tables,
+  // history pages, the window slots the BF16 CTAs read, q) is unchanged until the merge that follows.
   if (!a.step) pdl_wait();
   pdl_trigger();
   if ((int)blockIdx.x < a.n_bf) bf16_role<G>(a, sm);
   else hist_role<G>(a, sm, (int)blockIdx.x - a.n_bf);
+  // every thread has waited for the query rotation before the grid completes: the merge's wait (and the
+  // next step's query rotation, which overwrites the fragments) then follows it as well
+  if (a.step) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------------------------
 // Merge: grid (G, Hkv, B), 512 threads; one CTA per (query head of the group, KV head, sequence).
-// The history partials of a segment sit in consecutive slots (CTA index + segment index).  Latency
-// bound, so the global reads are issued in few dependent rounds: the pool counters (to locate the
-// segment's partials), then every partial's (m, l) together with up to OV output values per thread and
-// the R_v rows of the un-rotation; the softmax weights are applied once the maximum is known.  The
-// un-rotation o[c] = sum_j o_rot[j] R_v[c][j] gives each warp 8 outputs c, its lanes splitting j, so
-// that each R_v row is read as one contiguous 512-byte run.
+// The history partials of a segment sit in consecutive slots (CTA index + segment index), the demoted
+// token's partial (decode step) and the five BF16 partials in slots of their own.  Latency bound:
+// everything that does not depend on the attention kernel's partials is done before the
+// griddepcontrol.wait (the partials' location from the pool counters, R_v staged in shared memory), so
+// that after it only the partials are read, by bulk async copies into shared memory (one round trip per
+// PMAX slots), and combined by short loops: the code run after the wait is small, since each CTA runs
+// it once on an SM whose instruction cache holds the attention kernel.  The un-rotation
+// o[c] = sum_j o_rot[j] R_v[c][j] gives thread (slice sl, channel c) the 32 terms j = 32 sl .. 32 sl + 31.
+// Decode-step form (k_new != NULL): the pool counters still hold the state before the step (every kernel
+// of the step read them).  After the wait the CTA of query head 0 stores the new token of its KV head
+// into the sink or the window; the CTA that arrives last on pool.sync[0] (each CTA arrives once it has
+// read every counter it needs, before its wait) advances every sequence's counters after the wait, so
+// no merge CTA reads a counter that this step has already advanced, however many waves the grid takes.
 constexpr int MT = 512;
-constexpr int MAXPARTS = 1040;
-// Decode-step form (k_new != NULL): the merge also performs the step's demotion and append.  The pool
-// counters still hold the state before the step (the attention kernel read them); before its
-// griddepcontrol.wait the CTA rotates, clips and quantizes the window's oldest K and V vectors of its
-// KV head (when the window is full) — all inputs of that are state the step's earlier kernels leave
-// unchanged, so the work overlaps the attention kernel's tail.  The demoted token then enters the
-// merge as one more partial (m = its score, l = 1, o = its dequantized rotated value).  The CTA of
-// query head 0 stores the demoted codes into the history; the last CTA of a sequence to finish (arrival
-// counter pool.sync[b]; every CTA has read the window by then) stores the new token into the sink or
-// the window and advances the counters.  Warps 0-7 rotate the K vector, warps 8-15 the V vector, each
-// warp 16 rows of R held in registers, as the demotion kernel does.
+constexpr int RV_LD = D + 4;  // padded row stride of the shared copy of R_v
+constexpr int PMAX = 96;      // partial slots staged in shared memory per round
+constexpr uint32_t PART_BYTES = PART_STRIDE * sizeof(float);
+constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX * PART_BYTES + 16;
 template <int G>
 __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
-                                                   const float *qrot, float sm_log2, const uint16_t *k_new,
-                                                   const uint16_t *v_new) {
-  constexpr int OV = 36;  // partials per slice issued at once (4 slices: 144 partials)
-  constexpr int DW = 8, DR = D / DW;  // demotion: 8 warps per vector, 16 rows of R each
-  __shared__ float wgt[MAXPARTS], lsum[MAXPARTS];
-  __shared__ float red[MT / 32];
+                                                   const uint16_t *k_new, const uint16_t *v_new) {
+  extern __shared__ float4 rvs4[];  // R_v of this KV head (row stride RV_LD floats), then the staged slots
+  float *pst = reinterpret_cast<float *>(rvs4 + D * (RV_LD / 4));
+  uint64_t *mbar = reinterpret_cast<uint64_t *>(pst + (size_t)PMAX * PART_STRIDE);
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
   __shared__ long long s_pref, s_total;
-  __shared__ float s_md;
-  __shared__ int s_last;
-  __shared__ float xdem[2][D];
-  __shared__ float pacc[2][DW][32][4], psab[2][DW][32][4];
-  __shared__ uint8_t dcodes[2][D / 4];
-  __shared__ uint16_t dscale[2], dzero[2];
+  __shared__ int s_last_all;
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
   const bool step = k_new != nullptr;
-  StepState st{};
-  if (step) {
-    st = step_state(p, b);
-    if (st.demote) {
-      const int kv = warp / DW, w8 = warp % DW;
-      const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
-      float4 rrow[DR];
-      const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(DR * w8) * (D / 4) + lane;
+  if (tid == 0) {
+    mbar_init(mbar, 1);
+    mbar_fence_init();
+  }
+  // R_v rows into shared memory (coalesced 16-byte loads)
+  {
+    const float4 *R4 = reinterpret_cast<const float4 *>(p.R_v + (size_t)kvh * D * D);
+    float4 rv[8];
 #pragma unroll
-      for (int i = 0; i < DR; ++i) rrow[i] = R4[i * (D / 4)];
-      if (w8 == 0) {
-        const uint2 xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
-                                                         (((size_t)b * p.Hkv + kvh) * RECENT + st.rs) * D)[lane];
-        xdem[kv][4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
-        xdem[kv][4 * lane + 1] = bf16_to_f32(xw.x >> 16);
-        xdem[kv][4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
-        xdem[kv][4 * lane + 3] = bf16_to_f32(xw.y >> 16);
-      }
-      __syncthreads();
-      float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < 8; ++k) rv[k] = R4[tid + MT * k];
 #pragma unroll
-      for (int i = 0; i < DR; ++i) {
-        const float xi = xdem[kv][DR * w8 + i], ax = fabsf(xi);
-        acc[0] = fmaf(xi, rrow[i].x, acc[0]);
-        acc[1] = fmaf(xi, rrow[i].y, acc[1]);
-        acc[2] = fmaf(xi, rrow[i].z, acc[2]);
-        acc[3] = fmaf(xi, rrow[i].w, acc[3]);
-        sab[0] = fmaf(ax, fabsf(rrow[i].x), sab[0]);
-        sab[1] = fmaf(ax, fabsf(rrow[i].y), sab[1]);
-        sab[2] = fmaf(ax, fabsf(rrow[i].z), sab[2]);
-        sab[3] = fmaf(ax, fabsf(rrow[i].w), sab[3]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { pacc[kv][w8][lane][k] = acc[k]; psab[kv][w8][lane][k] = sab[k]; }
-      __syncthreads();
-      if (w8 == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float a8 = 0.f, s8 = 0.f;
-#pragma unroll
-          for (int w = 0; w < DW; ++w) { a8 += pacc[kv][w][lane][k]; s8 += psab[kv][w][lane][k]; }
-          acc[k] = a8;
-          sab[k] = s8;
-        }
-        QuantStats qst{0, 0, 0};
-        quantize_from_dots(xdem[kv], Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcodes[kv],
-                           &dscale[kv], &dzero[kv], qst);  // the step's merge serves uniform pools only
-      }
+    for (int k = 0; k < 8; ++k) {
+      const int i = tid + MT * k;
+      rvs4[(i / (D / 4)) * (RV_LD / 4) + i % (D / 4)] = rv[k];
     }
   }
-  // Everything up to here and the partials' location and the R_v rows below read only state that the
-  // attention kernel does not write (pool counters, R_v), so they overlap its tail.
+  StepState st{};
+  if (step) st = step_state(p, b);
+  // the partials' location (pool counters, unchanged until the grid's last arrival advances them)
   if (warp == 0) {
     long long total;
     int bb, kk, ll;
@@ -955,8 +1072,12 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
     }
     if (lane == 0) { s_pref = run; s_total = total; }
   }
-  __syncthreads();
   const int np = npages_of(p, b);
+  __syncthreads();  // every counter read of this CTA is done
+  if (step && tid == 0) {
+    __threadfence();
+    s_last_all = atomicAdd(p.sync, 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1;
+  }
   int nh = 0, i0 = 0;
   if (np > 0) {
     const long long chunk = (s_total + n_hist - 1) / n_hist;
@@ -964,103 +1085,69 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
     i0 = (int)(start / chunk);
     nh = (int)((end - 1) / chunk) - i0 + 1;
   }
-  const int nparts = nh + 5;
+  const int nrot = nh + (step ? 1 : 0);  // rotated-space partials: history (+ the demoted token)
+  const int nparts = nrot + 5;
   const size_t stride = (size_t)G * PART_STRIDE;
   const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
+  const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride + (size_t)h * PART_STRIDE;
   const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
-  auto slot = [&](int i) { return i < nh ? hp + (size_t)i * stride : bp + (size_t)(i - nh) * stride; };
-  // R_v rows c = warp + 16 k (k < 8), lane's four columns 4 lane .. 4 lane + 3
-  constexpr int UW = MT / 32, UPW = D / UW;
-  float4 rv[UPW];
-#pragma unroll
-  for (int k = 0; k < UPW; ++k)
-    rv[k] = reinterpret_cast<const float4 *>(p.R_v + ((size_t)kvh * D + warp + UW * k) * D)[lane];
+  auto slot = [&](int i) {
+    return i < nh ? hp + (size_t)i * stride : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
+  };
+  __syncthreads();  // s_last_all
+  // the grid's last arrival: every sequence's counters after the step (the first MT are read here, while
+  // no CTA reads them any more, and kept in registers for the stores after the wait)
+  const bool last_all = step && s_last_all;
+  StepState sa{};
+  if (last_all && tid < p.B) sa = step_state(p, tid);
   pdl_wait();
   pdl_trigger();
-  float od = 0.f;  // step form: the demoted token's dequantized rotated value at channel ch
-  if (step) {
-    __syncthreads();  // the demoted codes are in shared memory
-    if (st.demote) {
-      if (warp == 0) {
-        const float4 q4 = reinterpret_cast<const float4 *>(qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
-        const uint32_t cb = dcodes[0][lane];  // channels 4 lane .. 4 lane + 3
-        float dc = q4.x * (float)(cb & 3u) + q4.y * (float)((cb >> 2) & 3u) + q4.z * (float)((cb >> 4) & 3u) +
-                   q4.w * (float)((cb >> 6) & 3u);
-        float sq = (q4.x + q4.y) + (q4.z + q4.w);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          dc += __shfl_xor_sync(FULL, dc, o);
-          sq += __shfl_xor_sync(FULL, sq, o);
-        }
-        if (lane == 0) s_md = sm_log2 * fmaf(bf16_to_f32(dscale[0]), dc, bf16_to_f32(dzero[0]) * sq);
-      }
-      const uint32_t cv = (dcodes[1][ch / 4] >> (2 * (ch & 3))) & 3u;
-      od = fmaf((float)cv, bf16_to_f32(dscale[1]), bf16_to_f32(dzero[1]));
-      if (h == 0 && tid < 2 * (D / 4)) {  // store the demoted K and V codes, scale and zero in the history
-        const int kv = tid / (D / 4), byte = tid % (D / 4);
-        const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
-                           st.hl % PAGE;
-        (kv == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + byte] = dcodes[kv][byte];
-        if (byte == 0) {
-          (kv == 0 ? p.scale_k : p.scale_v)[row] = dscale[kv];
-          (kv == 0 ? p.zero_k : p.zero_v)[row] = dzero[kv];
-        }
-      }
-    } else if (tid == 0) {
-      s_md = -INFINITY;
+  // The partial slots are staged in shared memory by bulk async copies, PMAX per round (one round trip
+  // each, no registers), and combined with a running maximum across rounds; every warp forms the round's
+  // maximum and weight sum itself, the same way in every warp.
+  float M = -INFINITY, L = 0.f, acc = 0.f, accb = 0.f;
+  uint32_t phase = 0;
+  for (int r0 = 0; r0 < nparts; r0 += PMAX) {
+    const int n = min(PMAX, nparts - r0);
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(mbar, (uint32_t)n * PART_BYTES);
+      __syncwarp();
+      for (int i = lane; i < n; i += 32) bulk_g2s(pst + (size_t)i * PART_STRIDE, slot(r0 + i), PART_BYTES, mbar);
     }
-  }
-  float mx = -INFINITY;
-  for (int i = tid; i < nparts; i += MT) {
-    const float *q = slot(i);
-    const float m = q[D];
-    wgt[i] = m;
-    lsum[i] = q[D + 1];
-    mx = fmaxf(mx, m);
-  }
-  float ov[OV];
+    const bool ok = mbar_wait_bounded(mbar, phase);
+    if (__syncthreads_or(!ok)) {  // a copy did not complete: record it, let the copies drain, give up
+      if (tid == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
+      mbar_wait_bounded(mbar, phase);
+      return;
+    }
+    phase ^= 1;
+    float mr = -INFINITY;
+    for (int i = lane; i < n; i += 32) mr = fmaxf(mr, pst[(size_t)i * PART_STRIDE + D]);
 #pragma unroll
-  for (int k = 0; k < OV; ++k) {
-    const int i = sl + 4 * k;
-    ov[k] = i < nparts ? slot(i)[ch] : 0.f;
-  }
+    for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(FULL, mr, o));
+    const float Mn = fmaxf(M, mr);
+    if (Mn != M && M != -INFINITY) {
+      const float f = exp2f(M - Mn);
+      L *= f;
+      acc *= f;
+      accb *= f;
+    }
+    M = Mn;
+    float lr = 0.f;
+    for (int i = lane; i < n; i += 32) {
+      const float m = pst[(size_t)i * PART_STRIDE + D];
+      if (m != -INFINITY) lr = fmaf(exp2f(m - M), pst[(size_t)i * PART_STRIDE + D + 1], lr);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
-  if (lane == 0) red[warp] = mx;
-  __syncthreads();
-  float M = red[0];
-#pragma unroll
-  for (int w = 1; w < MT / 32; ++w) M = fmaxf(M, red[w]);
-  const float md = step ? s_md : -INFINITY;
-  M = fmaxf(M, md);
-  __syncthreads();
-  float ls = 0.f;
-  for (int i = tid; i < nparts; i += MT) {
-    const float e = (wgt[i] == -INFINITY) ? 0.f : exp2f(wgt[i] - M);
-    wgt[i] = e;
-    ls += e * lsum[i];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
-  if (lane == 0) red[warp] = ls;
-  __syncthreads();
-  float L = 0.f;
-#pragma unroll
-  for (int w = 0; w < MT / 32; ++w) L += red[w];
-  const float ed = md == -INFINITY ? 0.f : exp2f(md - M);
-  L += ed;
-  // weighted sums: history partials (rotated space) and BF16 partials (original space) apart
-  float acc = sl == 0 ? ed * od : 0.f, accb = 0.f;
-#pragma unroll
-  for (int k = 0; k < OV; ++k) {
-    const int i = sl + 4 * k;
-    const float w = i < nparts ? wgt[i] : 0.f;
-    if (i < nh) acc = fmaf(w, ov[k], acc);
-    else accb = fmaf(w, ov[k], accb);
-  }
-  for (int i = sl + 4 * OV; i < nparts; i += 4) {
-    if (i < nh) acc = fmaf(wgt[i], slot(i)[ch], acc);
-    else accb = fmaf(wgt[i], slot(i)[ch], accb);
+    for (int o = 16; o > 0; o >>= 1) lr += __shfl_xor_sync(FULL, lr, o);
+    L += lr;
+    for (int i = sl; i < n; i += 4) {  // rotated-space partials and BF16 partials (original space) apart
+      const float m = pst[(size_t)i * PART_STRIDE + D];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+      if (r0 + i < nrot) acc = fmaf(w, pst[(size_t)i * PART_STRIDE + ch], acc);
+      else accb = fmaf(w, pst[(size_t)i * PART_STRIDE + ch], accb);
+    }
+    __syncthreads();  // the next round overwrites the staged slots
   }
   Osl[sl][ch] = acc;
   Obs[sl][ch] = accb;
@@ -1068,52 +1155,45 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   if (sl == 0) Orot[ch] = ((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch];
   __syncthreads();
   {
-    const float4 o4 = reinterpret_cast<const float4 *>(Orot)[lane];
+    const float4 *o4 = reinterpret_cast<const float4 *>(Orot + 32 * sl);
+    const float4 *r4 = rvs4 + ch * (RV_LD / 4) + 8 * sl;
+    float u0 = 0.f, u1 = 0.f;
 #pragma unroll
-    for (int k = 0; k < UPW; ++k) {
-      float u = fmaf(rv[k].x, o4.x, fmaf(rv[k].y, o4.y, fmaf(rv[k].z, o4.z, rv[k].w * o4.w)));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(FULL, u, o);
-      if (lane == 0) Osl[0][warp + UW * k] = u;  // slot 0 of Osl is free again
+    for (int k = 0; k < 8; ++k) {
+      const float4 o = o4[k], r = r4[k];
+      u0 = fmaf(r.x, o.x, fmaf(r.y, o.y, u0));
+      u1 = fmaf(r.z, o.z, fmaf(r.w, o.w, u1));
     }
+    Osl[sl][ch] = u0 + u1;  // every read of Osl finished before the barrier above
   }
   __syncthreads();
   if (sl == 0) {
-    const float o = Osl[0][ch] + (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
+    const float o = (((Osl[0][ch] + Osl[1][ch]) + Osl[2][ch]) + Osl[3][ch]) +
+                    (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
     out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
   }
   if (!step) return;
-  // every CTA of the sequence has read the counters and the window before it arrives; the last one
-  // stores the new token of every KV head and advances the counters
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    s_last = atomicAdd(p.sync + b, 1) == (int)(gridDim.x * gridDim.y) - 1;
+  if (h == 0 && st.append && tid < 2 * (D / 4)) {  // the new token of KV head kvh (8-byte pieces of K and V)
+    const int kv = tid / (D / 4), j = tid % (D / 4);
+    uint16_t *dst = st.to_sink
+        ? (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kvh) * SINK + st.slen) * D
+        : (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kvh) * RECENT + (st.nrs + st.nrl - 1) % RECENT) * D;
+    reinterpret_cast<uint2 *>(dst)[j] = reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kvh) * D)[j];
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (st.append) {
-    for (int i = tid; i < p.Hkv * 2 * (D / 4); i += MT) {  // 8-byte pieces of the K and V rows
-      const int kh = i / (2 * (D / 4)), kv = (i / (D / 4)) & 1, j = i % (D / 4);
-      uint16_t *dst = st.to_sink
-          ? (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kh) * SINK + st.slen) * D
-          : (kv == 0 ? p.recent_k : p.recent_v) + (((size_t)b * p.Hkv + kh) * RECENT + (st.nrs + st.nrl - 1) % RECENT) * D;
-      reinterpret_cast<uint2 *>(dst)[j] =
-          reinterpret_cast<const uint2 *>((kv == 0 ? k_new : v_new) + ((size_t)b * p.Hkv + kh) * D)[j];
+  if (last_all) {
+    for (int bb = tid; bb < p.B; bb += MT) {
+      const StepState s2 = bb < MT ? sa : step_state(p, bb);
+      if (!s2.ok) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
+      else if (s2.want && !s2.demote)
+        atomicOr(p.err, s2.hl / PAGE >= p.max_pages ? OSCAR_DEVERR_HISTORY_FULL : OSCAR_DEVERR_PAGE_INDEX);
+      if (s2.ok && (s2.demote || s2.append)) {
+        p.sink_len[bb] = s2.nslen;
+        p.hist_len[bb] = s2.nhl;
+        p.recent_start[bb] = s2.nrs;
+        p.recent_len[bb] = s2.nrl;
+      }
     }
-  }
-  if (tid == 0) {
-    if (!st.ok) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
-    else if (st.want && !st.demote)
-      atomicOr(p.err, st.hl / PAGE >= p.max_pages ? OSCAR_DEVERR_HISTORY_FULL : OSCAR_DEVERR_PAGE_INDEX);
-    if (st.ok && (st.demote || st.append)) {
-      p.sink_len[b] = st.nslen;
-      p.hist_len[b] = st.nhl;
-      p.recent_start[b] = st.nrs;
-      p.recent_len[b] = st.nrl;
-    }
-    p.sync[b] = 0;
+    if (tid == 0) p.sync[0] = 0;
   }
 }
 
@@ -1151,7 +1231,7 @@ int v1_hist_ctas(const PoolArgs &p) {
   const int slots = resident_ctas_for(p.Hq / p.Hkv);
   const long long nbf = (long long)p.B * p.Hkv * 5;
   long long n = slots - (nbf < slots / 4 ? nbf : slots / 4);
-  if (n > 1000) n = 1000;  // the merge kernel gathers at most MAXPARTS partials per segment
+  if (n > 1000) n = 1000;
   const long long cap = (long long)p.B * p.Hkv * p.max_pages;
   if (cap < n) n = cap;
   return (int)(n < 1 ? 1 : n);
@@ -1159,13 +1239,13 @@ int v1_hist_ctas(const PoolArgs &p) {
 
 size_t v1_ws_bytes(const PoolArgs &p) {
   const int G = p.Hq / p.Hkv;
-  const size_t slots = (size_t)v1_hist_ctas(p) + (size_t)p.B * p.Hkv * 6;
+  // history slots (CTA index + segment index), 5 BF16 slots and one demoted-token slot per segment
+  const size_t slots = (size_t)v1_hist_ctas(p) + (size_t)p.B * p.Hkv * 7;
   const size_t frag = (size_t)p.B * p.Hkv * (G > 4 ? 36 : 18) * 32 * sizeof(uint32_t);
   return (size_t)p.B * p.Hq * D * sizeof(float) + frag + slots * G * PART_STRIDE * sizeof(float);
 }
 
-// k_new != NULL: the step form (append + demote + query rotation fused in the demote kernel);
-// otherwise the query rotation runs as its own kernel.
+// Workspace: [q_rot][query fragments][partial slots].  k_new != NULL: the decode-step form.
 template <int G>
 static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
                                cudaStream_t s, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr) {
@@ -1178,30 +1258,27 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.part = reinterpret_cast<float *>(frag + (size_t)p.B * p.Hkv * v1::frag_words<G>() * 32);
   a.sm_log2 = sm_scale * 1.4426950408889634f;
   a.n_hist = v1_hist_ctas(p);
-  if (k_new != nullptr) {  // leave the demotion kernel's CTAs their slots (each displaces two of ours)
-    const int r = 4 * p.B * p.Hkv;
-    a.n_hist = a.n_hist - (r < a.n_hist / 4 ? r : a.n_hist / 4);
-  }
   const int nbf = p.B * p.Hkv * 5;
   a.n_bf = nbf;
   const int smem = (int)sizeof(v1::Smem<G>);
   cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  // Step form: the demotion kernel (counters left unchanged), the query rotation and the attention
-  // kernel run alongside one another; the merge adds the demoted token and advances the counters.
   a.step = k_new != nullptr;
   a.k_new = k_new;
   a.v_new = v_new;
   // Step form: the attention reads only state the step leaves unchanged; the merge performs the
   // demotion (overlapping the attention's tail), the append and the counter update.
+  if ((e = cudaFuncSetAttribute(v1::merge_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)v1::MERGE_SMEM)) != cudaSuccess)
+    return e;
   if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2)) !=
       cudaSuccess)
     return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
-  return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), 0, s, p, (const float *)a.part, a.n_hist,
-                    out, (const float *)ws, a.sm_log2, k_new, v_new);
+  return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p,
+                    (const float *)a.part, a.n_hist, out, k_new, v_new);
 }
 
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,

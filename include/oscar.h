@@ -266,9 +266,10 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
  * out, softmax_scale, 0, ws, ws_bytes): the same pool afterwards, byte for byte, and the same
  * attention output up to float32 rounding ("OSCAR 的设计": the new token enters the recent window,
  * the oldest recent token is demoted into the INT2 history, then attention runs over the three
- * segments).  With group size 128 the attention runs over the history before the step and the BF16
- * window after the append, and the merge kernel performs the demotion and the append and adds the
- * demoted token.  Other group sizes run the two calls in turn.
+ * segments).  With group size 128 and the uniform levels the attention runs over the history before
+ * the step and the BF16 window after the append; the attention kernel's sink CTAs perform the demotion
+ * and add the demoted token as a partial, the merge kernel stores the new token and advances the
+ * counters.  Other pools run the two calls in turn.
  *   k_new, v_new   bf16 [batch][Hkv][d] (16-byte aligned); q bf16 [batch][Hq][d] (16-byte aligned)
  *   ws, ws_bytes   at least oscar_decode_workspace_size(pool, 0) bytes
  * Errors as for the two calls; all checks run before any launch.

@@ -129,3 +129,24 @@ def test_100k_context_sampled_heads():
     qh = [h for kv in heads for h in range(kv * wl.group, (kv + 1) * wl.group)]
     ref = O.decode(q, heads=qh)
     helpers.assert_attention_close(out[:, qh], ref[:, qh])
+
+
+def test_decode_step_with_a_merge_grid_of_several_waves():
+    """Qwen3-8B head shapes (32 query / 8 KV heads) with 8 sequences: the merge grid (4 x 8 x 8 CTAs of
+    512 threads) takes more than one wave, and the histories cross page boundaries at different steps,
+    so a late merge CTA must locate its partials from the counters before the step."""
+    seed, Hkv, Hq = 700, 8, 32
+    lens = [330 + 9 * b for b in range(8)]
+    O, P, _ = _setup(lens, Hq, Hkv, 128, seed, extra_pages=2)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for t in range(70):
+        kn = synth.outlier_kv(seed + 2000 + t, len(lens), Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, len(lens), Hkv, 128, ch)
+        qt = synth.outlier_q(seed + 4000 + t, len(lens), Hq, Hkv, 128, ch)
+        O.append(kn, vn)
+        out = ok.oscar_decode_step(P, helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn), helpers.to_dev_bf16(qt))
+        if t % 10 == 9:
+            helpers.assert_attention_close(out.cpu().numpy(), O.decode(qt))
+    torch.cuda.synchronize()
+    helpers.assert_pools_equal(O, P)
+    assert P.err() == 0 and int(P.sync.abs().sum()) == 0
