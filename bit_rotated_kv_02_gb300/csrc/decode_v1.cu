@@ -881,13 +881,16 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
 
   if (warp == CONSUMER_WARPS) {
     // ---------------- producer warp: up to STAGE_PAGES pages of one segment per stage ----------------
-    // Lane i owns page i of a stage: the page-table entries of a stage are read in one round trip and
-    // each lane issues its own page's bulk copies.  hist_len is read once per sequence.
+    // Lane i owns page i of a stage and issues its bulk copies.  The page-table entries are read 32 at a
+    // time (lane i holds entry pt_base + i of sequence b; every KV head of a sequence shares them), so
+    // that most stages issue their copies without a round trip of their own.  hist_len is read once per
+    // sequence.
     int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
     int np = sm.np0, hl = sm.hl0;
     int stage = 0, it = 0;
     uint32_t phase = 0;
     long long done = 0;
+    int pt_base = -1, pt_b = -1, ptv = -1;
     while (done < n) {
       bool abort = false;
       if (it >= NSTAGE) {  // every page slot of the stage released by its consumer warp
@@ -898,10 +901,15 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
       }
       const int seg = b * p.Hkv + kvh;
       const int cnt = abort ? 0 : (int)min((long long)STAGE_PAGES, min(n - done, (long long)(np - local)));
-      int pp = -1, ntk = 0;
+      if (cnt > 0 && (b != pt_b || local < pt_base || local + cnt > pt_base + 32)) {
+        pt_b = b;
+        pt_base = local;
+        ptv = local + lane < np ? p.page_table[(size_t)b * p.max_pages + local + lane] : -1;
+      }
+      int pp = __shfl_sync(FULL, ptv, (local - pt_base + lane) & 31), ntk = 0;
+      if (lane >= cnt) pp = -1;
       if (lane < cnt) {
         const int lp = local + lane;
-        pp = p.page_table[(size_t)b * p.max_pages + lp];
         ntk = min(PAGE, hl - lp * PAGE);
         if (pp < 0 || pp >= p.num_pages) {
           atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
