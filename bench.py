@@ -782,11 +782,11 @@ def main():
                          "timed_launches": len(hist_ms), "sampling": f"every {EVERY}th step of the timed region"},
             "demote": {"tokens_per_s": 1.0 / (dem_ms * 1e-3), "mean_call_us": dem_ms * 1e3,
                        "note": "oscar_append_kv (demotion + append kernel), timed on its own after the run; in "
-                               "the decode step the merge kernel performs the demotion"},
+                               "the decode step the attention kernel's sink CTAs perform the demotion"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 3,   # q rotation, attention, merge (+ demotion and append)
+            "gpu_launches": args.steps * 3,   # q rotation, attention (+ demotion), merge (+ append)
             "clocks": clk,
             "cpu_baseline": cpu,
         }
