@@ -442,7 +442,7 @@ def codebook_compare(args, peak):
                       "workload": WORKLOAD + (", Lloyd-Max codebooks" if name == "lloyd_max" else ", uniform INT2"),
                       "value": L_CTX / (ms * 1e-3), "unit": "KV tokens/s", "ms_per_step": ms, "steps": steps,
                       "step_gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak,
-                      "decode_path": "tensor-core INT2" if name == "uniform" else "CUDA-core codebook levels",
+                      "decode_path": "tensor-core INT2" if name == "uniform" else "tensor-core, three indicator planes",
                       "setup_s_incl_calibration": calib_s})
         del ws
     return lines

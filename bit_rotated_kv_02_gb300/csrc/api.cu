@@ -309,11 +309,9 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
   return cuda_status(launch_demote(a, nullptr, 2, k_new, v_new, static_cast<cudaStream_t>(stream)), "append_kv");
 }
 
-// Whole-vector groups with the uniform levels decode on the tensor-core path (codes as exact small
-// integers in the MMA); other group sizes and codebook pools on the CUDA-core path.
-static bool tensor_core_path(const PoolArgs &a) {
-  return a.g == OSCAR_HEAD_DIM && a.cb_k == nullptr && a.cb_v == nullptr;
-}
+// Whole-vector groups decode on the tensor-core path (codes, or a codebook's indicator planes, as exact
+// small integers in the MMA); other group sizes on the CUDA-core path.
+static bool tensor_core_path(const PoolArgs &a) { return a.g == OSCAR_HEAD_DIM; }
 
 oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_splits, size_t *bytes) {
   PoolArgs a;

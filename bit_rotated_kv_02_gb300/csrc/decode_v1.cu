@@ -116,6 +116,11 @@ __device__ __forceinline__ void unpack16(uint32_t x, uint32_t (&r)[16], int base
 #pragma unroll
   for (int k = 0; k < 3; ++k) r[base + 5 + k] = xs & (0x00030003u << (2 * k));
 }
+// Indicator plane [c >= i] (i = 1, 2, 3) of the 2-bit fields of w, in each field's low bit: a code
+// c = [c >= 1] + [c >= 2] + [c >= 3], and each plane unpacks like a code (an exact subnormal 0 or 4^k).
+__device__ __forceinline__ uint32_t plane_ge(uint32_t w, int i) {
+  return i == 1 ? (w | (w >> 1)) & 0x55555555u : i == 2 ? (w >> 1) & 0x55555555u : (w & (w >> 1)) & 0x55555555u;
+}
 __device__ __forceinline__ float code_factor_inv(int k) {  // 1 / 4^k' for register k (0..7)
   const int e = (k <= 4) ? 2 * k : 2 * (k - 5);
   return __int_as_float((127 - e) << 23);
@@ -408,8 +413,9 @@ __device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int 
       sab[k] = psab[(warp * 32 + lane) * 4 + k] + psab[((warp + 1) * 32 + lane) * 4 + k];
     }
     QuantStats qst{0, 0, 0};
+    const float *cb = kv == 0 ? p.cb_k : p.cb_v;
     quantize_from_dots(xs + kv * D, Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g,
-                       dcode + kv * (D / 4), dsz + kv, dsz + 2 + kv, qst);  // codebook pools: CUDA-core path
+                       dcode + kv * (D / 4), dsz + kv, dsz + 2 + kv, qst, cb != nullptr ? cb + 4 * kvh : nullptr);
   }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
   if (tid < 2 * (D / 4)) {  // the demoted K and V codes, scale and zero into history row hist_len
@@ -424,9 +430,11 @@ __device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int 
   }
   const float sk = bf16_to_f32(dsz[0]), zk = bf16_to_f32(dsz[2]);
   const float sv = bf16_to_f32(dsz[1]), zv = bf16_to_f32(dsz[3]);
+  // dequantization levels (the codes themselves without a codebook)
+  auto level = [&](const float *cb, uint32_t c) { return cb != nullptr ? cb[4 * kvh + c] : (float)c; };
   for (int i = tid; i < G * D; i += 128) {  // o: the dequantized rotated V, the same for every head
     const int c = i % D;
-    dslot[(i / D) * PART_STRIDE + c] = fmaf((float)((dcode[D / 4 + c / 4] >> (2 * (c & 3))) & 3u), sv, zv);
+    dslot[(i / D) * PART_STRIDE + c] = fmaf(level(p.cb_v, (dcode[D / 4 + c / 4] >> (2 * (c & 3))) & 3u), sv, zv);
   }
   pdl_wait();  // the query rotation has completed: its q_rot is read
   const uint32_t cb = dcode[lane];  // K codes of channels 4 lane .. 4 lane + 3
@@ -436,7 +444,7 @@ __device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int 
     float dc = 0.f, dce = 0.f, sq = 0.f;  // sum of q_rot * code with its rounding errors
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float cf = (float)((cb >> (2 * k)) & 3u);
+      const float cf = level(p.cb_k, (cb >> (2 * k)) & 3u);
       const float pr = qr[k] * cf, pe = fmaf(qr[k], cf, -pr);
       float t, e2;
       two_sum_f32(dc, pr, t, e2);
@@ -635,10 +643,23 @@ __device__ __forceinline__ void reset(WarpState<G> &ws) {
 }
 
 // Segment setup (consumer threads only): load q_rot, derive per-head scaling, build B fragments.
-template <int G>
+// Codebook levels of one KV head as the history consumers use them: l[c] = l0 + sum_{i < c} d[i]
+// (pools without a codebook for K or V use 0, 1, 2, 3); dvmax = max d[i] of V bounds the weight range.
+struct Levels {
+  float l0k, dk[3], l0v, dv[3], dvmax;
+};
+
+template <int G, bool CB>
 __device__ __forceinline__ void setup_segment(const Args &a, int b, int kvh, uint32_t (&bq)[Smem<G>::NT][8][2],
-                                              float (&kf)[Smem<G>::NT], float (&zf)[Smem<G>::NT]) {
+                                              float (&kf)[Smem<G>::NT], float (&zf)[Smem<G>::NT], Levels &lv) {
   constexpr int NT = Smem<G>::NT;
+  if (CB) {
+    const float4 ck = a.p.cb_k != nullptr ? reinterpret_cast<const float4 *>(a.p.cb_k)[kvh] : make_float4(0.f, 1.f, 2.f, 3.f);
+    const float4 cv = a.p.cb_v != nullptr ? reinterpret_cast<const float4 *>(a.p.cb_v)[kvh] : make_float4(0.f, 1.f, 2.f, 3.f);
+    lv.l0k = ck.x; lv.dk[0] = ck.y - ck.x; lv.dk[1] = ck.z - ck.y; lv.dk[2] = ck.w - ck.z;
+    lv.l0v = cv.x; lv.dv[0] = cv.y - cv.x; lv.dv[1] = cv.z - cv.y; lv.dv[2] = cv.w - cv.z;
+    lv.dvmax = fmaxf(fmaxf(lv.dv[0], lv.dv[1]), lv.dv[2]);
+  }
   if (a.step) pdl_wait();  // the step's query rotation (the previous kernel on this stream) has completed
   const uint32_t *fr = a.frag + (size_t)(b * a.p.Hkv + kvh) * frag_words<G>() * 32 + (threadIdx.x & 31);
 #pragma unroll
@@ -714,10 +735,13 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
 // movmatrix into the B operand of the P.V products, whose A operand therefore takes, for k-index
 // pairs (2t, 2t+1) and (2t+8, 2t+9) of tile mt, the tokens 16 t + 2 mt (+ 8) and 16 t + 2 mt + 1 (+ 8).
 // Rows past ntok are masked: score -inf, value scale and zero 0 (their codes are finite integers).
-template <int G>
+// CB: codebook levels.  Q.K takes the three indicator planes [c >= i] through the same query fragments
+// (their sums stay exact) and combines them as l0 * sum(q) + sum_i d_k[i] * plane_i; P.V takes the planes
+// against the weights scaled by d_v[i]; the zero points absorb scale * l0.
+template <int G, bool CB>
 __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState<G> &ws,
                                           const uint32_t (&bq)[Smem<G>::NT][8][2], const float (&kf_)[Smem<G>::NT],
-                                          const float (&zf_)[Smem<G>::NT]) {
+                                          const float (&zf_)[Smem<G>::NT], const Levels &lv) {
   constexpr int NT = Smem<G>::NT;
   constexpr bool ALL_LIVE = (G % 4) == 0;
   const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
@@ -730,14 +754,41 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
     for (int nt = 0; nt < NT; ++nt) S[mt][nt][0] = S[mt][nt][1] = S[mt][nt][2] = S[mt][nt][3] = 0.f;
     const uint2 ka = *reinterpret_cast<const uint2 *>(kc + 64 * mt);
     const uint2 kb = *reinterpret_cast<const uint2 *>(kc + 64 * mt + 32);
-    uint32_t T0[16], T1[16];
-    unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
-    unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
+    if (!CB) {
+      uint32_t T0[16], T1[16];
+      unpack16(ka.x, T0, 0); unpack16(ka.y, T0, 8);
+      unpack16(kb.x, T1, 0); unpack16(kb.y, T1, 8);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mma16816(S[mt][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+        for (int j = 0; j < 8; ++j)
+          mma16816(S[mt][nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+    } else {
+      float T[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) T[nt][0] = T[nt][1] = 0.f;
+#pragma unroll
+      for (int i = 1; i <= 3; ++i) {
+        float Si[NT][4];
+        uint32_t T0[16], T1[16];
+        unpack16(plane_ge(ka.x, i), T0, 0); unpack16(plane_ge(ka.y, i), T0, 8);
+        unpack16(plane_ge(kb.x, i), T1, 0); unpack16(plane_ge(kb.y, i), T1, 8);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          Si[nt][0] = Si[nt][1] = Si[nt][2] = Si[nt][3] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            mma16816(Si[nt], T0[2 * j], T1[2 * j], T0[2 * j + 1], T1[2 * j + 1], bq[nt][j][0], bq[nt][j][1]);
+#pragma unroll
+          for (int e = 0; e < 2; ++e) T[nt][e] = fmaf(lv.dk[i - 1], Si[nt][2 * e] + Si[nt][2 * e + 1], T[nt][e]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        S[mt][nt][0] = T[nt][0]; S[mt][nt][1] = 0.f;
+        S[mt][nt][2] = T[nt][1]; S[mt][nt][3] = 0.f;
+      }
+    }
   }
   // ---- scale / zero of the lane's tokens 8g .. 8g+7 ----
   const uint4 ks4 = *reinterpret_cast<const uint4 *>(pb + OFF_KS + 16 * gq);
@@ -757,6 +808,10 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
       vz[2 * i] = __uint_as_float(uw[i] << 16); vz[2 * i + 1] = __uint_as_float(uw[i] & 0xffff0000u);
     }
   }
+  if (CB) {  // zero points that absorb scale * l0
+#pragma unroll
+    for (int j = 0; j < 8; ++j) { kz[j] = fmaf(ks[j], lv.l0k, kz[j]); vz[j] = fmaf(vs[j], lv.l0v, vz[j]); }
+  }
   if (nvalid < 8) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -765,6 +820,7 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
   // ---- weight scaling exponent tau: weights p * vs * 2^tau stay below 2^14 ----
   // (a warp vote on the lane maxima; the cross-lane maximum is formed only when tau must change)
   float vmax = fmaxf(max3f(vs[0], vs[1], vs[2]), max3f(max3f(vs[3], vs[4], vs[5]), vs[6], vs[7]));
+  if (CB) vmax *= lv.dvmax;  // the largest weight factor of the three planes
   if (__any_sync(FULL, vmax >= ws.tau_lim && vmax > 0.f)) {
     vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 4));
     vmax = fmaxf(vmax, __shfl_xor_sync(FULL, vmax, 8));
@@ -786,7 +842,7 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
   }
   const float untau = pow2f(-ws.tau);
   // ---- scores, lazily rescaled online softmax, weights ----
-  uint32_t bw[NT][4][2];
+  uint32_t bw[CB ? 3 : 1][NT][4][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int h = ALL_LIVE ? 4 * nt + t : min(4 * nt + t, G - 1);
@@ -821,22 +877,30 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
     // p * 2^tau = exp2(score - (m - tau)); l and the zero-point sum take p itself
     const float mref = ws.m2[nt] - (float)ws.tau;
     float lsum = 0.f, zsum = 0.f;
-    uint32_t wp[8];
+    float wv[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float pr = fast_exp2(sc[j] - mref);  // 0 for rows past ntok (score -inf)
       lsum += pr;
       zsum = fmaf(pr, vz[j], zsum);
-      const float w = live_h ? pr * vs[j] : 0.f;
-      const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
-      wp[j] = pack_half2(hi, w - hi);                                      // (hi, lo)
+      wv[j] = live_h ? pr * vs[j] : 0.f;
     }
     ws.l[nt] = fmaf(lsum, untau, ws.l[nt]);
     ws.oz[nt] = fmaf(zsum, untau, ws.oz[nt]);
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      bw[nt][mt][0] = movmatrix_trans(wp[2 * mt]);
-      bw[nt][mt][1] = movmatrix_trans(wp[2 * mt + 1]);
+    for (int pl = 0; pl < (CB ? 3 : 1); ++pl) {
+      uint32_t wp[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float w = CB ? wv[j] * lv.dv[pl] : wv[j];
+        const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
+        wp[j] = pack_half2(hi, w - hi);                                      // (hi, lo)
+      }
+#pragma unroll
+      for (int mt = 0; mt < 4; ++mt) {
+        bw[pl][nt][mt][0] = movmatrix_trans(wp[2 * mt]);
+        bw[pl][nt][mt][1] = movmatrix_trans(wp[2 * mt + 1]);
+      }
     }
   }
   // ---- P.V per tile: A = V codes^T (group g: channels 16g .. 16g+15, one 32-bit word per token) ----
@@ -845,18 +909,29 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
   for (int mt = 0; mt < 4; ++mt) {
     const uint32_t xa = vrow[16 * mt], xb = vrow[64 + 16 * mt];           // tokens 16t+2mt, 16t+8+2mt
     const uint32_t xc = vrow[16 * mt + 8], xd = vrow[64 + 16 * mt + 8];   // the same + 1
-    uint32_t VA[16], VB[16];
-    unpack16(prmt(xa, xb, 0x5410), VA, 0); unpack16(prmt(xa, xb, 0x7632), VA, 8);
-    unpack16(prmt(xc, xd, 0x5410), VB, 0); unpack16(prmt(xc, xd, 0x7632), VB, 8);
+    const uint32_t w0 = prmt(xa, xb, 0x5410), w1 = prmt(xa, xb, 0x7632);
+    const uint32_t w2 = prmt(xc, xd, 0x5410), w3 = prmt(xc, xd, 0x7632);
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int pl = 0; pl < (CB ? 3 : 1); ++pl) {
+      uint32_t VA[16], VB[16];
+      if (CB) {
+        unpack16(plane_ge(w0, pl + 1), VA, 0); unpack16(plane_ge(w1, pl + 1), VA, 8);
+        unpack16(plane_ge(w2, pl + 1), VB, 0); unpack16(plane_ge(w3, pl + 1), VB, 8);
+      } else {
+        unpack16(w0, VA, 0); unpack16(w1, VA, 8);
+        unpack16(w2, VB, 0); unpack16(w3, VB, 8);
+      }
 #pragma unroll
-      for (int m8 = 0; m8 < 8; ++m8)
-        mma16816(ws.O[nt][m8], VA[2 * m8], VA[2 * m8 + 1], VB[2 * m8], VB[2 * m8 + 1], bw[nt][mt][0], bw[nt][mt][1]);
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int m8 = 0; m8 < 8; ++m8)
+          mma16816(ws.O[nt][m8], VA[2 * m8], VA[2 * m8 + 1], VB[2 * m8], VB[2 * m8 + 1], bw[pl][nt][mt][0],
+                   bw[pl][nt][mt][1]);
+    }
   }
 }
 
-template <int G>
+template <int G, bool CB>
 __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int cta) {
   constexpr int NT = Smem<G>::NT;
   const PoolArgs &p = a.p;
@@ -972,7 +1047,8 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   // the first segment's query setup needs no pages: it overlaps the first bulk copies
   int cur = sm.b0 * p.Hkv + sm.kvh0, stage = 0;
   ws.csync_par = 0;
-  setup_segment<G>(a, sm.b0, sm.kvh0, bq, kf, zf);
+  Levels lv{};
+  setup_segment<G, CB>(a, sm.b0, sm.kvh0, bq, kf, zf, lv);
   uint32_t phase = 0;
   while (true) {
     if (!mbar_wait_bounded(&sm.full[stage][warp], phase)) {
@@ -985,11 +1061,11 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     if (seg != cur) {
       if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
       cur = seg;
-      setup_segment<G>(a, seg / p.Hkv, seg % p.Hkv, bq, kf, zf);
+      setup_segment<G, CB>(a, seg / p.Hkv, seg % p.Hkv, bq, kf, zf, lv);
     }
     const int ntok = sm.meta_ntok[stage][warp];
     const uint8_t *pb = sm.ring[stage] + warp * PAGE_BYTES;
-    if (ntok > 0) page_pass<G>(pb, ntok, ws, bq, kf, zf);
+    if (ntok > 0) page_pass<G, CB>(pb, ntok, ws, bq, kf, zf, lv);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage][warp]);
     if (flags & 1) break;
@@ -998,7 +1074,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
 }
 
-template <int G>
+template <int G, bool CB>
 __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
@@ -1008,7 +1084,7 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   if (!a.step) pdl_wait();
   pdl_trigger();
   if ((int)blockIdx.x < a.n_bf) bf16_role<G>(a, sm);
-  else hist_role<G>(a, sm, (int)blockIdx.x - a.n_bf);
+  else hist_role<G, CB>(a, sm, (int)blockIdx.x - a.n_bf);
   // every thread has waited for the query rotation before the grid completes: the merge's wait (and the
   // next step's query rotation, which overwrites the fragments) then follows it as well
   if (a.step) pdl_wait();
@@ -1210,15 +1286,15 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
 // ---------------------------------------------------------------------------------------------
 // Grid of the attention kernel: BF16 CTAs (5 per sequence and KV head) first, then history CTAs
 // sized so that both fit in one wave of resident CTAs (history CTAs get at least 3/4 of it).
-template <int G>
+template <int G, bool CB>
 static int resident_ctas() {
   static int cached = 0;
   if (cached == 0) {
     int dev = 0, sms = 148, occ = 1;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int smem = (int)sizeof(v1::Smem<G>);
-    cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v1::attn_kernel<G>, v1::THREADS, smem) != cudaSuccess ||
+    cudaFuncSetAttribute(v1::attn_kernel<G, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v1::attn_kernel<G, CB>, v1::THREADS, smem) != cudaSuccess ||
         occ < 1)
       occ = 1;
     cached = sms * occ;
@@ -1226,17 +1302,21 @@ static int resident_ctas() {
   return cached;
 }
 
+template <bool CB>
 static int resident_ctas_for(int G) {
   switch (G) {
-    case 1: return resident_ctas<1>();
-    case 2: return resident_ctas<2>();
-    case 4: return resident_ctas<4>();
-    default: return resident_ctas<8>();
+    case 1: return resident_ctas<1, CB>();
+    case 2: return resident_ctas<2, CB>();
+    case 4: return resident_ctas<4, CB>();
+    default: return resident_ctas<8, CB>();
   }
 }
 
+// Pools with a codebook for K or V run the codebook form of the attention kernel.
+static bool has_codebook(const PoolArgs &p) { return p.cb_k != nullptr || p.cb_v != nullptr; }
+
 int v1_hist_ctas(const PoolArgs &p) {
-  const int slots = resident_ctas_for(p.Hq / p.Hkv);
+  const int slots = has_codebook(p) ? resident_ctas_for<true>(p.Hq / p.Hkv) : resident_ctas_for<false>(p.Hq / p.Hkv);
   const long long nbf = (long long)p.B * p.Hkv * 5;
   long long n = slots - (nbf < slots / 4 ? nbf : slots / 4);
   if (n > 1000) n = 1000;
@@ -1269,7 +1349,8 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   const int nbf = p.B * p.Hkv * 5;
   a.n_bf = nbf;
   const int smem = (int)sizeof(v1::Smem<G>);
-  cudaError_t e = cudaFuncSetAttribute(v1::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto attn = has_codebook(p) ? v1::attn_kernel<G, true> : v1::attn_kernel<G, false>;
+  cudaError_t e = cudaFuncSetAttribute(attn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   a.step = k_new != nullptr;
   a.k_new = k_new;
@@ -1283,7 +1364,7 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
       cudaSuccess)
     return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
-  if ((e = launch_pdl(v1::attn_kernel<G>, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(attn, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
   return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p,
                     (const float *)a.part, a.n_hist, out, k_new, v_new);

@@ -77,10 +77,11 @@ typedef void *oscar_stream_t;  /* cudaStream_t */
  *                                               levels l0 < l1 < l2 < l3 of a Lloyd-Max codebook in the
  *                                               group's coordinate t = (x_rot - zero) / scale; a code is the
  *                                               nearest level (ties to the even code) and dequantizes to
- *                                               zero + scale * l[code]; 16-byte aligned.  Pools with a
- *                                               codebook decode on the CUDA-core attention path, and
- *                                               oscar_decode_step takes them through oscar_demote +
- *                                               oscar_decode_attention (same results).
+ *                                               zero + scale * l[code]; 16-byte aligned.  With group
+ *                                               size 128 the tensor-core attention takes the codes'
+ *                                               indicator planes [c >= i] (three MMAs where the uniform
+ *                                               levels need one); other group sizes decode on the
+ *                                               CUDA-core path with a 4-entry table.
  *   err                     uint32 [1]          device error word (OSCAR_DEVERR_* bits)
  *   sync                    int32 [batch]       arrival counters; zero them once before the first
  *                                               call, every call leaves them zero again
@@ -266,8 +267,8 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
  * out, softmax_scale, 0, ws, ws_bytes): the same pool afterwards, byte for byte, and the same
  * attention output up to float32 rounding ("OSCAR 的设计": the new token enters the recent window,
  * the oldest recent token is demoted into the INT2 history, then attention runs over the three
- * segments).  With group size 128 and the uniform levels the attention runs over the history before
- * the step and the BF16 window after the append; the attention kernel's sink CTAs perform the demotion
+ * segments).  With group size 128 the attention runs over the history before the step and the BF16
+ * window after the append; the attention kernel's sink CTAs perform the demotion
  * and add the demoted token as a partial, the merge kernel stores the new token and advances the
  * counters.  Other pools run the two calls in turn.
  *   k_new, v_new   bf16 [batch][Hkv][d] (16-byte aligned); q bf16 [batch][Hq][d] (16-byte aligned)
