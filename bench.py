@@ -534,7 +534,7 @@ def other_workload(args):
             L, Hq, Hkv = wl.context[0], wl.num_q_heads, wl.num_kv_heads
             hist = L - SINK - RECENT
             steps = max(3, min(args.steps, 200 if B < 64 else 40))
-            pages = -(-(hist + steps + args.warmup + 8) // PAGE)
+            pages = -(-(hist + 2 * steps + args.warmup + 8) // PAGE)  # the steps, then as many appends timed alone
             chan = torch.from_numpy(synth.outlier_channels(wl.seed, Hkv, D, 4).astype(np.int64)).cuda()
             Rk, Rv = _gpu_rotations(ok, Hkv, D, 100), _gpu_rotations(ok, Hkv, D, 200)
             clip = torch.full((Hkv,), 0.9)
