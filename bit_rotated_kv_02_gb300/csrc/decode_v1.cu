@@ -1096,9 +1096,7 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
 // token's partial (decode step) and the five BF16 partials in slots of their own.  Latency bound:
 // everything that does not depend on the attention kernel's partials is done before the
 // griddepcontrol.wait (the partials' location from the pool counters, R_v staged in shared memory), so
-// that after it only the partials are read, by bulk async copies into shared memory (one round trip per
-// PMAX slots), and combined by short loops: the code run after the wait is small, since each CTA runs
-// it once on an SM whose instruction cache holds the attention kernel.  The un-rotation
+// that after it only the partials are read (one round trip per PMAX slots) and combined.  The un-rotation
 // o[c] = sum_j o_rot[j] R_v[c][j] gives thread (slice sl, channel c) the 32 terms j = 32 sl .. 32 sl + 31.
 // Decode-step form (k_new != NULL): the pool counters still hold the state before the step (every kernel
 // of the step read them).  After the wait the CTA of query head 0 stores the new token of its KV head
@@ -1109,24 +1107,20 @@ constexpr int MT = 512;
 constexpr int RV_LD = D + 4;  // padded row stride of the shared copy of R_v
 constexpr int PMAX = 96;      // partial slots staged in shared memory per round
 constexpr uint32_t PART_BYTES = PART_STRIDE * sizeof(float);
-constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX * PART_BYTES + 16;
+constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX * PART_BYTES;
 template <int G>
 __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
                                                    const uint16_t *k_new, const uint16_t *v_new) {
   extern __shared__ float4 rvs4[];  // R_v of this KV head (row stride RV_LD floats), then the staged slots
   float *pst = reinterpret_cast<float *>(rvs4 + D * (RV_LD / 4));
-  uint64_t *mbar = reinterpret_cast<uint64_t *>(pst + (size_t)PMAX * PART_STRIDE);
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
+  __shared__ float pw[PMAX], s_stat[2];
   __shared__ long long s_pref, s_total;
   __shared__ int s_last_all;
   const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
   const bool step = k_new != nullptr;
-  if (tid == 0) {
-    mbar_init(mbar, 1);
-    mbar_fence_init();
-  }
   // R_v rows into shared memory (coalesced 16-byte loads)
   {
     const float4 *R4 = reinterpret_cast<const float4 *>(p.R_v + (size_t)kvh * D * D);
@@ -1186,50 +1180,57 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   if (last_all && tid < p.B) sa = step_state(p, tid);
   pdl_wait();
   pdl_trigger();
-  // The partial slots are staged in shared memory by bulk async copies, PMAX per round (one round trip
-  // each, no registers), and combined with a running maximum across rounds; every warp forms the round's
-  // maximum and weight sum itself, the same way in every warp.
+  // The partial slots are staged in shared memory, PMAX per round, by 16-byte loads of every thread
+  // (one round trip); warp 0 forms the round's maximum, the weights and their sum once, and the
+  // threads (slice, channel) add the weighted outputs of every fourth slot.  Rounds combine with a
+  // running maximum.
   float M = -INFINITY, L = 0.f, acc = 0.f, accb = 0.f;
-  uint32_t phase = 0;
+  constexpr int V4 = PART_STRIDE / 4;  // float4 per staged slot
   for (int r0 = 0; r0 < nparts; r0 += PMAX) {
     const int n = min(PMAX, nparts - r0);
+    {
+      constexpr int PER = (PMAX * V4 + MT - 1) / MT;
+      float4 v[PER];
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int e = tid + MT * k;
+        if (e < n * V4) v[k] = reinterpret_cast<const float4 *>(slot(r0 + e / V4))[e % V4];
+      }
+#pragma unroll
+      for (int k = 0; k < PER; ++k) {
+        const int e = tid + MT * k;
+        if (e < n * V4) reinterpret_cast<float4 *>(pst)[e] = v[k];
+      }
+    }
+    __syncthreads();
     if (warp == 0) {
-      if (lane == 0) mbar_arrive_expect_tx(mbar, (uint32_t)n * PART_BYTES);
-      __syncwarp();
-      for (int i = lane; i < n; i += 32) bulk_g2s(pst + (size_t)i * PART_STRIDE, slot(r0 + i), PART_BYTES, mbar);
-    }
-    const bool ok = mbar_wait_bounded(mbar, phase);
-    if (__syncthreads_or(!ok)) {  // a copy did not complete: record it, let the copies drain, give up
-      if (tid == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
-      mbar_wait_bounded(mbar, phase);
-      return;
-    }
-    phase ^= 1;
-    float mr = -INFINITY;
-    for (int i = lane; i < n; i += 32) mr = fmaxf(mr, pst[(size_t)i * PART_STRIDE + D]);
+      float mr = -INFINITY;
+      for (int i = lane; i < n; i += 32) mr = fmaxf(mr, pst[(size_t)i * PART_STRIDE + D]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(FULL, mr, o));
-    const float Mn = fmaxf(M, mr);
-    if (Mn != M && M != -INFINITY) {
-      const float f = exp2f(M - Mn);
-      L *= f;
-      acc *= f;
-      accb *= f;
+      for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(FULL, mr, o));
+      const float Mn = fmaxf(M, mr);
+      float lr = 0.f;
+      for (int i = lane; i < n; i += 32) {
+        const float m = pst[(size_t)i * PART_STRIDE + D];
+        const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
+        pw[i] = w;
+        lr = fmaf(w, pst[(size_t)i * PART_STRIDE + D + 1], lr);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lr += __shfl_xor_sync(FULL, lr, o);
+      if (lane == 0) { s_stat[0] = Mn; s_stat[1] = lr; }
     }
+    __syncthreads();
+    const float Mn = s_stat[0];
+    const float f = (M == -INFINITY || Mn == M) ? 1.f : exp2f(M - Mn);  // rescale of the earlier rounds
+    L = fmaf(L, f, s_stat[1]);
+    acc *= f;
+    accb *= f;
     M = Mn;
-    float lr = 0.f;
-    for (int i = lane; i < n; i += 32) {
-      const float m = pst[(size_t)i * PART_STRIDE + D];
-      if (m != -INFINITY) lr = fmaf(exp2f(m - M), pst[(size_t)i * PART_STRIDE + D + 1], lr);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lr += __shfl_xor_sync(FULL, lr, o);
-    L += lr;
     for (int i = sl; i < n; i += 4) {  // rotated-space partials and BF16 partials (original space) apart
-      const float m = pst[(size_t)i * PART_STRIDE + D];
-      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-      if (r0 + i < nrot) acc = fmaf(w, pst[(size_t)i * PART_STRIDE + ch], acc);
-      else accb = fmaf(w, pst[(size_t)i * PART_STRIDE + ch], accb);
+      const float w = pw[i], o = pst[(size_t)i * PART_STRIDE + ch];
+      if (r0 + i < nrot) acc = fmaf(w, o, acc);
+      else accb = fmaf(w, o, accb);
     }
     __syncthreads();  // the next round overwrites the staged slots
   }
