@@ -21,9 +21,9 @@
 //                 adds the BF16 part and normalises.
 // The decode step (oscar_decode_step) uses the same three launches: the attention kernel reads only what
 // the step leaves unchanged (the history before the step, the window slots other than the new token's,
-// which it takes from k_new / v_new); its sink CTAs, idle long before the history CTAs finish, perform
-// the demotion and write the demoted token as a partial of its own; the merge stores the new token and
-// advances the pool counters.
+// which it takes from k_new / v_new); two of its BF16 CTAs per (sequence, KV head), idle long before the
+// history CTAs finish, perform the demotion (K in the sink CTA, V in the first window CTA) and write the
+// demoted token as a partial of its own; the merge stores the new token and advances the pool counters.
 //
 // Exactness of the tensor-core arithmetic: a 2-bit code c placed in the low mantissa bits of an
 // fp16 with a zero exponent field is the subnormal c * 4^k * 2^-24 (k = its bit position / 2), so
@@ -347,52 +347,56 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
 }
 
 // ---------------------------------------------------------------------------------------------
-// Decode-step demotion, run by the sink CTA of each (sequence, KV head) once its BF16 chunk is done (the
-// history CTAs take far longer): the window's oldest K and V vectors (slot recent_start, unchanged
-// until the merge) are rotated, clipped and quantized exactly as the demotion kernel does, their codes,
-// scale and zero are stored into history row hist_len (which no consumer of this step reads), and the
-// demoted token becomes one more rotated-space partial of every query head of the group: m = its score
-// q_rot . (zero + scale * codes) * log2(e) * softmax_scale (a compensated sum), l = 1, o = its
-// dequantized V.  Without a demotion the slot holds an empty partial.  Warps 0-1 rotate K, warps 2-3 V,
-// each 64 rows of R in four batches of 16 (any summation order: quantize_from_dots bounds it); the
-// scratch lives in the page ring, which BF16 CTAs do not use.
+// Decode-step demotion, run by BF16 CTAs once their chunk is done (the history CTAs take far longer):
+// the sink CTA (chunk 0) demotes the window's oldest K vector, the first window CTA (chunk 1) its V
+// vector (slot recent_start, unchanged until the merge).  The vector is rotated, clipped and quantized
+// exactly as the demotion kernel does (four warps, 32 rows of R each in two batches of 16; any summation
+// order: quantize_from_dots bounds it), its codes, scale and zero are stored into history row hist_len
+// (which no consumer of this step reads), and the demoted token becomes one more rotated-space partial of
+// every query head of the group: the K CTA writes m = its score q_rot . (zero + scale * level[code]) *
+// log2(e) * softmax_scale (a compensated sum) and l = 1, the V CTA o = its dequantized V.  Without a
+// demotion the slot holds an empty partial.  The scratch lives in the page ring, which BF16 CTAs do not
+// use.
 template <int G>
-__device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int kvh, int seg, const StepState &st) {
+__device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int kvh, int seg, const StepState &st,
+                                         int kv) {
   const PoolArgs &p = a.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float *dslot = a.part + ((size_t)a.n_hist + (size_t)p.B * p.Hkv * 6 + seg) * G * PART_STRIDE;
   if (!st.demote) {
-    for (int i = tid; i < G * PART_STRIDE; i += 128) dslot[i] = (i % PART_STRIDE) == D ? -INFINITY : 0.f;
+    for (int i = tid; i < G * PART_STRIDE; i += 128) {
+      const int c = i % PART_STRIDE;
+      if (kv == 0 ? (c == D || c == D + 1) : c < D) dslot[i] = c == D ? -INFINITY : 0.f;
+    }
     return;
   }
-  float *xs = reinterpret_cast<float *>(sm.ring[0]);   // [2][D]: the K and V vectors
-  float *pacc = xs + 2 * D;                            // [4 warps][32 lanes][4]
+  float *xs = reinterpret_cast<float *>(sm.ring[0]);   // [D]: the vector
+  float *pacc = xs + D;                                // [4 warps][32 lanes][4]
   float *psab = pacc + 4 * 32 * 4;
-  uint8_t *dcode = reinterpret_cast<uint8_t *>(psab + 4 * 32 * 4);  // [2][D / 4]
-  uint16_t *dsz = reinterpret_cast<uint16_t *>(dcode + 2 * (D / 4));  // scale K, scale V, zero K, zero V
-  const int kv = warp >> 1, w2 = warp & 1;
+  uint8_t *dcode = reinterpret_cast<uint8_t *>(psab + 4 * 32 * 4);  // [D / 4]
+  uint16_t *dsz = reinterpret_cast<uint16_t *>(dcode + D / 4);      // scale, zero
   const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
-  if (w2 == 0) {
+  const float *cb = kv == 0 ? p.cb_k : p.cb_v;
+  if (warp == 0) {
     const uint2 xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
                                                      (((size_t)b * p.Hkv + kvh) * RECENT + st.rs) * D)[lane];
-    float *dst = xs + kv * D + 4 * lane;
-    dst[0] = bf16_to_f32(xw.x & 0xffffu);
-    dst[1] = bf16_to_f32(xw.x >> 16);
-    dst[2] = bf16_to_f32(xw.y & 0xffffu);
-    dst[3] = bf16_to_f32(xw.y >> 16);
+    xs[4 * lane + 0] = bf16_to_f32(xw.x & 0xffffu);
+    xs[4 * lane + 1] = bf16_to_f32(xw.x >> 16);
+    xs[4 * lane + 2] = bf16_to_f32(xw.y & 0xffffu);
+    xs[4 * lane + 3] = bf16_to_f32(xw.y >> 16);
   }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
   float acc[4] = {0.f, 0.f, 0.f, 0.f}, sab[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-  for (int bt = 0; bt < 4; ++bt) {
-    const int r0 = 64 * w2 + 16 * bt;
+  for (int bt = 0; bt < 2; ++bt) {
+    const int r0 = 32 * warp + 16 * bt;
     const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)r0 * (D / 4) + lane;
     float4 rrow[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) rrow[i] = R4[i * (D / 4)];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float xi = xs[kv * D + r0 + i], ax = fabsf(xi);
+      const float xi = xs[r0 + i], ax = fabsf(xi);
       acc[0] = fmaf(xi, rrow[i].x, acc[0]);
       acc[1] = fmaf(xi, rrow[i].y, acc[1]);
       acc[2] = fmaf(xi, rrow[i].z, acc[2]);
@@ -406,45 +410,45 @@ __device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int 
 #pragma unroll
   for (int k = 0; k < 4; ++k) { pacc[(warp * 32 + lane) * 4 + k] = acc[k]; psab[(warp * 32 + lane) * 4 + k] = sab[k]; }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
-  if (w2 == 0) {
+  if (warp == 0) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      acc[k] = pacc[(warp * 32 + lane) * 4 + k] + pacc[((warp + 1) * 32 + lane) * 4 + k];
-      sab[k] = psab[(warp * 32 + lane) * 4 + k] + psab[((warp + 1) * 32 + lane) * 4 + k];
+      acc[k] = (pacc[lane * 4 + k] + pacc[(32 + lane) * 4 + k]) + (pacc[(64 + lane) * 4 + k] + pacc[(96 + lane) * 4 + k]);
+      sab[k] = (psab[lane * 4 + k] + psab[(32 + lane) * 4 + k]) + (psab[(64 + lane) * 4 + k] + psab[(96 + lane) * 4 + k]);
     }
     QuantStats qst{0, 0, 0};
-    const float *cb = kv == 0 ? p.cb_k : p.cb_v;
-    quantize_from_dots(xs + kv * D, Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g,
-                       dcode + kv * (D / 4), dsz + kv, dsz + 2 + kv, qst, cb != nullptr ? cb + 4 * kvh : nullptr);
+    quantize_from_dots(xs, Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcode, dsz, dsz + 1, qst,
+                       cb != nullptr ? cb + 4 * kvh : nullptr);
   }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
-  if (tid < 2 * (D / 4)) {  // the demoted K and V codes, scale and zero into history row hist_len
-    const int kv2 = tid / (D / 4), byte = tid % (D / 4);
+  if (tid < D / 4) {  // the demoted codes, scale and zero into history row hist_len
     const size_t row = ((size_t)p.page_table[(size_t)b * p.max_pages + st.hl / PAGE] * p.Hkv + kvh) * PAGE +
                        st.hl % PAGE;
-    (kv2 == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + byte] = dcode[kv2 * (D / 4) + byte];
-    if (byte == 0) {
-      (kv2 == 0 ? p.scale_k : p.scale_v)[row] = dsz[kv2];
-      (kv2 == 0 ? p.zero_k : p.zero_v)[row] = dsz[2 + kv2];
+    (kv == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + tid] = dcode[tid];
+    if (tid == 0) {
+      (kv == 0 ? p.scale_k : p.scale_v)[row] = dsz[0];
+      (kv == 0 ? p.zero_k : p.zero_v)[row] = dsz[1];
     }
   }
-  const float sk = bf16_to_f32(dsz[0]), zk = bf16_to_f32(dsz[2]);
-  const float sv = bf16_to_f32(dsz[1]), zv = bf16_to_f32(dsz[3]);
+  const float sc = bf16_to_f32(dsz[0]), zr = bf16_to_f32(dsz[1]);
   // dequantization levels (the codes themselves without a codebook)
-  auto level = [&](const float *cb, uint32_t c) { return cb != nullptr ? cb[4 * kvh + c] : (float)c; };
-  for (int i = tid; i < G * D; i += 128) {  // o: the dequantized rotated V, the same for every head
-    const int c = i % D;
-    dslot[(i / D) * PART_STRIDE + c] = fmaf(level(p.cb_v, (dcode[D / 4 + c / 4] >> (2 * (c & 3))) & 3u), sv, zv);
+  auto level = [&](uint32_t c) { return cb != nullptr ? cb[4 * kvh + c] : (float)c; };
+  if (kv == 1) {  // o: the dequantized rotated V, the same for every head
+    for (int i = tid; i < G * D; i += 128) {
+      const int c = i % D;
+      dslot[(i / D) * PART_STRIDE + c] = fmaf(level((dcode[c / 4] >> (2 * (c & 3))) & 3u), sc, zr);
+    }
+    return;
   }
   pdl_wait();  // the query rotation has completed: its q_rot is read
-  const uint32_t cb = dcode[lane];  // K codes of channels 4 lane .. 4 lane + 3
+  const uint32_t cw = dcode[lane];  // K codes of channels 4 lane .. 4 lane + 3
   for (int h = warp; h < G; h += 4) {
     const float4 q4 = reinterpret_cast<const float4 *>(a.qrot + ((size_t)b * p.Hq + kvh * G + h) * D)[lane];
     const float qr[4] = {q4.x, q4.y, q4.z, q4.w};
-    float dc = 0.f, dce = 0.f, sq = 0.f;  // sum of q_rot * code with its rounding errors
+    float dc = 0.f, dce = 0.f, sq = 0.f;  // sum of q_rot * level with its rounding errors
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float cf = level(p.cb_k, (cb >> (2 * k)) & 3u);
+      const float cf = level((cw >> (2 * k)) & 3u);
       const float pr = qr[k] * cf, pe = fmaf(qr[k], cf, -pr);
       float t, e2;
       two_sum_f32(dc, pr, t, e2);
@@ -463,7 +467,7 @@ __device__ __noinline__ void demote_role(const Args &a, Smem<G> &sm, int b, int 
       sq += __shfl_xor_sync(FULL, sq, o);
     }
     if (lane == 0) {
-      dslot[h * PART_STRIDE + D] = a.sm_log2 * fmaf(sk, dc + dce, zk * sq);
+      dslot[h * PART_STRIDE + D] = a.sm_log2 * fmaf(sc, dc + dce, zr * sq);
       dslot[h * PART_STRIDE + D + 1] = 1.f;
     }
   }
@@ -602,7 +606,7 @@ __device__ __forceinline__ void bf16_role(const Args &a, Smem<G> &sm) {
     slot[h * PART_STRIDE + tid] = O;
     if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
   }
-  if (a.step && chunk == 0) demote_role<G>(a, sm, b, kvh, seg, st);
+  if (a.step && chunk < 2) demote_role<G>(a, sm, b, kvh, seg, st, chunk);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -150,3 +150,23 @@ def test_decode_step_with_a_merge_grid_of_several_waves():
     torch.cuda.synchronize()
     helpers.assert_pools_equal(O, P)
     assert P.err() == 0 and int(P.sync.abs().sum()) == 0
+
+
+def test_many_partials_per_segment_merge_in_several_rounds():
+    """One KV head with a 20k-token history: every history CTA of the launch works on the same segment,
+    so the merge stages its partial slots in several rounds (running maximum across rounds)."""
+    seed, Hkv, Hq = 720, 1, 4
+    O, P, q = _setup([20000], Hq, Hkv, 128, seed, extra_pages=1)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for t in range(3):
+        kn = synth.outlier_kv(seed + 2000 + t, 1, Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, 1, Hkv, 128, ch)
+        qt = synth.outlier_q(seed + 4000 + t, 1, Hq, Hkv, 128, ch)
+        O.append(kn, vn)
+        out = ok.oscar_decode_step(P, helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn), helpers.to_dev_bf16(qt))
+        helpers.assert_attention_close(out.cpu().numpy(), O.decode(qt))
+    torch.cuda.synchronize()
+    helpers.assert_pools_equal(O, P)
+    assert P.err() == 0
