@@ -30,6 +30,15 @@ __device__ __forceinline__ float level(uint32_t code, float4 l) {
   return code < 2 ? (code == 0 ? l.x : l.y) : (code == 2 ? l.z : l.w);
 }
 
+// true when token j of the chunk has weight 0 for every head (an invalid token: its staged row was not written)
+template <int G>
+__device__ __forceinline__ bool s_all_zero(float (*pbuf)[32], int j) {
+  bool z = true;
+#pragma unroll
+  for (int h = 0; h < G; ++h) z = z && pbuf[h][j] == 0.f;
+  return z;
+}
+
 // Online-softmax update of one 32-token chunk for G heads; scores s[h] are lane-local (one token per
 // lane), o[h][k] are lane-local output channels 4*lane+k.  p values go to pbuf[h][lane].
 template <int G>
@@ -93,6 +102,8 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
   __shared__ float qr[D][G];
   __shared__ float qsum[G][4];
   __shared__ float pbuf[4][G][32];
+  __shared__ uint4 vrow_s[4][32][2];      // per warp: the V codes of the chunk's 32 tokens (32 bytes each)
+  __shared__ uint16_t vsz_s[4][32][8];    // per warp: their V scales [0, ng) and zeros [4, 4 + ng)
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = p.g, ng = p.ng;
@@ -149,6 +160,17 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
       if (page < 0 || page >= p.num_pages) { valid = false; atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX); }
     }
     float s[G];
+    // this lane's token's V row and its scales / zeros, staged for the PV loop (one round of loads)
+    if (valid) {
+      const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (t % PAGE);
+      const uint4 *vp = reinterpret_cast<const uint4 *>(p.codes_v + row * (D / 4));
+      vrow_s[warp][lane][0] = vp[0];
+      vrow_s[warp][lane][1] = vp[1];
+      for (int gi = 0; gi < ng; ++gi) {
+        vsz_s[warp][lane][gi] = p.scale_v[row * ng + gi];
+        vsz_s[warp][lane][4 + gi] = p.zero_v[row * ng + gi];
+      }
+    }
     if (valid) {
       const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (t % PAGE);
       const uint4 *cp = reinterpret_cast<const uint4 *>(p.codes_k + row * (D / 4));
@@ -180,17 +202,14 @@ __global__ void __launch_bounds__(128) hist_partial_kernel(PoolArgs p, const uin
 #pragma unroll
       for (int h = 0; h < G; ++h) s[h] = -INFINITY;
     }
-    softmax_chunk<G>(s, m, l, o, pbuf[warp]);
+    softmax_chunk<G>(s, m, l, o, pbuf[warp]);  // ends with a __syncwarp: the staged rows are visible
     const int nv = min(32, t1 - base);
+    const int gi = (4 * lane) / g;
     for (int j = 0; j < nv; ++j) {
-      const int tj = base + j;
-      const int pg = pt[tj / PAGE];
-      if (pg < 0 || pg >= p.num_pages) continue;
-      const size_t row = ((size_t)pg * p.Hkv + kvh) * PAGE + (tj % PAGE);
-      const uint32_t byte = p.codes_v[row * (D / 4) + lane];
-      const int gi = (4 * lane) / g;
-      const float sc = bf16_to_f32(p.scale_v[row * ng + gi]);
-      const float z = bf16_to_f32(p.zero_v[row * ng + gi]);
+      if (pbuf[warp][0][j] == 0.f && (G == 1 || s_all_zero<G>(pbuf[warp], j))) continue;  // invalid or no weight
+      const uint32_t byte = reinterpret_cast<const uint8_t *>(&vrow_s[warp][j][0])[lane];
+      const float sc = bf16_to_f32(vsz_s[warp][j][gi]);
+      const float z = bf16_to_f32(vsz_s[warp][j][4 + gi]);
       float v[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) v[k] = fmaf(level((byte >> (2 * k)) & 3u, lv), sc, z);
