@@ -1360,8 +1360,8 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.step = k_new != nullptr;
   a.k_new = k_new;
   a.v_new = v_new;
-  // Step form: the attention reads only state the step leaves unchanged; the merge performs the
-  // demotion (overlapping the attention's tail), the append and the counter update.
+  // Step form: the attention reads only state the step leaves unchanged and its BF16 CTAs perform the
+  // demotion (overlapping the history CTAs); the merge performs the append and the counter update.
   if ((e = cudaFuncSetAttribute(v1::merge_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)v1::MERGE_SMEM)) != cudaSuccess)
     return e;
