@@ -230,7 +230,7 @@ __device__ __forceinline__ void flush(const Args &a, Smem<G> &sm, WarpState &ws,
 // the sum).
 __device__ __forceinline__ void page_pass(uint8_t *kpage, int ntok, float sm_log2, WarpState &ws,
                                           const uint32_t (&bq)[8][2]) {
-  const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5), g = lane >> 2, t = lane & 3;
+  const int lane = threadIdx.x & 31, warp = (threadIdx.x >> 5), g = lane >> 2;
   const int r0 = 16 * warp;
   uint8_t *vpage = kpage + HALF_BYTES;
   if (ntok < r0 + 16) {
