@@ -23,9 +23,10 @@
 //    R_hi + R_lo + Delta gives an interval of at most a few float32 ulps around x_hat; if that still
 //    leaves the decision open, the float64 double-double / 128-bit integer evaluation decides.
 //
-// Warp roles (320 threads, one CTA per SM): warp 0 issues TMA loads of x tiles into a 4-stage ring,
-// warp 1 owns tensor memory and issues the MMAs into 4 accumulators of 128 columns, warps 2-9 form two
-// epilogue groups of four warps that take alternate tiles; in an epilogue warp each thread owns one
+// Warp roles (448 threads, one CTA per SM): warp 0 issues TMA loads of x tiles into a 4-stage ring,
+// warp 1 owns tensor memory and issues the MMAs into 4 accumulators of 128 columns, warps 2-13 form
+// three epilogue groups of four warps that take every third tile (the epilogue bounds the kernel: a
+// third group adds latency hiding; two groups ran 7% slower); in an epilogue warp each thread owns one
 // token row.  Each CTA processes a contiguous range of (head, tile) units; the R image in shared
 // memory is rebuilt when the range crosses into the next head.
 #include <cuda.h>
@@ -44,8 +45,9 @@ constexpr int ATOM = 16384;                    // one 128-row x 64-channel bf16 
 constexpr int STAGE_BYTES = 2 * ATOM;          // a tile: channels 0-63 and 64-127
 constexpr int NACC = 4;                        // fp32 accumulators of 128 TMEM columns
 constexpr int TMEM_COLS = NACC * 128;
-constexpr int THREADS = 320;
-constexpr int EPI_THREADS = 256;
+constexpr int NGRP = 3;                        // epilogue groups of four warps
+constexpr int THREADS = 64 + 128 * NGRP;
+constexpr int EPI_THREADS = 128 * NGRP;
 constexpr int DL_STRIDE = 130;                 // bf16 per row of the Delta table (spreads banks)
 constexpr float KAPPA_TC = 0x1p-17f;
 constexpr float MAGIC = 12582912.0f;           // 1.5 * 2^23: adding it rounds [0, 3] to an integer
@@ -237,16 +239,19 @@ __device__ __forceinline__ float row_bound(const uint8_t *st, int row, float cE)
   return __fadd_ru(__fmul_ru(cE, __fsqrt_ru(__fadd_ru(__fmul_ru(ss, 1.0f + 0x1p-14f), 1e-36f))), 1e-37f);
 }
 
-// Rebuild the shared-memory image of head h's R (epilogue threads, tb in [0, 256)): the MMA operand
+// Rebuild the shared-memory image of head h's R (epilogue threads tb in [0, 256) build it, the rest of
+// the epilogue threads only take part in the barriers): the MMA operand
 // [R_hi ; R_lo]^T in swizzled K-major atoms, the residual table Delta, and the bound constant cE.
 __device__ void build_head(const QArgs &a, uint8_t *sm, uint32_t *misc, uint64_t *bready, int h, int tb) {
   named_bar_sync(1, EPI_THREADS);  // every tile of the previous head is finished (its MMAs complete)
-  const int j = tb & (D - 1), half = tb >> 7;
+  const int j = tb & (D - 1), half = tb >> 7;  // threads tb >= 256 only take part in the barriers
+  bool exact = true;
+  float sd = 0.f, sr = 0.f;
+  float *part = reinterpret_cast<float *>(sm + OFF_PART);
+  if (tb < 256) {
   const float *R = a.R32 + (size_t)h * D * D;
   uint8_t *Bs = sm + OFF_B;
   uint16_t *Dl = reinterpret_cast<uint16_t *>(sm + OFF_DL);
-  float sd = 0.f, sr = 0.f;
-  bool exact = true;
   float rr[D / 2];
 #pragma unroll
   for (int m = 0; m < D / 2; ++m) rr[m] = R[(2 * m + half) * D + j];  // all loads in flight at once
@@ -268,10 +273,10 @@ __device__ void build_head(const QArgs &a, uint8_t *sm, uint32_t *misc, uint64_t
     const float t = __fadd_rn(fabsf(bfv(rh)), fabsf(bfv(rl)));
     sr = fmaf(t, t, sr);
   }
-  float *part = reinterpret_cast<float *>(sm + OFF_PART);
   if (half) {
     part[j] = sd;
     part[D + j] = sr;
+  }
   }
   fence_proxy_async_smem();
   const bool all_exact = named_bar_and(1, EPI_THREADS, exact);
@@ -279,7 +284,7 @@ __device__ void build_head(const QArgs &a, uint8_t *sm, uint32_t *misc, uint64_t
     misc[M_TABLE_EXACT] = all_exact ? 1u : 0u;
     mbar_arrive(bready);
   }
-  if (!half) {
+  if (tb < 128) {
     // per-column bound factor, every step rounded up; 1 + 2^-12 covers the float32 sums above
     const float ssr = __fmul_ru(__fadd_ru(sr, part[D + j]), 1.0f + 0x1p-12f);
     const float ssd = __fmul_ru(__fadd_ru(sd, part[j]), 1.0f + 0x1p-12f);
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(THREADS, 1) quant_tc_kernel(const __grid_const
       const float clip = a.clip[h];
       for (; u < seg_end; ++u, ++it) {
         // decisions stay warp-uniform: the tensor-memory loads below are warp-collective
-        if ((int)(it & 1u) != grp || __any_sync(FULL, aborted(misc))) continue;
+        if ((int)(it % NGRP) != grp || __any_sync(FULL, aborted(misc))) continue;
         const uint32_t s = it % NSTAGE, b = it % NACC;
         // the row norm needs only the loaded tile: compute it while the MMA runs
         if (!__all_sync(FULL, wait_or_abort(full + s, (it / NSTAGE) & 1u, a, misc))) continue;
