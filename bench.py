@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--layers", type=int, default=8, help="rotating layer buffers (working set > L2)")
+    ap.add_argument("--layers", type=int, default=10,
+                    help="rotating layer buffers (working set >= 4x the 129 MB L2)")
     ap.add_argument("--e2e-steps", type=int, default=2000)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -641,9 +642,10 @@ def main():
 
     NL = args.layers
     DEM_N = 200  # appends timed on their own after the run
+    HOT_N, HOT_W = 500, 20  # the L2-hot steps (layer 0 only) after the run
     total = args.warmup + args.steps + args.e2e_steps + DEM_N
     per_layer = -(-total // NL)
-    layers = setup_layers(NL, per_layer + 8)
+    layers = setup_layers(NL, per_layer + HOT_N + HOT_W + 8)
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev)
     gen.manual_seed(77 + rank)
@@ -740,6 +742,26 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     dem_ms = e0.elapsed_time(e1) / DEM_N
+    # L2-hot: the same step on one layer again and again, so that its ~58 MB stay in the 129 MB L2
+    hot_tokens = 0
+
+    def hot_step():
+        st = lib.oscar_decode_step(layers[0].ref, C.c_void_p(kn[0].data_ptr()), C.c_void_p(vn[0].data_ptr()),
+                                   C.c_void_p(qs[0].data_ptr()), C.c_void_p(outs[0].data_ptr()), scale,
+                                   C.c_void_p(ws.data_ptr()), ws_bytes, sp)
+        if st:
+            raise RuntimeError(lib.oscar_last_error_string().decode())
+        appended[0] += 1
+        return L_CTX + appended[0]
+    for _ in range(HOT_W):
+        hot_step()
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(HOT_N):
+        hot_tokens += hot_step()
+    e1.record()
+    torch.cuda.synchronize()
+    hot_ms = e0.elapsed_time(e1)
     for P in layers:
         if P.err() != 0:
             raise RuntimeError(f"device error flags {P.err():#x}")
@@ -772,7 +794,7 @@ def main():
             "vs_baseline": None, "dtype": "int2-kv/f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D,
                        "group_size": GROUP, "clip": CLIP, "page_tokens": PAGE, "rotation": "covariance (GPU calib)",
-                       "l2": f"{NL} rotating layer buffers ({NL * step_bytes / 1e6:.0f} MB > L2)",
+                       "l2": f"{NL} rotating layer buffers ({NL * step_bytes / 1e6:.0f} MB >= 4x L2)",
                        "parallelism": f"replicas x{world}"},
             "decode_steps_per_s": world * args.steps / (ms * 1e-3),
             "bytes_per_step": step_bytes,
@@ -780,6 +802,7 @@ def main():
             "roofline": {"bound": "hbm", "kernel": "attn_kernel (INT2 history + BF16 sink/recent CTAs)",
                          "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                         "frac_of_nominal_8tbs": achieved / 8000.0,
                          "traffic": traffic_from_profiles(os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc",
                                                                        "decode_v1.cu")),
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3,
@@ -787,6 +810,8 @@ def main():
             "demote": {"tokens_per_s": 1.0 / (dem_ms * 1e-3), "mean_call_us": dem_ms * 1e3,
                        "note": "oscar_append_kv (demotion + append kernel), timed on its own after the run; in "
                                "the decode step the attention kernel's sink CTAs perform the demotion"},
+            "l2_hot": {"value": hot_tokens / (hot_ms * 1e-3), "unit": "KV tokens/s", "ms_per_step": hot_ms / HOT_N,
+                       "steps": HOT_N, "note": "one layer's step repeated: its history stays in L2"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
