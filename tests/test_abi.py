@@ -36,6 +36,7 @@ def _pool(**kw):
     p.num_pages, p.max_pages = 4, 4
     for name, _ in _lib.oscar_pool._fields_[7:]:
         setattr(p, name, 0x10000)
+    p.codebook_k = p.codebook_v = None  # the uniform levels unless a test sets a codebook
     for k, v in kw.items():
         setattr(p, k, v)
     return p
@@ -117,3 +118,26 @@ def test_bf16_cache_call_validation(lib):
     assert lib.oscar_bf16_prefill(C.byref(c), 2, 10, FAKE, FAKE, None) == 1          # seq out of range
     assert lib.oscar_bf16_prefill(C.byref(c), 0, 8 * 64 + 1, FAKE, FAKE, None) == 1  # longer than max_pages*64
     assert lib.oscar_bf16_prefill(C.byref(c), 0, 10, None, FAKE, None) == 1
+
+
+def test_codebook_validation(lib):
+    """Codebook pools and the codebook calls reject bad arguments before any launch."""
+    assert lib.oscar_demote(C.byref(_pool(codebook_k=0x10004)), None, None) == 1   # codebooks 16-byte aligned
+    assert lib.oscar_demote(C.byref(_pool(codebook_v=0x10008)), None, None) == 1
+    n = C.c_size_t(0)
+    assert lib.oscar_decode_workspace_size(C.byref(_pool(codebook_k=0x10000, codebook_v=0x10000)), 0,
+                                           C.byref(n)) == 0 and n.value > 0
+    src, dst = (FAKE,) * 3, (FAKE,) * 3
+    assert lib.oscar_quantize_kv_codebook(16, 2, 128, 128, *src, None, *dst, None, None) == 1
+    assert lib.oscar_quantize_kv_codebook(16, 2, 128, 128, *src, C.c_void_p(0x10004), *dst, None, None) == 1
+    assert lib.oscar_quantize_kv_codebook(16, 2, 128, 48, *src, FAKE, *dst, None, None) == 2
+    assert lib.oscar_quantize_kv_codebook(16, 2, 64, 128, *src, FAKE, *dst, None, None) == 2
+    assert lib.oscar_quantize_kv_codebook(0, 2, 128, 128, *src, FAKE, *dst, None, None) == 0  # empty: no-op
+    # Lloyd-Max calibration: the workspace query, a missing workspace, bad sizes
+    assert lib.oscar_lloyd_max_workspace_size(10, 2, C.byref(n)) == 0 and n.value == 10 * 2 * 128 * 4
+    assert lib.oscar_lloyd_max_workspace_size(-1, 2, C.byref(n)) == 1
+    assert lib.oscar_lloyd_max_workspace_size(10, 2, None) == 1
+    assert lib.oscar_lloyd_max_codebook(10, 2, 128, 128, FAKE, FAKE, FAKE, 200, FAKE, FAKE, 16, None) == 3
+    assert lib.oscar_lloyd_max_codebook(10, 2, 128, 128, FAKE, FAKE, FAKE, -1, FAKE, FAKE, 10240, None) == 1
+    assert lib.oscar_lloyd_max_codebook(10, 2, 64, 128, FAKE, FAKE, FAKE, 200, FAKE, FAKE, 10240, None) == 2
+    assert lib.oscar_lloyd_max_codebook(10, 2, 128, 128, FAKE, FAKE, FAKE, 200, None, FAKE, 10240, None) == 1
