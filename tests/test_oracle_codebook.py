@@ -83,3 +83,39 @@ def test_codebook_pool_round_trip_and_distortion():
         exact = quant.rotate_exact_many(K[64:L - 256, 0], R).astype(np.float64)
         err[name] = np.mean((hk - exact) ** 2)
     assert err["lloyd"] < err["uniform"]
+
+
+def test_calibration_values_hand_computed_rows():
+    """calibration_values on rows whose t are known by hand (R = I, so x_hat = x):
+    row A: min -3, max 6, clip 1: scale 3, zero -3, t = (x + 3) / 3;
+    row B: min -4, max 8, clip 0.5: the clip scales the extremes only (lo -2, hi 4, scale 2, zero -2), so
+           x = -4 gives t = -1 and x = 8 gives t = 5 (no clamp of x);
+    row C: min 0, max 1, clip 1: scale = bf16(fp32(1/3)) = 0.333984375 (0x3EAB), so x = 1 gives
+           t = fp32(1 / 0.333984375) = 2.9941520..., not 3 (the stored bf16 scale is the divisor);
+    row D: constant: scale 0, the group is left out."""
+    d = 128
+    I = np.eye(d, dtype=np.float32)
+    base = np.zeros(d, np.float32)
+    A = base.copy(); A[[0, 1, 2, 3]] = [-3.0, 6.0, 0.0, 1.5]
+    B = base.copy(); B[[0, 1, 2]] = [-4.0, 8.0, 0.0]
+    C = base.copy(); C[[5, 9]] = [1.0, 0.5]
+    Dc = np.full(d, 2.0, np.float32)
+    rows = lambda *r: synth.to_bf16_bits(np.stack(r))
+    tA = codebook.calibration_values(rows(A), I, 1.0, 128)
+    assert tA.shape == (128,)
+    np.testing.assert_array_equal(tA[:4], np.array([0.0, 3.0, 1.0, 1.5], np.float32))
+    assert np.all(tA[4:] == np.float32(1.0))                       # x = 0 -> (0 + 3) / 3
+    tB = codebook.calibration_values(rows(B), I, 0.5, 128)
+    np.testing.assert_array_equal(tB[:3], np.array([-1.0, 5.0, 1.0], np.float32))
+    tC = codebook.calibration_values(rows(C), I, 1.0, 128)
+    assert tC[5] == np.float32(1.0) / np.float32(0.333984375) and tC[5] != np.float32(3.0)
+    assert tC[0] == 0.0 and tC[9] == np.float32(0.5) / np.float32(0.333984375)
+    assert codebook.calibration_values(rows(Dc), I, 1.0, 128).size == 0
+    # group 32: the constant group of a row is left out, the others kept in order
+    E = base.copy(); E[:32] = 7.0; E[32:64] = np.linspace(-1, 2, 32).round(2); E[64] = -6.0; E[127] = 3.0
+    tE = codebook.calibration_values(rows(E), I, 1.0, 32)
+    assert tE.size == 96                                           # groups 1, 2, 3 of 4
+    g3 = tE[64:]                                                   # group 3: min 0, max 3 -> scale 1, zero 0
+    assert g3[-1] == np.float32(3.0) and np.all(g3[:-1] == 0.0)
+    g2 = tE[32:64]                                                 # group 2: min -6, max 0 -> scale 2, zero -6
+    assert g2[0] == 0.0 and np.all(g2[1:] == np.float32(3.0))
