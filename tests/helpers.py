@@ -73,3 +73,59 @@ def assert_attention_close(got: np.ndarray, ref: np.ndarray):
     assert err.max() <= ATOL, f"max-abs error {err.max():.3e} > {ATOL}"
     assert rel <= RTOL_L2, f"relative L2 error {rel:.3e} > {RTOL_L2}"
     return err.max(), rel
+
+
+# ---- sampled-sequence parity at full workload sizes ---------------------------------------------------
+# At the batch sweep's and the mixed batch's sizes the oracle cannot hold or quantize every sequence, so
+# it builds a pool of a few sampled sequences (the other sequences are in the device pool only, with
+# GPU-drawn contents that nothing compares).  Each sampled sequence has the same page-table row length
+# in both pools; the oracle's pages are numbered compactly, and the device pages are gathered through
+# the device page table before a byte comparison.
+
+def make_sampled_pools(B, Hq, Hkv, g, pages_per_seq, sampled, seed, clip_k=None, clip_v=None, extra_pages=0):
+    """(oracle Pool of the sampled sequences, device Pool of all B, device page table as numpy)."""
+    import bit_rotated_kv_02_gb300 as ok
+    Rk = oracle_rotations(seed, Hkv)
+    Rv = oracle_rotations(seed + 1000, Hkv)
+    clip_k = np.full(Hkv, 0.9, np.float32) if clip_k is None else np.asarray(clip_k, np.float32)
+    clip_v = np.full(Hkv, 0.9, np.float32) if clip_v is None else np.asarray(clip_v, np.float32)
+    own = [p + extra_pages for p in pages_per_seq]
+    max_pages = max(max(own), 1)
+    pt, num_pages = synth.page_tables(seed, own, max_pages)
+    sub_own = [own[b] for b in sampled]
+    O = opool.Pool(len(sampled), Hq, Hkv, 128, g, max(sum(sub_own), 1), max_pages, Rk, Rv, clip_k, clip_v)
+    o = 0
+    for j, n in enumerate(sub_own):
+        O.page_table[j, :n] = np.arange(o, o + n, dtype=np.int32)
+        o += n
+    P = ok.Pool(B, Hq, Hkv, g, num_pages, max_pages, torch.from_numpy(Rk), torch.from_numpy(Rv),
+                torch.from_numpy(clip_k), torch.from_numpy(clip_v))
+    P.set_page_table(pt)
+    return O, P, pt
+
+
+def assert_sampled_pools_equal(O, P, pt, sampled, heads=None):
+    """Byte equality of the sampled sequences' sink, window, history pages (gathered through the device
+    page table) and counters; `heads` restricts the history comparison to those KV heads."""
+    hs = slice(None) if heads is None else list(heads)
+    dev = {name: device_array(P, name) for name in POOL_ARRAYS}
+    cnt = {name: getattr(P, name).cpu().numpy() for name in ("sink_len", "hist_len", "recent_start", "recent_len")}
+    for j, b in enumerate(sampled):
+        for name in ("sink_len", "hist_len", "recent_start", "recent_len"):
+            assert getattr(O, name)[j] == cnt[name][b], f"{name} of sequence {b}"
+        for name in ("sink_k", "sink_v", "recent_k", "recent_v"):
+            assert np.array_equal(getattr(O, name)[j], dev[name][b]), f"{name} of sequence {b}"
+        np_ = -(-int(O.hist_len[j]) // 64)
+        dp, op = pt[b, :np_], O.page_table[j, :np_]
+        for name in ("codes_k", "codes_v", "scale_k", "zero_k", "scale_v", "zero_v"):
+            a, d = getattr(O, name)[op][:, hs], dev[name][dp][:, hs]
+            assert np.array_equal(a, d), f"{name} of sequence {b}: {np.count_nonzero(a != d)} entries differ"
+
+
+def gpu_outlier_kv(gen, n, Hkv, channels, factor=20.0):
+    """bf16 [n][Hkv][128] on the GPU: N(0,1) draws of a seeded torch generator with the given outlier
+    channels scaled; the contents of unsampled sequences (never compared, never seen by the oracle)."""
+    x = torch.randn((n, Hkv, 128), generator=gen, device="cuda")
+    idx = torch.as_tensor(np.asarray(channels, np.int64), device="cuda")[None].expand(n, -1, -1)
+    x.scatter_(2, idx, x.gather(2, idx) * factor)
+    return x.to(torch.bfloat16)
