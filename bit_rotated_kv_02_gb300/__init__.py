@@ -20,7 +20,7 @@ from ._lib import OscarError
 
 HEAD_DIM, PAGE, SINK, RECENT = 128, 64, 64, 256
 ROT_HAAR, ROT_COVARIANCE = 0, 1
-DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT = 1, 2, 4, 8
+DEVERR_PAGE_INDEX, DEVERR_HISTORY_FULL, DEVERR_COUNTERS, DEVERR_TIMEOUT, DEVERR_DEBUG_CHECK = 1, 2, 4, 8, 16
 
 __all__ = ["OscarError", "Pool", "oscar_version", "oscar_make_rotation", "oscar_calib_covariance_k",
            "oscar_calib_covariance_v", "oscar_quantize_kv", "oscar_quantize_kv_codebook", "oscar_lloyd_max_codebook", "oscar_prefill_pool", "oscar_prefill_pool_shared", "oscar_demote", "oscar_append_kv",

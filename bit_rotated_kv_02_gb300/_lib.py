@@ -81,11 +81,12 @@ def header_functions() -> list[str]:
 
 
 def load(path: str | None = None) -> C.CDLL:
-    """Load liboscar.so; raises if it has not been built (there is no fallback implementation)."""
+    """Load liboscar.so (liboscar_debug.so, the build with device-side bounds checks, when the environment
+    sets OSCAR_DEBUG=1); raises if it has not been built (there is no fallback implementation)."""
     global _LIB
     if _LIB is not None:
         return _LIB
-    path = path or _build.LIB
+    path = path or (_build.LIB_DEBUG if os.environ.get("OSCAR_DEBUG") == "1" else _build.LIB)
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
                            "(the CUDA library is the only implementation; there is no fallback)")

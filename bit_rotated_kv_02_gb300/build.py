@@ -11,6 +11,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OBJDIR = os.path.join(os.path.dirname(HERE), "_build")
 LIB = os.path.join(HERE, "liboscar.so")
+# The debug build: the same sources with the device-side bounds checks compiled in (OSCAR_DEBUG), loaded
+# instead of liboscar.so when the environment sets OSCAR_DEBUG=1.
+LIB_DEBUG = os.path.join(HERE, "liboscar_debug.so")
+DEBUG_FLAGS = ["-DOSCAR_DEBUG"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
@@ -32,23 +36,26 @@ def _deps() -> list[str]:
     return sources() + hdrs + [os.path.join(INCLUDE, "oscar.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile every .cu under csrc/ and link liboscar.so next to this file; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None, debug: bool = False) -> str:
+    """Compile every .cu under csrc/ and link liboscar.so (debug: liboscar_debug.so, with the device-side
+    bounds checks) next to this file; returns its path."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    objdir = os.path.join(OBJDIR, "debug") if debug else OBJDIR
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
-    flags = FLAGS + (extra_flags or [])
+    flags = FLAGS + (DEBUG_FLAGS if debug else []) + (extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,13 +66,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -3,6 +3,7 @@
 // return status and oscar_last_error_string().
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 
 #include "oscar_internal.cuh"
@@ -63,8 +64,8 @@ oscar_status_t check_pool(const oscar_pool *pool, PoolArgs &a) {
        reinterpret_cast<uintptr_t>(p.R_k) | reinterpret_cast<uintptr_t>(p.R_v)) & 15u)
     return fail(OSCAR_ERR_INVALID_ARG, "pool arrays must be 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(p.scale_k) | reinterpret_cast<uintptr_t>(p.zero_k) |
-       reinterpret_cast<uintptr_t>(p.scale_v) | reinterpret_cast<uintptr_t>(p.zero_v)) & 7u)
-    return fail(OSCAR_ERR_INVALID_ARG, "pool scale/zero arrays must be 8-byte aligned");
+       reinterpret_cast<uintptr_t>(p.scale_v) | reinterpret_cast<uintptr_t>(p.zero_v)) & 15u)
+    return fail(OSCAR_ERR_INVALID_ARG, "pool scale/zero arrays must be 16-byte aligned");
   a.B = p.batch; a.Hq = p.num_q_heads; a.Hkv = p.num_kv_heads; a.d = p.head_dim; a.g = p.group_size;
   a.ng = p.head_dim / p.group_size; a.num_pages = p.num_pages; a.max_pages = p.max_pages;
   a.sink_k = p.sink_k; a.sink_v = p.sink_v; a.recent_k = p.recent_k; a.recent_v = p.recent_v;
@@ -311,9 +312,22 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
   return cuda_status(launch_demote(a, nullptr, 2, k_new, v_new, static_cast<cudaStream_t>(stream)), "append_kv");
 }
 
-// Whole-vector groups decode on the tensor-core path (codes, or a codebook's indicator planes, as exact
-// small integers in the MMA); other group sizes on the CUDA-core path.
-static bool tensor_core_path(const PoolArgs &a) { return a.g == OSCAR_HEAD_DIM; }
+// Decode paths.  Whole-vector groups (128): the warp-MMA kernels of decode_v1.cu (uniform levels, or a
+// codebook's indicator planes).  Groups of 32 or 64 with uniform levels: the tcgen05 kernels of decode_tc.cu
+// (one accumulator column pair per group); with a codebook: the CUDA-core kernels of decode.cu.
+enum class Path { TC, V1, CORE };
+static Path decode_path(const PoolArgs &a) {
+  if (a.g == OSCAR_HEAD_DIM) return Path::V1;
+  return (a.cb_k == nullptr && a.cb_v == nullptr) ? Path::TC : Path::CORE;
+}
+
+static size_t ws_need(const PoolArgs &a, int num_splits) {
+  switch (decode_path(a)) {
+    case Path::TC: return tc_ws_bytes(a);
+    case Path::V1: return v1_ws_bytes(a);
+    default: return decode_ws_bytes(a, num_splits == 0 ? auto_splits(a) : num_splits);
+  }
+}
 
 oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_splits, size_t *bytes) {
   PoolArgs a;
@@ -321,12 +335,7 @@ oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_s
   if (st != OSCAR_OK) return st;
   if (bytes == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "bytes is NULL");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
-  if (tensor_core_path(a)) {
-    *bytes = v1_ws_bytes(a);
-  } else {
-    const int s = num_splits == 0 ? auto_splits(a) : num_splits;
-    *bytes = decode_ws_bytes(a, s);
-  }
+  *bytes = ws_need(a, num_splits);
   return OSCAR_OK;
 }
 
@@ -338,18 +347,21 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
-  if (tensor_core_path(a)) {
-    const size_t need = v1_ws_bytes(a);
-    if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
-    if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
-    return cuda_status(launch_decode_v1(a, q, out, softmax_scale, static_cast<float *>(ws), static_cast<cudaStream_t>(stream)),
-                       "decode_attention");
-  }
-  const int s = num_splits == 0 ? auto_splits(a) : num_splits;
-  const size_t need = decode_ws_bytes(a, s);
+  const Path path = decode_path(a);
+  const size_t need = ws_need(a, num_splits);
   if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
-  return cuda_status(launch_decode(a, q, out, softmax_scale, s, static_cast<float *>(ws), static_cast<cudaStream_t>(stream)),
-                     "decode_attention");
+  if (path != Path::CORE && (reinterpret_cast<uintptr_t>(q) & 15u))
+    return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "ws must be 16-byte aligned");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float *w = static_cast<float *>(ws);
+  switch (path) {
+    case Path::TC: return cuda_status(launch_decode_tc(a, q, out, softmax_scale, w, s), "decode_attention");
+    case Path::V1: return cuda_status(launch_decode_v1(a, q, out, softmax_scale, w, s), "decode_attention");
+    default:
+      return cuda_status(launch_decode(a, q, out, softmax_scale, num_splits == 0 ? auto_splits(a) : num_splits, w, s),
+                         "decode_attention");
+  }
 }
 
 oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
@@ -363,15 +375,20 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
     return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
-  if (!tensor_core_path(a)) {
+  const Path path = decode_path(a);
+  if (path == Path::CORE) {
     if ((st = oscar_append_kv(pool, k_new, v_new, stream)) != OSCAR_OK) return st;
     return oscar_decode_attention(pool, q, out, softmax_scale, 0, ws, ws_bytes, stream);
   }
-  const size_t need = v1_ws_bytes(a);
+  const size_t need = ws_need(a, 0);
   if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
-  return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws),
-                                    static_cast<cudaStream_t>(stream)),
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "ws must be 16-byte aligned");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == Path::TC)
+    return cuda_status(launch_decode_tc(a, q, out, softmax_scale, static_cast<float *>(ws), s, k_new, v_new),
+                       "decode_step");
+  return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws), s),
                      "decode_step");
 }
 

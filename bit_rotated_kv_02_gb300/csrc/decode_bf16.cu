@@ -560,18 +560,17 @@ __global__ void __launch_bounds__(256) prefill_kernel(CacheArgs c, int seq, int 
 // ---------------------------------------------------------------------------------------------
 template <int G>
 static int bf_resident_ctas() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, sms = 148, occ = 1;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  static std::atomic<int> slots[kMaxDevices];
+  return per_device(slots, [](int dev) {
+    int sms = 148, occ = 1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaFuncSetAttribute(bf::attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, bf::smem_bytes<G>());
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bf::attn_kernel<G>, bf::THREADS, bf::smem_bytes<G>()) !=
             cudaSuccess ||
         occ < 1)
       occ = 1;
-    cached = sms * occ;
-  }
-  return cached;
+    return sms * occ;
+  });
 }
 
 int bf16_attn_ctas(const CacheArgs &c) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "oscar_internal.cuh"
 
 namespace oscar {
@@ -24,6 +26,22 @@ inline void profile_end(int which, cudaStream_t s) {
   ProfileSlot &p = profile_slot(which);
   if (p.stop) cudaEventRecord(p.stop, s);
   p.start = p.stop = nullptr;
+}
+
+// A value computed once per device (SM count x resident CTAs of a kernel) and kept for the process:
+// `slots` holds one entry per device index (0 = not yet computed); `compute` runs with that device
+// current.  Concurrent first calls from several host threads compute the same value; the store is atomic.
+constexpr int kMaxDevices = 64;
+template <class F>
+int per_device(std::atomic<int> (&slots)[kMaxDevices], F compute) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return compute(dev);
+  int v = slots[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    v = compute(dev);
+    slots[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
 }
 
 // Sets the calling thread's oscar_last_error_string() (api.cu).
@@ -78,6 +96,19 @@ cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, f
 // performs the demotion and the append.
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
                            float *out, float sm_scale, float *ws, cudaStream_t s);
+
+// The merge kernel of decode_v1.cu (LSE merge, o . R_v^T, normalisation; k_new != NULL: the decode-step form
+// with the append and the counter update) over partial slots in its layout.
+cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
+                            const uint16_t *v_new, cudaStream_t s);
+
+// decode_tc.cu (tcgen05 path, uniform levels, group sizes 32, 64, 128): history CTAs (one per SM), workspace
+// bytes, and the launch (query rotation + operand images, history, BF16 + demotion, merge); k_new != NULL:
+// the decode-step form.
+int tc_hist_ctas(const PoolArgs &p);
+size_t tc_ws_bytes(const PoolArgs &p);
+cudaError_t launch_decode_tc(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
+                             cudaStream_t s, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr);
 
 // quant_tc.cu: cuTensorMapEncodeTiled from the driver (nullptr if the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

@@ -5,6 +5,9 @@
 // queries and split-K partials) comes from the file-scope array below instead of from the caller.
 #include <cstdio>
 #include <mutex>
+#include <utility>
+
+#include <cuda.h>
 
 #include "oscar_internal.cuh"
 #include "kernels.h"
@@ -16,8 +19,39 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[OSCAR_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
+// The looked-up address per device, with the identifier of the context it belongs to: a device reset
+// (cudaDeviceReset) ends the context and the array gets a new address in the next one, so the address
+// is looked up again whenever the current context is not the one it was found in.
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;
+  void *addr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mutex;
+
+// Identifier of the calling thread's current CUDA context (driver entry points cuCtxGetCurrent and
+// cuCtxGetId, looked up once); 0 if the driver does not provide them.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  using GetId = CUresult (*)(CUcontext, unsigned long long *);
+  static const std::pair<GetCurrent, GetId> fns = [] {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess)
+      a = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      b = nullptr;
+    return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+  }();
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.first == nullptr || fns.second == nullptr || fns.first(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      fns.second(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 }  // namespace
 
@@ -49,17 +83,23 @@ extern "C" oscar_status_t oscar_decode_attention_noalloc(const oscar_pool *pool,
   }
   void *scratch = nullptr;
   {
+    // (the size query above has already made the runtime create the device's context)
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {  // set-up, once per device, with that device current
-      e = cudaGetSymbolAddress(&g_scratch_addr[dev], g_noalloc_scratch);
+    ScratchAddr &slot = g_scratch_addr[dev];
+    if (slot.addr == nullptr || slot.ctx_id != ctx) {  // set-up, once per device (and context), device current
+      void *addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
       if (e != cudaSuccess) {
-        g_scratch_addr[dev] = nullptr;
+        slot = ScratchAddr{};
         snprintf(msg, sizeof msg, "decode_attention_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
         oscar::set_last_error(msg);
         return OSCAR_ERR_CUDA;
       }
+      slot.addr = addr;
+      slot.ctx_id = ctx;
     }
-    scratch = g_scratch_addr[dev];
+    scratch = slot.addr;
   }
   return oscar_decode_attention(pool, q, out, softmax_scale, 0, scratch, OSCAR_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -35,6 +35,15 @@ struct PoolArgs {
   const float *cb_k, *cb_v;  // [Hkv][4] codebook levels, or nullptr for the uniform levels 0, 1, 2, 3
 };
 
+// Device-side bounds checks of the debug build (compiled with -DOSCAR_DEBUG into liboscar_debug.so): a failed
+// check ORs OSCAR_DEVERR_DEBUG_CHECK into the error word and the caller skips the access; the release build
+// compiles them away.  They never trap: the context stays usable and the host reads the error word.
+#ifdef OSCAR_DEBUG
+#define OSCAR_DCHECK(cond, errp) ((cond) ? true : (atomicOr((errp), OSCAR_DEVERR_DEBUG_CHECK), false))
+#else
+#define OSCAR_DCHECK(cond, errp) true
+#endif
+
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
 

@@ -1,0 +1,96 @@
+// Split of the history over the history CTAs of a decode launch: the flattened (sequence, KV head, page)
+// space is cut into equal contiguous ranges, chunk = ceil(total / n_hist), CTA i taking [i chunk, (i+1) chunk).
+// The merge kernel locates a segment's partial slots with the same arithmetic.
+#pragma once
+
+#include "oscar_internal.cuh"
+
+namespace oscar {
+namespace split {
+
+__device__ __forceinline__ int npages_of(const PoolArgs &p, int b) {
+  int hl = p.hist_len[b];
+  hl = max(0, min(hl, p.max_pages * PAGE));
+  return (hl + PAGE - 1) / PAGE;
+}
+
+// Map a flattened page index to (b, kvh, local page) by a warp-cooperative scan over sequences.
+// Run by one full warp; results valid in every lane.  total receives the number of pages.
+static __device__ void locate(const PoolArgs &p, long long start, int &b0, int &kvh0, int &local0, long long &total) {
+  const int lane = threadIdx.x & 31;
+  long long run = 0;
+  b0 = -1; kvh0 = 0; local0 = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int b = base + lane;
+    const long long v = (b < p.B) ? (long long)npages_of(p, b) * p.Hkv : 0;
+    long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const long long excl = run + inc - v;
+    const unsigned hit = __ballot_sync(FULL, b < p.B && v > 0 && start >= excl && start < excl + v);
+    if (b0 < 0 && hit) {
+      const int src = __ffs(hit) - 1;
+      const long long e = __shfl_sync(FULL, excl, src);
+      const int bb = base + src;
+      const int np = npages_of(p, bb);
+      b0 = bb;
+      kvh0 = (int)((start - e) / np);
+      local0 = (int)((start - e) % np);
+    }
+    run += __shfl_sync(FULL, inc, 31);
+  }
+  total = run;
+}
+
+// This CTA's share of the flattened (sequence, KV head, page) space: pages [lo, lo + n) with
+// chunk = ceil(total / n_hist), lo = cta * chunk, and the position (b0, kvh0, local0) of page lo plus
+// the page count np0 and history length hl0 of sequence b0.  Run by one full warp; results valid in
+// every lane.  Up to 32 sequences one load of hist_len per lane serves everything.
+static __device__ void locate_range(const PoolArgs &p, int n_hist, int cta, long long &lo, long long &n, int &b0, int &kvh0,
+                             int &local0, int &np0, int &hl0) {
+  const int lane = threadIdx.x & 31;
+  b0 = 0; kvh0 = 0; local0 = 0; np0 = 0; hl0 = 0;
+  if (p.B <= 32) {
+    const int hl = lane < p.B ? max(0, min(p.hist_len[lane], p.max_pages * PAGE)) : 0;
+    const int np = (hl + PAGE - 1) / PAGE;
+    const long long v = (long long)np * p.Hkv;
+    long long inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(FULL, inc, o);
+      if (lane >= o) inc += t;
+    }
+    const long long total = __shfl_sync(FULL, inc, 31);
+    const long long chunk = (total + n_hist - 1) / n_hist;
+    lo = (long long)cta * chunk;
+    n = max(0ll, min(total, lo + chunk) - lo);
+    const long long excl = inc - v;
+    const unsigned hit = __ballot_sync(FULL, v > 0 && lo >= excl && lo < excl + v);
+    if (n > 0 && hit) {
+      const int src = __ffs(hit) - 1;
+      const long long e = __shfl_sync(FULL, excl, src);
+      np0 = __shfl_sync(FULL, np, src);
+      hl0 = __shfl_sync(FULL, hl, src);
+      b0 = src;
+      kvh0 = (int)((lo - e) / np0);
+      local0 = (int)((lo - e) % np0);
+    }
+    return;
+  }
+  long long total;
+  locate(p, 0, b0, kvh0, local0, total);  // total only
+  const long long chunk = (total + n_hist - 1) / n_hist;
+  lo = (long long)cta * chunk;
+  n = max(0ll, min(total, lo + chunk) - lo);
+  if (n > 0) {
+    locate(p, lo, b0, kvh0, local0, total);
+    np0 = npages_of(p, b0);
+    hl0 = max(0, min(p.hist_len[b0], p.max_pages * PAGE));
+  }
+}
+
+}  // namespace split
+}  // namespace oscar

@@ -56,6 +56,9 @@ typedef void *oscar_stream_t;  /* cudaStream_t */
 #define OSCAR_DEVERR_HISTORY_FULL 2u /* hist_len would exceed max_pages * 64             */
 #define OSCAR_DEVERR_COUNTERS 4u     /* sink_len/recent_start/recent_len/hist_len invalid */
 #define OSCAR_DEVERR_TIMEOUT 8u      /* an internal pipeline wait exceeded its time limit   */
+#define OSCAR_DEVERR_DEBUG_CHECK 16u /* debug build only (liboscar_debug.so, compiled with OSCAR_DEBUG):
+                                        a device-side bounds check of a workspace, partial-slot or pool
+                                        index failed; the access was skipped                 */
 
 /* Rotation construction modes for oscar_make_rotation. */
 #define OSCAR_ROT_HAAR 0        /* M = d x d standard-normal draws; U = Q of QR(M), sign-fixed */
@@ -85,6 +88,7 @@ typedef void *oscar_stream_t;  /* cudaStream_t */
  *   err                     uint32 [1]          device error word (OSCAR_DEVERR_* bits)
  *   sync                    int32 [batch]       arrival counters; zero them once before the first
  *                                               call, every call leaves them zero again
+ * Every array of the pool is 16-byte aligned (the decode kernels move pages with bulk asynchronous copies).
  * Token placement: positions 0..63 -> sink; later tokens -> recent slot
  * (recent_start + recent_len) % 256; the oldest recent token (slot recent_start) is demoted to
  * history position hist_len: page page_table[b][hist_len / 64], row hist_len % 64.
@@ -254,7 +258,7 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
  *                   to fill the GPU.  With group size 128 the library balances the history pages of
  *                   all (sequence, KV head) pairs over a GPU-filling grid itself and ignores it.
  *   ws, ws_bytes    workspace of at least oscar_decode_workspace_size() bytes (same pool shape and
- *                   num_splits)
+ *                   num_splits), 16-byte aligned
  * out[b][h] = sum over all pool tokens of softmax(score) * value, with score = q·k*scale for sink
  * and recent tokens and (q·R_k)·k_rot*scale for history tokens, whose values enter as v_rot·R_v^T.
  */
@@ -302,7 +306,9 @@ oscar_status_t oscar_profile_events(int32_t which, void *start, void *stop);
  *   - Pools whose decode workspace (oscar_decode_workspace_size with num_splits 0) exceeds
  *     OSCAR_NOALLOC_SCRATCH_BYTES are rejected with OSCAR_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks the array's device address up (cudaGetSymbolAddress) with
- *     that device current; make that first call before starting any stream capture.
+ *     that device current; make that first call before starting any stream capture.  A device reset
+ *     (cudaDeviceReset) ends the context the address belongs to: the first call in the new context looks
+ *     it up again (the calls key the address by the current context's identifier).
  *   - All calls share the one array, and each call writes every scratch word it later reads, so
  *     nothing needs clearing; but two calls whose kernels overlap on the GPU (different streams, or
  *     different host threads) race on it.  Order such calls on one stream.

@@ -141,3 +141,13 @@ def test_codebook_validation(lib):
     assert lib.oscar_lloyd_max_codebook(10, 2, 128, 128, FAKE, FAKE, FAKE, -1, FAKE, FAKE, 10240, None) == 1
     assert lib.oscar_lloyd_max_codebook(10, 2, 64, 128, FAKE, FAKE, FAKE, 200, FAKE, FAKE, 10240, None) == 2
     assert lib.oscar_lloyd_max_codebook(10, 2, 128, 128, FAKE, FAKE, FAKE, 200, None, FAKE, 10240, None) == 1
+
+
+def test_debug_build_is_a_separate_library_with_the_checks_compiled_in():
+    """The debug build compiles the same sources with OSCAR_DEBUG into liboscar_debug.so; the binding loads it
+    only when the environment asks for it (OSCAR_DEBUG=1)."""
+    from bit_rotated_kv_02_gb300 import build
+    assert "-DOSCAR_DEBUG" in build.DEBUG_FLAGS
+    assert build.LIB_DEBUG != build.LIB and build.LIB_DEBUG.endswith("liboscar_debug.so")
+    src = open(build.os.path.join(build.CSRC, "oscar_internal.cuh")).read()
+    assert "#ifdef OSCAR_DEBUG" in src and "OSCAR_DEVERR_DEBUG_CHECK" in src and "__trap" not in src
