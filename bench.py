@@ -30,6 +30,11 @@ sys.path.insert(0, ROOT)
 L_CTX, HQ, HKV, D, GROUP, CLIP = 100_000, 32, 8, 128, 128, 0.9
 SINK, RECENT, PAGE = 64, 256, 64
 CALIB_T = 4096
+ATTN_KERNEL = "v1::attn_kernel (INT2 history + BF16 sink/recent CTAs)"
+ATTN_KERNEL_KEY = "v1::attn_kernel"
+ATTN_SRC = os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc", "decode_v1.cu")
+# the BF16 sink/window bytes are read by the same launch (its BF16 CTAs)
+ATTN_HAS_BF16 = True
 METRIC = "INT2-KV decode attn: KV tokens/s, HBM GB/s as frac of GB300 peak; demote tok/s"
 WORKLOAD = "qwen3-8b-layer decode, 100k context (64 sink + 99,680 INT2 history + 256 recent), batch 1"
 
@@ -50,49 +55,85 @@ def parse():
                     default="decode100k",
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-cores", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--roofline-launches", type=int, default=64,
+                    help="attention launches timed one by one with CUDA events after the run")
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------------------------------------
-# Oracle CPU baseline (the only place besides --impl reference that runs oracle/): one decode step
-# of KV head 0 (its 4 query heads), i.e. 1/8 of the layer's step, repeated within a time budget.
-def cpu_baseline_child(budget_s: float) -> dict:
+# Oracle CPU baseline (the only place besides --impl reference that runs oracle/): decode steps of one KV
+# head (its 4 query heads), i.e. 1/8 of the layer's step each, within a time budget.  On all cores every
+# process runs the same sample on its own copy (processes started with spawn, one thread each).
+def _oracle_sample_setup():
     import numpy as np
     import synth
     from oracle import pool as opool
     from oracle import rotation as orot
     ch = synth.outlier_channels(7, 1, D, 4)
-    K = synth.outlier_kv(8, L_CTX + 64, 1, D, ch)
-    V = synth.outlier_kv(9, L_CTX + 64, 1, D, ch)
+    K = synth.outlier_kv(8, L_CTX + 512, 1, D, ch)
+    V = synth.outlier_kv(9, L_CTX + 512, 1, D, ch)
     q = synth.outlier_q(10, 1, HQ // HKV, 1, D, ch)
     R = orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(11, D)))[None]
     hist = L_CTX - SINK - RECENT
-    pages = -(-hist // PAGE) + 2
+    pages = -(-(hist + 512) // PAGE) + 2
     O = opool.Pool(1, HQ // HKV, 1, D, GROUP, pages, pages, R, R, [CLIP], [CLIP])
     O.page_table[0] = synth.shuffled_pages(12, pages)
     O.prefill(0, K[:L_CTX], V[:L_CTX])
-    n, t_total, ctx = 0, 0.0, 0
-    while t_total < budget_s and n < 64:
+    return O, K, V, q
+
+
+def oracle_sample_steps(n_steps: int, budget_s: float = 1e9):
+    """(per-step seconds, tokens attended) of up to n_steps oracle decode steps of KV head 0 at 100k
+    context (append with demotion + float64 attention), stopping once budget_s is spent."""
+    O, K, V, q = _oracle_sample_setup()
+    times, ctx = [], []
+    for n in range(min(n_steps, 512)):
         t0 = time.perf_counter()
         O.append(K[L_CTX + n][None], V[L_CTX + n][None])
         O.decode(q)
-        t_total += time.perf_counter() - t0
-        ctx += L_CTX + n + 1
-        n += 1
-    # KV tokens/s of the full layer: this sample did 1/8 of each step's work
-    return {"value": ctx / t_total / HKV, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} decode steps of KV head 0 (4 of 32 query heads, 1/8 of the layer) at 100k context, "
-                      "append with demotion + float64 attention; value scaled to the full layer",
-            "seconds": round(t_total, 3)}
+        times.append(time.perf_counter() - t0)
+        ctx.append(L_CTX + n + 1)
+        if sum(times) >= budget_s:
+            break
+    return times, ctx
 
 
-def run_cpu_baseline(budget_s: float) -> dict:
+def _oracle_worker(args):
+    budget_s, = args
+    import os as _os
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        _os.environ[k] = "1"
+    times, ctx = oracle_sample_steps(10 ** 9, budget_s)
+    return sum(times), sum(ctx)
+
+
+SAMPLE_NOTE = ("decode steps of KV head 0 (4 of 32 query heads, 1/8 of the layer) at 100k context, append with "
+               "demotion + float64 attention; KV tokens/s scaled to the full layer (x 1/8)")
+
+
+def cpu_baseline_child(budget_s: float, cores: int) -> dict:
+    if cores <= 1:
+        t, c = _oracle_worker((budget_s,))
+        return {"value": c / t / HKV, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
+                "sample": f"{SAMPLE_NOTE}; one process", "seconds": round(t, 3)}
+    import multiprocessing as mp
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_oracle_worker, [(budget_s,)] * cores)
+    # every process ran for about the budget at once: aggregate tokens over the slowest process's time
+    t = max(r[0] for r in res)
+    return {"value": sum(r[1] for r in res) / t / HKV, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{SAMPLE_NOTE}; {cores} processes of one thread each, the same sample", "seconds": round(t, 3)}
+
+
+def run_cpu_baseline(budget_s: float, cores: int = 1) -> dict:
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--cpu-seconds",
-                        str(budget_s)], capture_output=True, text=True, env=env, timeout=900)
+                        str(budget_s), "--cpu-cores", str(cores)], capture_output=True, text=True, env=env,
+                       timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
     return json.loads(r.stdout.strip().splitlines()[-1])
 
@@ -127,7 +168,7 @@ class ClockSampler:
         self.proc = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_index, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -160,24 +201,18 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_from_profiles(kernel_src: str):
-    """DRAM bytes per launch of the history kernel from the committed ncu summary, if the kernel's
-    source has not changed since that capture (else None)."""
-    path = os.path.join(ROOT, "profiles", "attn_kernel_decode100k.md")
-    if not os.path.exists(path):
+def traffic_from_profiles(kernel: str, kernel_src: str):
+    """DRAM bytes per launch of `kernel` from profiles/traffic.json (written from an ncu capture, with the
+    capture's command), if the kernel's source file has not changed since that capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))[kernel]
+    except (OSError, ValueError, KeyError):
         return None
     sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    fields = {}
-    for line in open(path):
-        if ":" in line and line.startswith("- "):
-            k, v = line[2:].split(":", 1)
-            fields[k.strip()] = v.strip().strip("`")
-    if fields.get("source_sha256_16") != sha:
+    if rec.get("source_sha256_16") != sha:
         return None
-    try:
-        return float(fields["dram_bytes_per_launch_full_workload"])
-    except (KeyError, ValueError):
-        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 # ---------------------------------------------------------------------------------------------
@@ -457,7 +492,7 @@ def quality_workload(args):
     import numpy as np
     import torch
     import synth
-    from bit_rotated_kv_02_gb300 import quality
+    import quality_harness as quality
     T, L, G = 2048, 4416, HQ // HKV
     ch = synth.outlier_channels(77, HKV, D, 4)
     Qs = synth.calib_samples(78, T + 1, HQ, D, ch, heads_per_channel_set=G, factor=4.0)
@@ -604,7 +639,7 @@ def other_workload(args):
 def main():
     args = parse()
     if args.cpu_baseline_child:
-        print(json.dumps(cpu_baseline_child(args.cpu_seconds)))
+        print(json.dumps(cpu_baseline_child(args.cpu_seconds, args.cpu_cores)))
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -612,13 +647,18 @@ def main():
 
     if args.impl == "reference":
         if rank == 0:
-            cpu = cpu_baseline_child(args.cpu_seconds)
-            val = cpu["value"]
+            # W untimed + K timed oracle steps, each one decode step of the sample (1/8 of the layer)
+            times, ctx = oracle_sample_steps(args.warmup + args.steps)
+            times, ctx = times[args.warmup:], ctx[args.warmup:]
+            sec = sum(times)
+            val = sum(ctx) / sec / HKV if sec > 0 else None
+            cpu = {"value": val, "unit": "KV tokens/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{SAMPLE_NOTE}; each step of this line is one such sample step", "seconds": round(sec, 3)}
             print(json.dumps({"impl": "reference", "metric": METRIC, "value": val, "unit": "KV tokens/s",
-                              "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-                              "ms_per_step": 1000.0 * L_CTX / val if val else None, "higher_is_better": True,
+                              "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+                              "ms_per_step": 1e3 * sec / max(len(times), 1), "higher_is_better": True,
                               "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                              "config": {"workload": WORKLOAD + " (oracle sample: KV head 0)"},
+                              "config": {"workload": WORKLOAD + " (oracle sample: KV head 0 per step)"},
                               "cpu_baseline": cpu,
                               "e2e": {"value": val, "unit": "KV tokens/s", "h2d_bytes_per_step": 0,
                                       "d2h_bytes_per_step": 0}}))
@@ -643,7 +683,7 @@ def main():
     NL = args.layers
     DEM_N = 200  # appends timed on their own after the run
     HOT_N, HOT_W = 500, 20  # the L2-hot steps (layer 0 only) after the run
-    total = args.warmup + args.steps + args.e2e_steps + DEM_N
+    total = args.warmup + args.steps + args.e2e_steps + DEM_N + max(50, args.roofline_launches)
     per_layer = -(-total // NL)
     layers = setup_layers(NL, per_layer + HOT_N + HOT_W + 8)
     dev = torch.device("cuda")
@@ -675,34 +715,26 @@ def main():
         appended[l] += 1
         return L_CTX + appended[l]      # tokens attended in this step
 
+    # nvidia-smi samples SM clocks and throttle reasons every 20 ms from before the warm-up until after the
+    # last GPU loop below: the timed region itself (steps x ~0.02-0.04 ms) is shorter than one sample
+    # interval, so the line reports the samples of the whole window of GPU work around it.
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or "0"
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    wall0 = time.time()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    # Per-kernel CUDA events bracket the attention and demote launches of every EVERY-th timed step
-    # only: an event recorded between two kernels ends their programmatic overlap, so arming them on
-    # every step would slow the step it is meant to measure.
-    EVERY = 8
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(-(-args.steps // EVERY))]
-    for e4 in evs:              # torch creates the CUDA event on first record; create them all now
-        for e in e4:
-            e.record()
-    torch.cuda.synchronize()
-    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0] or "0"
-    clocks = ClockSampler(gpu_index)
-    time.sleep(0.3)
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     tokens = 0
-    wall0 = time.time()
     t_start.record()
     for i in range(args.steps):
-        tokens += step(args.warmup + i, evs[i // EVERY] if i % EVERY == 0 else None)
+        tokens += step(args.warmup + i)
     t_stop.record()
     torch.cuda.synchronize()
-    clk = clocks.stop(wall0, time.time())
     ms = t_start.elapsed_time(t_stop)
-    hist_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms = max_over_ranks(ms)
     for P in layers:
         if P.err() != 0:
@@ -742,6 +774,23 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     dem_ms = e0.elapsed_time(e1) / DEM_N
+    # The dominant kernel on its own: CUDA events recorded on the step's stream immediately before and
+    # after the attention kernel of each of these steps (an event between two kernels ends their
+    # programmatic overlap, so these launches include the kernel's whole start-up; the layers rotate, so
+    # every launch reads its history from HBM).
+    RL = max(50, args.roofline_launches)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(RL)]
+    for e2 in evs:              # torch creates the CUDA event on first record; create them all now
+        for e in e2:
+            e.record()
+    torch.cuda.synchronize()
+    rl_tokens = 0
+    base = args.warmup + args.steps + args.e2e_steps
+    for i in range(RL):
+        rl_tokens += step(base + i, evs[i])
+    torch.cuda.synchronize()
+    hist_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    rl_hist_avg = rl_tokens / RL - SINK - RECENT
     # L2-hot: the same step on one layer again and again, so that its ~58 MB stay in the 129 MB L2
     hot_tokens = 0
 
@@ -762,17 +811,22 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     hot_ms = e0.elapsed_time(e1)
+    clk = clocks.stop(wall0, time.time())
+    clk["window"] = "warm-up, timed steps, e2e steps, demotion, roofline launches and L2-hot steps"
     for P in layers:
         if P.err() != 0:
             raise RuntimeError(f"device error flags {P.err():#x}")
 
-    # algorithmic bytes of the history kernel per launch (codes + scale/zero + page table + q)
+    # algorithmic bytes per launch of the history kernel: codes + scale/zero + page-table entries + q of the
+    # history; the step adds the BF16 sink and window (their own kernel), q, out, the new token and the
+    # demoted row
+    def hist_bytes_for(hist_tokens):
+        b = hist_tokens * HKV * 2 * (D // 4 + 4 * (D // GROUP)) + 4 * math.ceil(hist_tokens / PAGE) + HQ * D * 2
+        return b + ((SINK + RECENT) * HKV * 2 * D * 2 if ATTN_HAS_BF16 else 0)
     hist_tokens_avg = (tokens / args.steps) - SINK - RECENT
-    hist_bytes = hist_tokens_avg * HKV * 2 * (D // 4 + 4 * (D // GROUP)) + 4 * math.ceil(hist_tokens_avg / PAGE) \
-        + HQ * D * 4
-    bf16_bytes = (SINK + RECENT) * HKV * 2 * D * 2 + HQ * D * 2
-    attn_bytes = hist_bytes + bf16_bytes      # the attention launch serves both history and BF16 CTAs
-    step_bytes = hist_bytes + bf16_bytes + HQ * D * 4 + HKV * 2 * D * 2 * 3 + HKV * 2 * (D // 4 + 4)
+    step_bytes = hist_bytes_for(hist_tokens_avg) + (0 if ATTN_HAS_BF16 else (SINK + RECENT) * HKV * 2 * D * 2) \
+        + HQ * D * 4 + HKV * 2 * D * 2 * 3 + HKV * 2 * (D // 4 + 4)
+    attn_bytes = hist_bytes_for(rl_hist_avg)
     hist_mean_ms = statistics.mean(hist_ms)
     peaks = {}
     try:
@@ -784,9 +838,10 @@ def main():
     peak = peak or 6800.0
     achieved = attn_bytes / (hist_mean_ms * 1e-3) / 1e9
     value = replica_throughput(tokens, ms, world)
-    cpu = None
+    cpu = cpu_all = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.cpu_seconds)
+        cpu_all = run_cpu_baseline(args.cpu_seconds, os.cpu_count() or 1)
     if rank == 0:
         rec = {
             "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world, "steps": args.steps,
@@ -799,14 +854,14 @@ def main():
             "decode_steps_per_s": world * args.steps / (ms * 1e-3),
             "bytes_per_step": step_bytes,
             "step_gbs": step_bytes * args.steps / (ms * 1e-3) / 1e9,
-            "roofline": {"bound": "hbm", "kernel": "attn_kernel (INT2 history + BF16 sink/recent CTAs)",
+            "roofline": {"bound": "hbm", "kernel": ATTN_KERNEL,
                          "achieved": achieved, "peak": peak,
                          "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
                          "frac_of_nominal_8tbs": achieved / 8000.0,
-                         "traffic": traffic_from_profiles(os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc",
-                                                                       "decode_v1.cu")),
+                         "traffic": traffic_from_profiles(ATTN_KERNEL_KEY, ATTN_SRC),
                          "algorithmic_bytes_per_launch": attn_bytes, "mean_launch_us": hist_mean_ms * 1e3,
-                         "timed_launches": len(hist_ms), "sampling": f"every {EVERY}th step of the timed region"},
+                         "timed_launches": len(hist_ms),
+                         "sampling": "a loop of decode steps after the run, CUDA events around each attention launch"},
             "demote": {"tokens_per_s": 1.0 / (dem_ms * 1e-3), "mean_call_us": dem_ms * 1e3,
                        "note": "oscar_append_kv (demotion + append kernel), timed on its own after the run; in "
                                "the decode step the attention kernel's sink CTAs perform the demotion"},
@@ -815,9 +870,10 @@ def main():
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
                     "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
-            "gpu_launches": args.steps * 3,   # q rotation, attention (+ demotion), merge (+ append)
+            "gpu_launches": args.steps * 3,   # q rotation, attention (history + BF16 CTAs + demotion), merge
             "clocks": clk,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
         }
         print(json.dumps(rec))
     if world > 1:

@@ -1,4 +1,5 @@
-"""Attention quality of INT2 history variants, measured with the library's own kernels.
+"""Attention-quality harness (a measurement beside the benchmark, not part of the library's decode path):
+attention quality of INT2 history variants, measured with the library's own kernels.
 
 "超越TurboQuant！OSCAR：面向真实服务的2-bit KV Cache量化", section "OSCAR 的动机" (Fig. 1): naive INT2
 and Hadamard-only rotation distort the attention at two bits, OSCAR's covariance-aligned rotation
@@ -24,9 +25,9 @@ import math
 
 import torch
 
-from . import (HEAD_DIM, PAGE, RECENT, SINK, ROT_COVARIANCE, ROT_HAAR, Pool, oscar_calib_covariance_k,
-               oscar_calib_covariance_v, oscar_decode_attention, oscar_lloyd_max_codebook, oscar_make_rotation,
-               oscar_prefill_pool)
+from bit_rotated_kv_02_gb300 import (HEAD_DIM, PAGE, RECENT, SINK, ROT_COVARIANCE, ROT_HAAR, Pool,
+                                     oscar_calib_covariance_k, oscar_calib_covariance_v, oscar_decode_attention,
+                                     oscar_lloyd_max_codebook, oscar_make_rotation, oscar_prefill_pool)
 
 
 def identity_rotation(num_kv_heads: int, device="cuda") -> torch.Tensor:
