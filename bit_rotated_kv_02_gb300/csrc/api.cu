@@ -315,10 +315,19 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
 // Decode paths.  Whole-vector groups (128): the warp-MMA kernels of decode_v1.cu (uniform levels, or a
 // codebook's indicator planes).  Groups of 32 or 64 with uniform levels: the tcgen05 kernels of decode_tc.cu
 // (one accumulator column pair per group); with a codebook: the CUDA-core kernels of decode.cu.
+// OSCAR_DECODE_TC=1 in the environment sends uniform pools of group size 128 to the tcgen05 kernels as well.
 enum class Path { TC, V1, CORE };
+static bool force_tc() {
+  static const bool on = [] {
+    const char *e = getenv("OSCAR_DECODE_TC");
+    return e != nullptr && e[0] == '1' && e[1] == '\0';
+  }();
+  return on;
+}
 static Path decode_path(const PoolArgs &a) {
-  if (a.g == OSCAR_HEAD_DIM) return Path::V1;
-  return (a.cb_k == nullptr && a.cb_v == nullptr) ? Path::TC : Path::CORE;
+  const bool uniform = a.cb_k == nullptr && a.cb_v == nullptr;
+  if (a.g == OSCAR_HEAD_DIM) return (uniform && force_tc()) ? Path::TC : Path::V1;
+  return uniform ? Path::TC : Path::CORE;
 }
 
 static size_t ws_need(const PoolArgs &a, int num_splits) {

@@ -35,6 +35,8 @@
 //   o_rot[ch] = 2^(24 - 2k - tau) * (O_hi + O_lo)[ch] + sum_t p_t zero_t,g(ch),
 // with weights p * scale * 2^tau split into fp16 hi + lo (22 significant bits) and a lazily rescaled base-2
 // online softmax (the reference grows only when a score exceeds it by more than 2^LAZY).
+#include <cuda_fp8.h>
+
 #include "oscar_internal.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
@@ -46,10 +48,9 @@ namespace oscar {
 namespace tc {
 
 constexpr int TILE = 128;
-constexpr int W_PROD = 0, W_MMA = 1, W_K0 = 2, W_V0 = 6, W_S0 = 10;
+constexpr int W_PROD = 0, W_MMA = 1, W_V0 = 6, W_S0 = 10;  // K unpack warps: 2..5
 constexpr int TI = 16;        // tile-information ring
-constexpr int MR = 4;         // scale/zero ring (tiles in flight between the K unpack and the softmax)
-constexpr int NAK = 4;        // K operand buffers in tensor memory
+constexpr int MR = 4;         // scale/zero ring: tiles in flight between the K unpack and the softmax
 constexpr int LAZY = 16;      // the softmax reference grows only when a score exceeds it by more than 2^16
 constexpr int WEXP = 14 - LAZY;
 constexpr int OFF_KC = 0, OFF_VC = 2048, OFF_META = 4096;
@@ -74,17 +75,30 @@ struct Cfg {
   // one Q.K operand buffer for N = 64 (eight heads x four groups), two otherwise, and a shorter ring there
   static constexpr int BQN = N >= 64 ? 1 : 2;
   static constexpr int RING = NG == 1 ? 7 : (N >= 64 ? 4 : 5);
+  // Q.K in fp8 (kind::f8f6f4, e4m3, K = 32 per MMA) when the six digit planes of every head and group fit in
+  // N <= 128 (an MMA of N <= 128 costs the same): K codes as e4m3 subnormals, q_rot as six base-16 digits.
+  // Otherwise (eight heads x four groups) Q.K in fp16 with the hi / lo split (two columns per head and group).
+  static constexpr int QT = 6;                                          // digit planes of q_rot
+  static constexpr int NQG8 = ((GH * NG * QT + 7) / 8) * 8;
+  static constexpr bool QK8 = SG * NQG8 <= 128;
+  static constexpr int NQG = QK8 ? NQG8 : NCG;                          // S columns per softmax warpgroup
+  static constexpr int NQ = QK8 ? ((SG * NQG8 + 15) / 16) * 16 : N;     // MMA N of Q.K
+  static constexpr int AKC = QK8 ? 32 : 64;                             // TMEM columns of one K operand
   static constexpr int BQ_FACTORS = ((G + G * NG) * 4 + 15) / 16 * 16;  // kf[G], zf[G][NG]
-  static constexpr int BQ_IMG = N * 256;                                // [N][128] fp16, two atom columns
+  static constexpr int BQ_IMG = QK8 ? NQ * 128 : N * 256;               // [NQ][128] e4m3 / [N][128] fp16
   static constexpr int BQ_BYTES = BQ_IMG + BQ_FACTORS;
   static constexpr int BW_BYTES = N * 256;
-  // tensor memory columns: K operands (64 columns each), S (two tiles), O (two segments)
-  static constexpr int TM_AK = 0, TM_S = 64 * NAK, TM_O = TM_S + 2 * N;
+  // tensor memory columns: K operands and S for NSQ tiles (Q.K runs two tiles ahead of P.V), O for two segments
+  static constexpr int NSQ = 4 * (AKC + NQ) + 2 * N <= 512 ? 4 : 3;
+  static constexpr int TM_AK = 0, TM_S = AKC * NSQ, TM_O = TM_S + NSQ * NQ;
   static constexpr int TM_USED = TM_O + 2 * N;
   static constexpr int TM_COLS = TM_USED <= 256 ? 256 : 512;
-  // shared memory (the operand images at 1024-byte boundaries)
+  // shared memory (the operand images at 1024-byte boundaries); V tiles: four where they fit, else three
+  static constexpr int BQ_STRIDE0 = ((BQ_BYTES + 1023) / 1024) * 1024;
+  static constexpr int REST = BQN * BQ_STRIDE0 + 2 * BW_BYTES + RING * STAGE_BYTES + MR * TILE * 4 * META + 4096;
+  static constexpr int NAV = 4 * AV_BYTES + REST <= 227 * 1024 ? 4 : 3;
   static constexpr int OFF_AV = 0;
-  static constexpr int OFF_BQ = OFF_AV + 2 * AV_BYTES;
+  static constexpr int OFF_BQ = OFF_AV + NAV * AV_BYTES;
   static constexpr int BQ_STRIDE = ((BQ_BYTES + 1023) / 1024) * 1024;
   static constexpr int OFF_BW = OFF_BQ + BQN * BQ_STRIDE;
   static constexpr int OFF_RING = OFF_BW + 2 * BW_BYTES;
@@ -92,7 +106,7 @@ struct Cfg {
   static constexpr int MRING_TILE = TILE * 4 * META;
   static constexpr int OFF_TINFO = OFF_MRING + MR * MRING_TILE;
   static constexpr int OFF_BAR = OFF_TINFO + TI * 16;
-  static constexpr int NBAR = 2 * RING + 2 * NAK + 2 * 2 + 2 * 2 + 2 * 2 + 2 * MR;
+  static constexpr int NBAR = 2 * RING + 2 * NSQ + 2 * NAV + 2 + 2 * 2 + 2 * MR;
   static constexpr int OFF_RED = OFF_BAR + NBAR * 8;
   // softmax scratch per warpgroup: the flush's sums [4 warps][GH][NG + 1], then the tile maxima [4][GH + 1]
   static constexpr int RED_FLUSH = 4 * GH * (NG + 1);
@@ -101,7 +115,7 @@ struct Cfg {
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack to align the base to 1024
   static_assert(OFF_BQ % 1024 == 0 && OFF_BW % 1024 == 0 && BW_BYTES % 1024 == 0, "operand alignment");
   static_assert(STAGE_BYTES % 16 == 0 && OFF_RING % 16 == 0, "bulk copy alignment");
-  static_assert(TM_USED <= 512 && GH * NG * 2 <= NCG, "tensor memory and column layout");
+  static_assert(TM_USED <= 512 && GH * NG * 2 <= NCG && (!QK8 || GH * NG * QT <= NQG), "tensor memory and columns");
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 // Column (and Q.K image row) of (head h, group g, term t): warpgroup h / GH owns the block of NCG columns
@@ -132,18 +146,21 @@ struct HArgs {
 template <int G, int NG>
 struct Bars {
   uint64_t *full, *empty;          // [RING]   page stage landed / released (8 unpack warps)
-  uint64_t *ak_full, *ak_free;     // [NAK]    K codes in TMEM (4 warps) / the tile's Q.K done (MMA commit)
-  uint64_t *av_full;               // [2]      V tile in smem (4 warps)
-  uint64_t *s_full, *pv_done;      // [2]      Q.K / P.V of a tile complete (MMA commits)
+  uint64_t *ak_full, *qk_done;     // [NSQ]    K codes in TMEM (4 warps) / the tile's Q.K done: S ready and the
+                                   //          K buffer free (MMA commit)
+  uint64_t *av_full, *pv_done;     // [NAV]    V tile in smem (4 warps) / the tile's P.V done: the V tile, the
+                                   //          weight buffer and the accumulator free (MMA commit)
   uint64_t *w_full;                // [2]      weights of a tile written (4 warps per softmax warpgroup)
   uint64_t *bq_full, *bq_free;     // [2]      Q.K operand image landed / released (MMA commit + softmax warps)
   uint64_t *meta_full, *meta_free; // [MR]     scale/zero of a tile copied (4 K-unpack warps) / read (softmax)
   __device__ Bars(uint8_t *sm) {
     uint64_t *b = reinterpret_cast<uint64_t *>(sm + Cfg<G, NG>::OFF_BAR);
-    constexpr int R = Cfg<G, NG>::RING;
+    constexpr int R = Cfg<G, NG>::RING, NV = Cfg<G, NG>::NAV;
     full = b; empty = b + R;
-    ak_full = b + 2 * R; ak_free = ak_full + NAK;
-    av_full = ak_free + NAK; s_full = av_full + 2; pv_done = s_full + 2; w_full = pv_done + 2;
+    constexpr int NS = Cfg<G, NG>::NSQ;
+    ak_full = b + 2 * R; qk_done = ak_full + NS;
+    av_full = qk_done + NS; pv_done = av_full + NV;
+    w_full = pv_done + NV;
     bq_full = w_full + 2; bq_free = bq_full + 2;
     meta_full = bq_free + 2; meta_free = meta_full + MR;
   }
@@ -171,11 +188,19 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, const P
   }
   return true;
 }
-// Warp-collective bounded wait: true on every lane when the phase completed.
+// Warp-collective bounded wait: every lane polls the barrier (no divergence); true on every lane when the phase
+// completed.  A completed phase stays completed for try_wait, so the vote settles after one more poll.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const PoolArgs &p, uint32_t *misc) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p, misc);
-  return __shfl_sync(FULL, ok ? 1 : 0, 0) != 0;
+  if (__all_sync(FULL, mbar_try_wait_hint(bar, parity, 1000000u))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!__all_sync(FULL, mbar_try_wait_hint(bar, parity, 1000000u))) {
+    if (__any_sync(FULL, aborted(misc))) return false;
+    if (globaltimer_ns() - t0 > 1000000000ull) {
+      if ((threadIdx.x & 31) == 0) set_abort(p, misc);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ---- tcgen05 helpers (kind::f16, A from tensor memory or shared memory) ----
@@ -189,6 +214,11 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uin
 }
 __device__ __forceinline__ void mma_tmem_a(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+               ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+// kind::f8f6f4 with A from tensor memory (both operands e4m3: instruction-descriptor format fields 0).
+__device__ __forceinline__ void mma_tmem_a_f8(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n"
                ::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 __device__ __forceinline__ void mma_smem_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -207,6 +237,16 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
       "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]),
       "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]),
       "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
@@ -248,6 +288,19 @@ __device__ __forceinline__ void unpack_word(uint32_t x, uint32_t *r) {
 #pragma unroll
   for (int k = 0; k < 3; ++k) r[5 + k] = xs & (0x00030003u << (2 * k));
 }
+// The same word as e4m3 subnormals for the fp8 Q.K: register i (0..3) byte b holds code 4 b + i, as c * 2^-9
+// (i even: the code in the mantissa's low bits) or c * 2^-7 (i odd: two bits up, the exponent's low bit taking
+// the code's high bit: 1 -> 2^-7, 2 -> 2^-6, 3 -> 1.5 * 2^-6, linear in c).  Operand position p = 16 w + 4 i + b
+// (w the word) holds channel 16 w + 4 b + i.
+__device__ __forceinline__ void unpack_word_f8(uint32_t x, uint32_t *r) {
+  r[0] = x & 0x03030303u;
+  r[1] = x & 0x0C0C0C0Cu;
+  const uint32_t xs = x >> 4;
+  r[2] = xs & 0x03030303u;
+  r[3] = xs & 0x0C0C0C0Cu;
+}
+__host__ __device__ __forceinline__ int pos8_channel(int p) { return (p & ~15) + 4 * (p & 3) + ((p & 15) >> 2); }
+__host__ __device__ __forceinline__ bool pos8_low(int p) { return ((p >> 2) & 1) == 0; }  // code factor 2^-9
 __host__ __device__ __forceinline__ int pos_channel(int p) { return (p & ~15) + ((p & 15) >> 1) + 8 * (p & 1); }
 __host__ __device__ __forceinline__ int pos_k(int p) {
   const int k = (p & 15) >> 1;
@@ -276,11 +329,12 @@ __global__ void __launch_bounds__(256) qrot_kernel(PoolArgs p, const uint16_t *q
   __shared__ int s_sig[G];
   const int s = blockIdx.x, b = s / p.Hkv, kvh = s % p.Hkv;
   const int tid = threadIdx.x, c = tid & (D - 1), half = tid >> 7;
-  // thread (c, half) sums rows 64 half .. 64 half + 63 of column c, 16 rows per batch of loads
+  // thread (c, half) sums rows 64 half .. 64 half + 63 of column c; all 64 loads are issued at once, before
+  // the wait for the previous kernel (R_k is not written by the decode)
   const float *R = p.R_k + (size_t)kvh * D * D + (size_t)(64 * half) * D + c;
-  float r[16];
+  float r[64];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) r[i] = R[(size_t)i * D];
+  for (int i = 0; i < 64; ++i) r[i] = R[(size_t)i * D];
   for (int i = tid; i < G * D; i += 256) qs[i / D][i % D] = bf16_to_f32(q[((size_t)b * p.Hq + kvh * G) * D + i]);
   pdl_wait();
   pdl_trigger();
@@ -289,21 +343,9 @@ __global__ void __launch_bounds__(256) qrot_kernel(PoolArgs p, const uint16_t *q
 #pragma unroll
   for (int h = 0; h < G; ++h) acc[h] = 0.f;
 #pragma unroll
-  for (int bt = 0; bt < 4; ++bt) {
-    float rn[16];
-    if (bt < 3) {
+  for (int i = 0; i < 64; ++i)
 #pragma unroll
-      for (int i = 0; i < 16; ++i) rn[i] = R[(size_t)(16 * (bt + 1) + i) * D];
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-#pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][64 * half + 16 * bt + i], r[i], acc[h]);
-    if (bt < 3) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) r[i] = rn[i];
-    }
-  }
+    for (int h = 0; h < G; ++h) acc[h] = fmaf(qs[h][64 * half + i], r[i], acc[h]);
 #pragma unroll
   for (int h = 0; h < G; ++h) part2[half][h][c] = acc[h];
   __syncthreads();
@@ -341,36 +383,72 @@ __global__ void __launch_bounds__(256) qrot_kernel(PoolArgs p, const uint16_t *q
       if (amax > 0.f) frexpf(amax, &e);
       const int sig = (amax > 0.f) ? 14 - e : 0;  // amax * 2^sig < 2^14
       s_sig[h] = sig;
-      fac[h] = pow2i(24 - sig) * sm_log2;
+      // score factor: sum_c code_c q_rot_c = 2^(24 - sigma) (S_hi + S_lo) (fp16 split), or 2^(-2 - sigma)
+      // sum_t 16^t S_t (fp8 digits)
+      fac[h] = pow2i(C::QK8 ? -2 - sig : 24 - sig) * sm_log2;
 #pragma unroll
       for (int g = 0; g < NG; ++g) fac[G + h * NG + g] = gs[g] * sm_log2;
     }
   }
   __syncthreads();
-  // the image: N rows x 128 positions, two 16-bit values per thread-step
-  for (int i = tid; i < C::N * (D / 2); i += 256) {
-    const int n = i / (D / 2), p2 = 2 * (i % (D / 2));
-    uint32_t word = 0;
-    const int sgi = n / C::NCG, loc = n % C::NCG;  // row n = col_of(h, g, term)
-    if (loc < C::GH * NG * 2) {
-      const int h = sgi * C::GH + loc / (2 * NG), g = (loc / 2) % NG, term = loc & 1;
-      const float s2 = pow2i(s_sig[h]);
-      float v[2];
+  if constexpr (C::QK8) {
+    // the fp8 image: NQ rows x 128 e4m3 (one 128-byte-swizzled atom column); row sg * NQG + (hl * NG + g) * 6 + t
+    // holds digit t of Y = rint(q_rot[h][ch] * 2^sigma * 2^9) (|Y| < 2^23) in balanced base 16,
+    // Y = sum_t 16^t d_t with |d_t| <= 8, times 4 where the code of position p sits two bits lower
+    // (code factor 2^-9 instead of 2^-7): every product is c * d * 2^-7 and a column's 128 sum exactly.
+    for (int i = tid; i < C::NQ * (D / 4); i += 256) {
+      const int n = i / (D / 4), p4 = 4 * (i % (D / 4));
+      const int sgi = n / C::NQG, loc = n % C::NQG;
+      uint32_t word = 0;
+      if (sgi < C::SG && loc < C::GH * NG * C::QT) {
+        const int h = sgi * C::GH + loc / (NG * C::QT), g = (loc / C::QT) % NG, t = loc % C::QT;
+        const float s2 = pow2i(s_sig[h] + 9);
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int pp = p2 + e, ch = pos_channel(pp);
-        float t = 0.f;
-        if (ch / (D / NG) == g) {
-          const float y = qs[h][ch] * s2;  // exact: s2 is a power of two
-          const float hi = 8.f * rintf(y * 0.125f);
-          const float lo = rintf((y - hi) * 256.f) * (1.f / 256.f);
-          t = (term == 0 ? hi : lo) * pow2i(-2 * pos_k(pp));
+        for (int e = 0; e < 4; ++e) {
+          const int pp = p4 + e, ch = pos8_channel(pp);
+          float dv = 0.f;
+          if (ch / (D / NG) == g) {
+            int Y = __float2int_rn(qs[h][ch] * s2);
+            int d = 0;
+            for (int k = 0; k <= t; ++k) {
+              d = (k == C::QT - 1) ? Y : ((Y + 8) & 15) - 8;
+              Y = (Y - d) >> 4;  // exact: Y - d is a multiple of 16
+            }
+            dv = (float)(pos8_low(pp) ? 4 * d : d);
+          }
+          const __nv_fp8_e4m3 f8(dv);  // exact: |dv| <= 32 with at most four significant bits
+          word |= (uint32_t)f8.__x << (8 * e);
         }
-        v[e] = t;
       }
-      word = pack_half2(v[0], v[1]);
+      *reinterpret_cast<uint32_t *>(img + (n >> 3) * 1024 + (n & 7) * 128 + ((((p4 >> 4) ^ (n & 7))) << 4) +
+                                    (p4 & 15)) = word;
     }
-    *reinterpret_cast<uint32_t *>(img + op_offset(C::N, n, p2)) = word;
+  } else {
+    // the fp16 image: N rows x 128 positions, two 16-bit values per thread-step
+    for (int i = tid; i < C::N * (D / 2); i += 256) {
+      const int n = i / (D / 2), p2 = 2 * (i % (D / 2));
+      uint32_t word = 0;
+      const int sgi = n / C::NCG, loc = n % C::NCG;  // row n = col_of(h, g, term)
+      if (loc < C::GH * NG * 2) {
+        const int h = sgi * C::GH + loc / (2 * NG), g = (loc / 2) % NG, term = loc & 1;
+        const float s2 = pow2i(s_sig[h]);
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int pp = p2 + e, ch = pos_channel(pp);
+          float t = 0.f;
+          if (ch / (D / NG) == g) {
+            const float y = qs[h][ch] * s2;  // exact: s2 is a power of two
+            const float hi = 8.f * rintf(y * 0.125f);
+            const float lo = rintf((y - hi) * 256.f) * (1.f / 256.f);
+            t = (term == 0 ? hi : lo) * pow2i(-2 * pos_k(pp));
+          }
+          v[e] = t;
+        }
+        word = pack_half2(v[0], v[1]);
+      }
+      *reinterpret_cast<uint32_t *>(img + op_offset(C::N, n, p2)) = word;
+    }
   }
 }
 
@@ -408,14 +486,13 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
   __shared__ int s_b0, s_kvh0, s_local0, s_np0, s_hl0;
   if (tid == 0) {
     for (int i = 0; i < C::RING; ++i) { mbar_init(bar.full + i, 1); mbar_init(bar.empty + i, 8); }
-    for (int i = 0; i < NAK; ++i) { mbar_init(bar.ak_full + i, 4); mbar_init(bar.ak_free + i, 1); }
+    for (int i = 0; i < C::NSQ; ++i) { mbar_init(bar.ak_full + i, 4); mbar_init(bar.qk_done + i, 1); }
+    for (int i = 0; i < C::NAV; ++i) { mbar_init(bar.av_full + i, 4); mbar_init(bar.pv_done + i, 1); }
+    for (int i = 0; i < MR; ++i) { mbar_init(bar.meta_full + i, 4); mbar_init(bar.meta_free + i, 4 * C::SG); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar.av_full + i, 4);
-      mbar_init(bar.s_full + i, 1); mbar_init(bar.pv_done + i, 1);
       mbar_init(bar.w_full + i, 4 * C::SG);
       mbar_init(bar.bq_full + i, 1); mbar_init(bar.bq_free + i, 1 + 4 * C::SG);
     }
-    for (int i = 0; i < MR; ++i) { mbar_init(bar.meta_full + i, 4); mbar_init(bar.meta_free + i, 4 * C::SG); }
     misc[M_ABORT] = 0;
     mbar_fence_init();
   }
@@ -553,69 +630,70 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
       }
     } else if (warp == W_MMA) {
       // ---------------- MMA issuer (one thread) ----------------
+      // Q.K runs up to two tiles ahead of P.V (NSQ >= 3 S and K buffers), so that the tensor pipe has work
+      // queued while the softmax of the current tile runs.  One commit per Q.K (qk_done: S ready, K buffer
+      // free) and one per P.V (pv_done: V tile, weight buffer and accumulator released).
       if (lane == 0) {
-        constexpr uint32_t ID_QK = idesc_f16(TILE, C::N, false), ID_PV = idesc_f16(TILE, C::N, true);
-        int sigma = -1, j = 0;
-        bool ok = true;
-        auto qk = [&](int t, int sig) {
-          const uint32_t bq = smem_u32(sm.bq(sig % C::BQN));
+        // the e4m3 formats of kind::f8f6f4 and the f16 formats of kind::f16 share the descriptor value 0
+        constexpr uint32_t ID_QK = idesc_f16(TILE, C::NQ, false), ID_PV = idesc_f16(TILE, C::N, true);
+        constexpr int NS = C::NSQ;
+        int sigma = -1, nq = 0, j = 0;
+        int sig_of[NS];
+        bool first_of[NS];
+        bool more = true, ok = true;
+        // issue Q.K of tile nq (its K codes in tensor memory; its segment's operand image in smem)
+        auto issue_qk = [&]() -> bool {
+          const int t = nq;
+          if (!wait_bar(bar.ak_full + (t % NS), (t / NS) & 1, p, misc)) return false;
+          tc_fence_after();
+          const TileInfo ti = *sm.tinfo(t);
+          if (ti.flags & F_FIRST) {
+            if (sigma >= 0) umma_commit(bar.bq_free + (sigma % C::BQN));  // segment sigma's last Q.K is issued
+            ++sigma;
+            if (!wait_bar(bar.bq_full + (sigma % C::BQN), (sigma / C::BQN) & 1, p, misc)) return false;
+            tc_fence_after();
+          }
+          sig_of[t % NS] = sigma;
+          first_of[t % NS] = (ti.flags & F_FIRST) != 0;
+          const uint32_t bq = smem_u32(sm.bq(sigma % C::BQN));
+          const uint32_t d = tmem + C::TM_S + C::NQ * (t % NS), a = tmem + C::TM_AK + C::AKC * (t % NS);
+          if constexpr (C::QK8) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_tmem_a(tmem + C::TM_S + C::N * (t & 1), tmem + C::TM_AK + 64 * (t % NAK) + 8 * kk,
-                       desc_sw128(bq + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024), ID_QK, kk > 0 ? 1u : 0u);
-          umma_commit(bar.s_full + (t & 1));
-          umma_commit(bar.ak_free + (t % NAK));
+            for (int kk = 0; kk < 4; ++kk)  // K = 32 e4m3 per MMA: 32 bytes of the operand rows
+              mma_tmem_a_f8(d, a + 8 * kk, desc_sw128(bq + kk * 32, 16, 1024), ID_QK, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_tmem_a(d, a + 8 * kk, desc_sw128(bq + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024), ID_QK,
+                         kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bar.qk_done + (t % NS));
+          if (ti.flags & F_LAST) more = false;
+          ++nq;
+          return true;
         };
-        // tile 0
-        ok = wait_bar(bar.ak_full, 0, p, misc);
-        TileInfo cur{};
-        if (ok) {
-          tc_fence_after();
-          cur = *sm.tinfo(0);
-          sigma = 0;
-          ok = wait_bar(bar.bq_full, 0, p, misc);  // segment 0
-          if (ok) {
-            tc_fence_after();
-            qk(0, 0);
-          }
-        }
-        int sig_cur = 0;
+        ok = issue_qk();
+        if (ok && more) ok = issue_qk();
         while (ok) {
-          TileInfo nxt{};
-          int sig_nxt = sig_cur;
-          if (!(cur.flags & F_LAST)) {
-            const int t1 = j + 1;
-            if (!wait_bar(bar.ak_full + (t1 % NAK), (t1 / NAK) & 1, p, misc)) break;
-            tc_fence_after();
-            nxt = *sm.tinfo(t1);
-            if (nxt.flags & F_FIRST) {
-              umma_commit(bar.bq_free + (sigma % C::BQN));  // the last Q.K of segment sigma has been issued
-              ++sigma;
-              sig_nxt = sigma;
-              if (!wait_bar(bar.bq_full + (sigma % C::BQN), (sigma / C::BQN) & 1, p, misc)) break;
-              tc_fence_after();
-            }
-            qk(t1, sig_nxt);
-          }
+          if (more && !issue_qk()) break;  // tile j + 2
           if (!wait_bar(bar.w_full + (j & 1), (j >> 1) & 1, p, misc)) break;
-          if (!wait_bar(bar.av_full + (j & 1), (j >> 1) & 1, p, misc)) break;
+          if (!wait_bar(bar.av_full + (j % C::NAV), (j / C::NAV) & 1, p, misc)) break;
           tc_fence_after();
-          const uint32_t av = smem_u32(sm.av(j & 1)), bw = smem_u32(sm.bw(j & 1));
-          const uint32_t first = (cur.flags & F_FIRST) ? 1u : 0u;
+          const uint32_t av = smem_u32(sm.av(j % C::NAV)), bw = smem_u32(sm.bw(j & 1));
+          const uint32_t o = tmem + C::TM_O + C::N * (sig_of[j % NS] & 1);
+          const bool first = first_of[j % NS];
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_smem_a(tmem + C::TM_O + C::N * (sig_cur & 1), desc_sw128(av + 2048 * kk, 16384, 1024),
+            mma_smem_a(o, desc_sw128(av + 2048 * kk, 16384, 1024),
                        desc_sw128(bw + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024), ID_PV,
                        (kk > 0 || !first) ? 1u : 0u);
-          umma_commit(bar.pv_done + (j & 1));
-          if (cur.flags & F_LAST) break;
-          cur = nxt;
-          sig_cur = sig_nxt;
+          umma_commit(bar.pv_done + (j % C::NAV));
+          if (!more && j == nq - 1) break;  // that was the CTA's last tile
           ++j;
         }
         // every MMA this thread issued completes before tensor memory is freed
         umma_commit(bar.bq_free + (max(sigma, 0) % C::BQN));
-        mbar_wait_bounded(bar.pv_done + (j & 1), (uint32_t)((j >> 1) & 1), 100000000ull);
+        mbar_wait_bounded(bar.pv_done + (j % C::NAV), (uint32_t)((j / C::NAV) & 1), 100000000ull);
       }
     } else if (warp < W_V0) {
       // ---------------- K codes -> tensor memory (A of Q.K); scale/zero -> the meta ring ----------------
@@ -625,36 +703,45 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         const int stage = j % C::RING;
         if (!warp_wait(bar.full + stage, (j / C::RING) & 1, p, misc)) break;
         const TileInfo ti = *sm.tinfo(j);
-        // the K operand buffer and the meta-ring slot of tile j - NAK / j - MR are free
-        if (j >= NAK && !warp_wait(bar.ak_free + (j % NAK), ((j / NAK) - 1) & 1, p, misc)) break;
+        // the K operand buffer of tile j - NSQ and the meta-ring slot of tile j - MR are free
+        if (j >= C::NSQ && !warp_wait(bar.qk_done + (j % C::NSQ), ((j / C::NSQ) - 1) & 1, p, misc)) break;
         if (j >= MR && !warp_wait(bar.meta_free + (j % MR), ((j / MR) - 1) & 1, p, misc)) break;
         const uint8_t *pg = sm.stage(stage) + slot * C::PAGE_BYTES;
         const uint4 c0 = *reinterpret_cast<const uint4 *>(pg + OFF_KC + row * 32);
         const uint4 c1 = *reinterpret_cast<const uint4 *>(pg + OFF_KC + row * 32 + 16);
-        uint32_t r[64];
         const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) unpack_word(w[i], r + 8 * i);
         tc_fence_after();
-        tmem_st64(tmem + lane_addr + C::TM_AK + 64 * (j % NAK), r);
-        // scale/zero of the token: Ks, Kz, Vs, Vz (NG bf16 each) -> one record of the meta ring
-        uint8_t *mr = sm.mring(j % MR) + t * 4 * C::META;
-        const uint8_t *mp = pg + OFF_META + row * C::META;
+        if constexpr (C::QK8) {
+          uint32_t r[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if constexpr (NG == 1) {
-            *reinterpret_cast<uint16_t *>(mr + 2 * q) = *reinterpret_cast<const uint16_t *>(mp + q * PAGE * C::META);
-          } else if constexpr (NG == 2) {
-            *reinterpret_cast<uint32_t *>(mr + 4 * q) = *reinterpret_cast<const uint32_t *>(mp + q * PAGE * C::META);
-          } else {
-            *reinterpret_cast<uint2 *>(mr + 8 * q) = *reinterpret_cast<const uint2 *>(mp + q * PAGE * C::META);
+          for (int i = 0; i < 8; ++i) unpack_word_f8(w[i], r + 4 * i);
+          tmem_st32(tmem + lane_addr + C::TM_AK + C::AKC * (j % C::NSQ), r);
+        } else {
+          uint32_t r[64];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) unpack_word(w[i], r + 8 * i);
+          tmem_st64(tmem + lane_addr + C::TM_AK + C::AKC * (j % C::NSQ), r);
+        }
+        // scale/zero of the token: Ks, Kz, Vs, Vz (NG bf16 each) -> one record of the meta ring
+        {
+          uint8_t *mr = sm.mring(j % MR) + t * 4 * C::META;
+          const uint8_t *mp = pg + OFF_META + row * C::META;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if constexpr (NG == 1) {
+              *reinterpret_cast<uint16_t *>(mr + 2 * q) = *reinterpret_cast<const uint16_t *>(mp + q * PAGE * C::META);
+            } else if constexpr (NG == 2) {
+              *reinterpret_cast<uint32_t *>(mr + 4 * q) = *reinterpret_cast<const uint32_t *>(mp + q * PAGE * C::META);
+            } else {
+              *reinterpret_cast<uint2 *>(mr + 8 * q) = *reinterpret_cast<const uint2 *>(mp + q * PAGE * C::META);
+            }
           }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar.ak_full + (j % NAK));
+          mbar_arrive(bar.ak_full + (j % C::NSQ));
           mbar_arrive(bar.meta_full + (j % MR));
           mbar_arrive(bar.empty + stage);
         }
@@ -663,16 +750,20 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
     } else if (warp < W_S0) {
       // ---------------- V codes -> the swizzled shared-memory tile (A of P.V, MN-major) ----------------
       const int t = 32 * (warp - W_V0) + lane, slot = t >> 6, row = t & 63;
+      uint32_t choff[8];  // swizzled 16-byte chunk c of the token's 128-byte atom row
+#pragma unroll
+      for (int c = 0; c < 8; ++c) choff[c] = (uint32_t)(((c ^ (t & 7)) << 4) + (t >> 3) * 1024 + (t & 7) * 128);
       for (int j = 0;; ++j) {
         const int stage = j % C::RING;
         if (!warp_wait(bar.full + stage, (j / C::RING) & 1, p, misc)) break;
         const TileInfo ti = *sm.tinfo(j);
-        if (j >= 2 && !warp_wait(bar.pv_done + (j & 1), ((j - 2) >> 1) & 1, p, misc)) break;
+        // P.V of tile j - NAV has completed: its V tile buffer is free
+        if (j >= C::NAV && !warp_wait(bar.pv_done + (j % C::NAV), ((j / C::NAV) - 1) & 1, p, misc)) break;
         const uint8_t *pg = sm.stage(stage) + slot * C::PAGE_BYTES;
         const uint4 c0 = *reinterpret_cast<const uint4 *>(pg + OFF_VC + row * 32);
         const uint4 c1 = *reinterpret_cast<const uint4 *>(pg + OFF_VC + row * 32 + 16);
         const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint8_t *av = sm.av(j & 1) + (t >> 3) * 1024 + (t & 7) * 128;
+        uint8_t *av = sm.av(j % C::NAV);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           uint32_t r[8];
@@ -681,14 +772,14 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
           for (int hlf = 0; hlf < 2; ++hlf) {
             const int c = 2 * i + hlf;
-            *reinterpret_cast<uint4 *>(av + (c >> 3) * 16384 + (((c & 7) ^ (t & 7)) << 4)) =
+            *reinterpret_cast<uint4 *>(av + (c >> 3) * 16384 + choff[c & 7]) =
                 make_uint4(r[4 * hlf], r[4 * hlf + 1], r[4 * hlf + 2], r[4 * hlf + 3]);
           }
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar.av_full + (j & 1));
+          mbar_arrive(bar.av_full + (j % C::NAV));
           mbar_arrive(bar.empty + stage);
         }
         if (ti.flags & F_LAST) break;
@@ -707,10 +798,14 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
       int sigma = -1, seg = -1, prev_tile = -1;  // prev_tile: last tile of the current segment so far
       float *red = sm.red() + sg * C::RED_GROUP;
       const int pch = pos_channel(r), pgrp = pch / (D / NG), pk = pos_k(r);
+      // byte offset of (row cbase + n, token r) in the weight operand: op_offset(N, cbase + n, r) split into a
+      // per-thread part and, for the compile-time n of the unrolled loops, a row part; cbase is a multiple of 8
+      const int bw_tok = (r >> 6) * C::N * 128 + (cbase >> 3) * 1024 + (r & 7) * 2, rcx = (r & 63) >> 3;
+      auto bw_row = [rcx](int n) { return (n >> 3) * 1024 + (n & 7) * 128 + (((rcx ^ (n & 7))) << 4); };
       // Flush the segment's accumulator (after its last P.V) into partial slot (cta + seg), this
       // warpgroup's heads.
       auto flush = [&](int last_tile) -> bool {
-        if (!warp_wait(bar.pv_done + (last_tile & 1), (last_tile >> 1) & 1, p, misc)) return false;
+        if (!warp_wait(bar.pv_done + (last_tile % C::NAV), (last_tile / C::NAV) & 1, p, misc)) return false;
         tc_fence_after();
         float o[NCG];
         tmem_ld_cols<NCG>(tmem + lane_addr + C::TM_O + C::N * (sigma & 1) + cbase, o);
@@ -763,6 +858,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
       };
       bool ok = true;
       for (int j = 0;; ++j) {
+        // the K unpack of tile j has copied its scale/zero rows into the meta ring
         if (!warp_wait(bar.meta_full + (j % MR), (j / MR) & 1, p, misc)) { ok = false; break; }
         const TileInfo ti = *sm.tinfo(j);
         if (ti.flags & F_FIRST) {
@@ -788,13 +884,28 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         // scale/zero of this thread's token
         float ks[NG], kz[NG], vs[NG], vz[NG];
         {
+          // the token's record: Ks[NG] Kz[NG] Vs[NG] Vz[NG] bf16, 8 NG bytes, read in 8- or 16-byte pieces
+          uint32_t wd[2 * NG];
           const uint8_t *mr = sm.mring(j % MR) + r * 4 * C::META;
+          if constexpr (NG == 1) {
+            const uint2 v = *reinterpret_cast<const uint2 *>(mr);
+            wd[0] = v.x; wd[1] = v.y;
+          } else {
+#pragma unroll
+            for (int i = 0; i < NG / 2; ++i) {
+              const uint4 v = reinterpret_cast<const uint4 *>(mr)[i];
+              wd[4 * i] = v.x; wd[4 * i + 1] = v.y; wd[4 * i + 2] = v.z; wd[4 * i + 3] = v.w;
+            }
+          }
+          auto half_at = [&](int idx) {  // bf16 number idx of the record
+            return __uint_as_float((idx & 1) ? (wd[idx >> 1] & 0xffff0000u) : (wd[idx >> 1] << 16));
+          };
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
-            ks[g] = bf16_to_f32(reinterpret_cast<const uint16_t *>(mr)[g]);
-            kz[g] = bf16_to_f32(reinterpret_cast<const uint16_t *>(mr + C::META)[g]);
-            vs[g] = bf16_to_f32(reinterpret_cast<const uint16_t *>(mr + 2 * C::META)[g]);
-            vz[g] = bf16_to_f32(reinterpret_cast<const uint16_t *>(mr + 3 * C::META)[g]);
+            ks[g] = half_at(g);
+            kz[g] = half_at(NG + g);
+            vs[g] = half_at(2 * NG + g);
+            vz[g] = half_at(3 * NG + g);
           }
         }
         __syncwarp();
@@ -804,17 +915,27 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
           for (int g = 0; g < NG; ++g) { vs[g] = 0.f; vz[g] = 0.f; }
         }
-        if (!warp_wait(bar.s_full + (j & 1), (j >> 1) & 1, p, misc)) { ok = false; break; }
+        if (!warp_wait(bar.qk_done + (j % C::NSQ), (j / C::NSQ) & 1, p, misc)) { ok = false; break; }
         tc_fence_after();
-        float s[NCG];
-        tmem_ld_cols<NCG>(tmem + lane_addr + C::TM_S + C::N * (j & 1) + cbase, s);
+        constexpr int NQG = C::NQG;
+        float s[NQG];
+        tmem_ld_cols<NQG>(tmem + lane_addr + C::TM_S + C::NQ * (j % C::NSQ) + sg * NQG, s);
         float sc[GH];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
           float acc = 0.f, zacc = 0.f;
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
-            acc = fmaf(s[(h * NG + g) * 2] + s[(h * NG + g) * 2 + 1], ks[g], acc);
+            float sum;
+            if constexpr (C::QK8) {  // sum_t 16^t S_t by Horner (exact until the last two steps)
+              const float *st = s + (h * NG + g) * C::QT;
+              sum = st[C::QT - 1];
+#pragma unroll
+              for (int t = C::QT - 2; t >= 0; --t) sum = fmaf(sum, 16.f, st[t]);
+            } else {
+              sum = s[(h * NG + g) * 2] + s[(h * NG + g) * 2 + 1];
+            }
+            acc = fmaf(sum, ks[g], acc);
             zacc = fmaf(kz[g], zf[h][g], zacc);
           }
           sc[h] = valid ? fmaf(acc, kf[h], zacc) : -INFINITY;
@@ -875,7 +996,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           if (prev_tile >= 0 && rescale) {
             // the accumulator holds the earlier tiles of this segment: rescale this warpgroup's columns in
             // place once the last P.V into it has completed
-            if (!warp_wait(bar.pv_done + (prev_tile & 1), (prev_tile >> 1) & 1, p, misc)) { ok = false; break; }
+            if (!warp_wait(bar.pv_done + (prev_tile % C::NAV), (prev_tile / C::NAV) & 1, p, misc)) { ok = false; break; }
             tc_fence_after();
             float o[NCG];
             const uint32_t oa = tmem + lane_addr + C::TM_O + C::N * (sigma & 1) + cbase;
@@ -892,8 +1013,9 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           }
         }
         // weights (fp16 hi + lo) -> the B operand of P.V, token r of its K dimension
-        if (j >= 2 && !warp_wait(bar.pv_done + (j & 1), ((j - 2) >> 1) & 1, p, misc)) { ok = false; break; }
-        uint8_t *bw = sm.bw(j & 1);
+        // P.V of tile j - 2 has completed: the weight buffer of tile j is free
+        if (j >= 2 && !warp_wait(bar.pv_done + ((j - 2) % C::NAV), ((j - 2) / C::NAV) & 1, p, misc)) { ok = false; break; }
+        uint8_t *bw = sm.bw(j & 1) + bw_tok;
         const float ut = pow2i(tau);
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
@@ -904,15 +1026,15 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
             ozp[h][g] = fmaf(pr, vz[g], ozp[h][g]);
             const float w = pr * vs[g] * ut;
             const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
-            const __half hh = __float2half_rn(hi), hl = __float2half_rn(w - hi);
-            const int n = cbase + (h * NG + g) * 2;
-            *reinterpret_cast<__half *>(bw + op_offset(C::N, n, r)) = hh;
-            *reinterpret_cast<__half *>(bw + op_offset(C::N, n + 1, r)) = hl;
+            const int n = (h * NG + g) * 2;  // the warpgroup's row (compile time) of the weight operand
+            *reinterpret_cast<__half *>(bw + bw_row(n)) = __float2half_rn(hi);
+            *reinterpret_cast<__half *>(bw + bw_row(n + 1)) = __float2half_rn(w - hi);
           }
         }
         if constexpr (GH * NG * 2 < NCG) {
           if (j < 2)  // padding rows of the weight operand: zero (once per buffer)
-            for (int n = cbase + GH * NG * 2; n < cbase + NCG; ++n) *reinterpret_cast<uint16_t *>(bw + op_offset(C::N, n, r)) = 0;
+#pragma unroll
+            for (int n = GH * NG * 2; n < NCG; ++n) *reinterpret_cast<uint16_t *>(bw + bw_row(n)) = 0;
         }
         fence_proxy_async_smem();
         tc_fence_before();

@@ -254,13 +254,18 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
  *   q       bf16 [batch][Hq][d]; query head h reads KV head h / (Hq/Hkv)
  *   out     fp32 [batch][Hq][d]
  *   softmax_scale   > 0 (usually 1/sqrt(d))
- *   num_splits      history split factor per (sequence, KV head) for group sizes 32/64; 0 = choose
- *                   to fill the GPU.  With group size 128 the library balances the history pages of
- *                   all (sequence, KV head) pairs over a GPU-filling grid itself and ignores it.
+ *   num_splits      history split factor per (sequence, KV head) for pools with a codebook and group
+ *                   size 32/64; 0 = choose to fill the GPU.  Every other pool balances the history
+ *                   pages of all (sequence, KV head) pairs over a GPU-filling grid itself and ignores it.
  *   ws, ws_bytes    workspace of at least oscar_decode_workspace_size() bytes (same pool shape and
  *                   num_splits), 16-byte aligned
  * out[b][h] = sum over all pool tokens of softmax(score) * value, with score = q·k*scale for sink
  * and recent tokens and (q·R_k)·k_rot*scale for history tokens, whose values enter as v_rot·R_v^T.
+ * Kernels: uniform pools of group size 128 run the warp-MMA history kernel, uniform pools of group
+ * size 32/64 the tensor-memory (tcgen05) history kernel, codebook pools of group size 32/64 the CUDA-core
+ * kernels.  The environment variable OSCAR_DECODE_TC=1 (read once per process) routes uniform pools of
+ * group size 128 to the tensor-memory kernel too (for comparison and tests; same results up to float32
+ * rounding).
  */
 oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_splits, size_t *bytes);
 oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *q, float *out, float softmax_scale,
@@ -274,7 +279,8 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
  * segments).  With group size 128 the attention runs over the history before the step and the BF16
  * window after the append; the attention kernel's sink CTAs perform the demotion
  * and add the demoted token as a partial, the merge kernel stores the new token and advances the
- * counters.  Other pools run the two calls in turn.
+ * counters; uniform pools of group size 32/64 do the same around the tensor-memory history kernel.
+ * Codebook pools of group size 32/64 run the two calls in turn.
  *   k_new, v_new   bf16 [batch][Hkv][d] (16-byte aligned); q bf16 [batch][Hq][d] (16-byte aligned)
  *   ws, ws_bytes   at least oscar_decode_workspace_size(pool, 0) bytes
  * Errors as for the two calls; all checks run before any launch.
