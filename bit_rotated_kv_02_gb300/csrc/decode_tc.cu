@@ -53,6 +53,7 @@ constexpr int TI = 16;        // tile-information ring
 constexpr int MR = 4;         // scale/zero ring: tiles in flight between the K unpack and the softmax
 constexpr int LAZY = 16;      // the softmax reference grows only when a score exceeds it by more than 2^16
 constexpr int WEXP = 14 - LAZY;
+constexpr int TAU_HEAD = 2;   // the weight scale leaves the V scales 4x headroom before it must shrink
 constexpr int OFF_KC = 0, OFF_VC = 2048, OFF_META = 4096;
 constexpr int AV_BYTES = 2 * 16384;  // one 128 x 128 fp16 tile: two 64-channel atom columns
 
@@ -88,6 +89,9 @@ struct Cfg {
   static constexpr int BQ_IMG = QK8 ? NQ * 128 : N * 256;               // [NQ][128] e4m3 / [N][128] fp16
   static constexpr int BQ_BYTES = BQ_IMG + BQ_FACTORS;
   static constexpr int BW_BYTES = N * 256;
+  // N = 64: the weight operand MN-major (token k's 64 columns form one 128-byte swizzled row, so that a thread
+  // stores its columns with 16-byte stores); smaller N: K-major (column n's 128 tokens in two 128-byte rows)
+  static constexpr bool BW_MN = N == 64;
   // tensor memory columns: K operands and S for NSQ tiles (Q.K runs two tiles ahead of P.V), O for two segments
   static constexpr int NSQ = 4 * (AKC + NQ) + 2 * N <= 512 ? 4 : 3;
   static constexpr int TM_AK = 0, TM_S = AKC * NSQ, TM_O = TM_S + NSQ * NQ;
@@ -116,6 +120,7 @@ struct Cfg {
   static_assert(OFF_BQ % 1024 == 0 && OFF_BW % 1024 == 0 && BW_BYTES % 1024 == 0, "operand alignment");
   static_assert(STAGE_BYTES % 16 == 0 && OFF_RING % 16 == 0, "bulk copy alignment");
   static_assert(TM_USED <= 512 && GH * NG * 2 <= NCG && (!QK8 || GH * NG * QT <= NQG), "tensor memory and columns");
+  static_assert(!BW_MN || (GH * NG * 2 == NCG && NCG % 8 == 0), "MN-major weights: every column of a 16-byte chunk written");
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 // Column (and Q.K image row) of (head h, group g, term t): warpgroup h / GH owns the block of NCG columns
@@ -204,8 +209,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
 }
 
 // ---- tcgen05 helpers (kind::f16, A from tensor memory or shared memory) ----
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, bool b_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 // 128-byte-swizzled operand descriptor with explicit leading / stride byte offsets.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
@@ -224,20 +230,6 @@ __device__ __forceinline__ void mma_tmem_a_f8(uint32_t d, uint32_t a, uint64_t b
 __device__ __forceinline__ void mma_smem_a(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
                ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
-      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
-      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]),
-      "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]),
-      "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]),
-      "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
-      : "memory");
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
   asm volatile(
@@ -635,7 +627,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
       // free) and one per P.V (pv_done: V tile, weight buffer and accumulator released).
       if (lane == 0) {
         // the e4m3 formats of kind::f8f6f4 and the f16 formats of kind::f16 share the descriptor value 0
-        constexpr uint32_t ID_QK = idesc_f16(TILE, C::NQ, false), ID_PV = idesc_f16(TILE, C::N, true);
+        constexpr uint32_t ID_QK = idesc_f16(TILE, C::NQ, false), ID_PV = idesc_f16(TILE, C::N, true, C::BW_MN);
         constexpr int NS = C::NSQ;
         int sigma = -1, nq = 0, j = 0;
         int sig_of[NS];
@@ -685,8 +677,9 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_smem_a(o, desc_sw128(av + 2048 * kk, 16384, 1024),
-                       desc_sw128(bw + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024), ID_PV,
-                       (kk > 0 || !first) ? 1u : 0u);
+                       C::BW_MN ? desc_sw128(bw + 2048 * kk, C::BW_BYTES, 1024)
+                                : desc_sw128(bw + (kk >> 2) * (C::N * 128) + (kk & 3) * 32, 16, 1024),
+                       ID_PV, (kk > 0 || !first) ? 1u : 0u);
           umma_commit(bar.pv_done + (j % C::NAV));
           if (!more && j == nq - 1) break;  // that was the CTA's last tile
           ++j;
@@ -717,10 +710,13 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           for (int i = 0; i < 8; ++i) unpack_word_f8(w[i], r + 4 * i);
           tmem_st32(tmem + lane_addr + C::TM_AK + C::AKC * (j % C::NSQ), r);
         } else {
-          uint32_t r[64];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) unpack_word(w[i], r + 8 * i);
-          tmem_st64(tmem + lane_addr + C::TM_AK + C::AKC * (j % C::NSQ), r);
+          for (int hlf = 0; hlf < 2; ++hlf) {  // two stores of 32 columns (register pressure)
+            uint32_t r[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) unpack_word(w[4 * hlf + i], r + 8 * i);
+            tmem_st32(tmem + lane_addr + C::TM_AK + C::AKC * (j % C::NSQ) + 32 * hlf, r);
+          }
         }
         // scale/zero of the token: Ks, Kz, Vs, Vz (NG bf16 each) -> one record of the meta ring
         {
@@ -977,7 +973,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           if (vm > 0.f && vm >= tau_lim) {
             int e;
             frexpf(vm, &e);
-            tnew = max(-100, min(100, WEXP - e));
+            tnew = max(-100, min(100, WEXP - e - TAU_HEAD));
             if (tau_lim > 0.f && tnew > tau) tnew = tau;  // the scale only ever shrinks within a segment
           }
           bool rescale = false;
@@ -1015,8 +1011,11 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         // weights (fp16 hi + lo) -> the B operand of P.V, token r of its K dimension
         // P.V of tile j - 2 has completed: the weight buffer of tile j is free
         if (j >= 2 && !warp_wait(bar.pv_done + ((j - 2) % C::NAV), ((j - 2) / C::NAV) & 1, p, misc)) { ok = false; break; }
-        uint8_t *bw = sm.bw(j & 1) + bw_tok;
         const float ut = pow2i(tau);
+        float vsu[NG];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) vsu[g] = vs[g] * ut;
+        uint32_t wp[GH * NG];  // (hi, lo) of head h, group g as one fp16x2: columns (h NG + g) 2 and + 1
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
           const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mref[h]);  // 0 past the tile's tokens
@@ -1024,14 +1023,31 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
           for (int g = 0; g < NG; ++g) {
             ozp[h][g] = fmaf(pr, vz[g], ozp[h][g]);
-            const float w = pr * vs[g] * ut;
+            const float w = pr * vsu[g];
             const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
-            const int n = (h * NG + g) * 2;  // the warpgroup's row (compile time) of the weight operand
-            *reinterpret_cast<__half *>(bw + bw_row(n)) = __float2half_rn(hi);
-            *reinterpret_cast<__half *>(bw + bw_row(n + 1)) = __float2half_rn(w - hi);
+            const __half2 hl = __floats2half2_rn(hi, w - hi);  // one packed conversion for the pair
+            wp[h * NG + g] = *reinterpret_cast<const uint32_t *>(&hl);
           }
         }
-        if constexpr (GH * NG * 2 < NCG) {
+        if constexpr (C::BW_MN) {
+          // row r of the tile: 16-byte chunk c (columns 8c .. 8c + 7) at ((c ^ (r & 7)) << 4)
+          uint8_t *row = sm.bw(j & 1) + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int q = 0; q < GH * NG / 4; ++q) {
+            const int c = (cbase >> 3) + q;
+            *reinterpret_cast<uint4 *>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(wp[4 * q], wp[4 * q + 1], wp[4 * q + 2], wp[4 * q + 3]);
+          }
+        } else {
+          uint8_t *bw = sm.bw(j & 1) + bw_tok;
+#pragma unroll
+          for (int i = 0; i < GH * NG; ++i) {
+            *reinterpret_cast<uint16_t *>(bw + bw_row(2 * i)) = (uint16_t)(wp[i] & 0xffffu);
+            *reinterpret_cast<uint16_t *>(bw + bw_row(2 * i + 1)) = (uint16_t)(wp[i] >> 16);
+          }
+        }
+        if constexpr (!C::BW_MN && GH * NG * 2 < NCG) {
+          uint8_t *bw = sm.bw(j & 1) + bw_tok;
           if (j < 2)  // padding rows of the weight operand: zero (once per buffer)
 #pragma unroll
             for (int n = GH * NG * 2; n < NCG; ++n) *reinterpret_cast<uint16_t *>(bw + bw_row(n)) = 0;
