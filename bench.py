@@ -32,7 +32,9 @@ SINK, RECENT, PAGE = 64, 256, 64
 CALIB_T = 4096
 ATTN_KERNEL = "v1::attn_kernel (INT2 history + BF16 sink/recent CTAs)"
 ATTN_KERNEL_KEY = "v1::attn_kernel"
-ATTN_SRC = os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc", "decode_v1.cu")
+# the sources the attention kernel is compiled from (a traffic record holds only while they are unchanged)
+ATTN_SRC = [os.path.join(ROOT, "bit_rotated_kv_02_gb300", "csrc", f)
+            for f in ("decode_v1.cu", "bf16_part.cuh", "split.cuh", "oscar_internal.cuh", "ptx.cuh")]
 # the BF16 sink/window bytes are read by the same launch (its BF16 CTAs)
 ATTN_HAS_BF16 = True
 METRIC = "INT2-KV decode attn: KV tokens/s, HBM GB/s as frac of GB300 peak; demote tok/s"
@@ -201,16 +203,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def traffic_from_profiles(kernel: str, kernel_src: str):
+def sources_sha(paths) -> str:
+    """First 16 hex digits of the SHA-256 of the concatenated source files (in the given order)."""
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, kernel_srcs):
     """DRAM bytes per launch of `kernel` from profiles/traffic.json (written from an ncu capture, with the
-    capture's command), if the kernel's source file has not changed since that capture (else None)."""
+    capture's command), if the kernel's source files have not changed since that capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))[kernel]
     except (OSError, ValueError, KeyError):
         return None
-    sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    if rec.get("source_sha256_16") != sha:
+    if rec.get("source_sha256_16") != sources_sha(kernel_srcs):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -627,12 +636,27 @@ def other_workload(args):
     out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
     ws = torch.empty(ok.oscar_decode_workspace_size(P), dtype=torch.uint8, device="cuda")
     ms = _time(lambda: ok.oscar_decode_attention(P, q, out=out, ws=ws), max(3, min(args.steps, 100)), 5)
+    # the history kernel alone: CUDA events around it (on the call's stream) in a loop of calls
+    lib = ok.lib()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for ev in evs:
+        lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
+        ok.oscar_decode_attention(P, q, out=out, ws=ws)
+    torch.cuda.synchronize()
+    hist_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
     assert P.err() == 0, hex(P.err())
     hist = sum(max(L - SINK - RECENT, 0) for L in lens)
-    byts = hist * Hkv * 2 * (D // 4 + 4 * 4) + B * (SINK + RECENT) * Hkv * 2 * D * 2
+    ng = D // 32
+    hist_byts = hist * Hkv * 2 * (D // 4 + 2 * 2 * ng) + sum(pages_b) * 4   # codes + scale/zero + page table
+    byts = hist_byts + B * (SINK + RECENT) * Hkv * 2 * D * 2
     lines.append({"metric": "decode attention: KV tokens/s", "value": sum(lens) / (ms * 1e-3), "unit": "KV tokens/s",
                   "ms_per_step": ms, "workload": wl.name, "lengths": lens,
-                  "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak})
+                  "gbs": byts / (ms * 1e-3) / 1e9, "frac_of_peak": byts / (ms * 1e-3) / 1e9 / peak,
+                  "roofline": {"bound": "hbm", "kernel": f"tc::hist_kernel<{Hq // Hkv}, {ng}> (INT2 history, tcgen05)",
+                               "achieved": hist_byts / (hist_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                               "frac": hist_byts / (hist_ms * 1e-3) / 1e9 / peak,
+                               "algorithmic_bytes_per_launch": hist_byts, "mean_launch_us": hist_ms * 1e3,
+                               "timed_launches": len(evs)}})
     return lines
 
 

@@ -9,29 +9,37 @@
 //
 // Launches (all with programmatic dependent launch on the caller's stream):
 //   qrot_kernel  per (sequence, KV head): q_rot = q . R_k for the G query heads and the image of the Q.K
-//                B operand (fixed-point fp16 split of q_rot, one column pair per head and group) with the
-//                score factors, in the workspace.
+//                B operand (six base-16 digit planes of the fixed-point q_rot in e4m3, or its fp16 hi / lo
+//                split; one set of columns per head and group) with the score factors, in the workspace.
 //   hist_kernel  one CTA per SM over an equal share of the flattened (sequence, KV head, page) space, in
 //                tiles of 128 tokens (two pages of one segment):
-//                  warp 0     bulk-copies pages (codes, scale/zero rows) into a ring and, per segment, the
-//                             Q.K operand image;
-//                  warp 1     allocates tensor memory and issues the MMAs (one thread);
-//                  warps 2-5  unpack each token's 128 K codes into fp16 and store them into tensor memory,
-//                             the A operand of Q.K (M = 128 tokens, K = 128 channels);
-//                  warps 6-9  unpack the V codes into a 128-byte-swizzled shared-memory tile, read as the
-//                             MN-major A operand of P.V (M = 128 channels, K = 128 tokens);
-//                  warps 10-13 (one token row per thread) read the scores from tensor memory, run the
-//                             online softmax, write the weights (fp16 hi + lo) as the B operand of P.V, and
-//                             flush each segment's accumulator into a partial (m, l, o_rot).
+//                  warp 0      bulk-copies pages (codes, scale/zero rows) into a ring and, per segment, the
+//                              Q.K operand image;
+//                  warp 1      allocates tensor memory and issues the MMAs (one thread): Q.K up to two tiles
+//                              ahead of P.V, one commit per Q.K and one per P.V;
+//                  warps 2-5   unpack each token's 128 K codes (e4m3 or fp16) into tensor memory, the A
+//                              operand of Q.K (M = 128 tokens, K = 128 channels), and copy its scale/zero
+//                              rows into a small ring for the softmax;
+//                  warps 6-9   unpack the V codes into a 128-byte-swizzled shared-memory tile, read as the
+//                              MN-major A operand of P.V (M = 128 channels, K = 128 tokens);
+//                  warps 10-17 two softmax warpgroups, each over half of the G query heads of every tile
+//                              (one token row per thread): scores from tensor memory, online softmax, the
+//                              weights (fp16 hi + lo) as the B operand of P.V, and each segment's flush into
+//                              a partial (m, l, o_rot).
 //   bf16_kernel  the BF16 sink/window partials and, in the decode step, the demotion (part::bf16_role).
 //   merge        v1::merge_kernel: LSE merge, o . R_v^T, normalisation (decode step: append, counters).
 //
-// Exactness of the tensor-core sums.  A 2-bit code c in the low mantissa bits of an fp16 with a zero exponent
-// field is the subnormal c * 4^k * 2^-24 (k = its 2-bit position in the 16-bit lane), so one AND places two
-// codes.  q_rot * 2^sigma is split on a fixed-point grid, hi = 8 rint(y / 8), lo = rint((y - hi) 256) / 256,
-// each scaled by 4^-k, so every product with a code is an integer multiple of 2^-21 (hi) or 2^-32 (lo) and a
-// token's 128 products stay below 2^24 such units: the float32 accumulation of Q.K is exact in any order.
-//   score = kf * sum_g scale_g * (S_hi,g + S_lo,g) + sum_g zero_g * zf_g,  kf = 2^(24 - sigma) log2(e) s,
+// Exactness of the tensor-core sums.  q_rot * 2^sigma is taken on a fixed-point grid with 24 significant
+// bits (y = q_rot 2^sigma, |y| < 2^14).  fp16 form: a 2-bit code c in the low mantissa bits of an fp16 with a
+// zero exponent field is the subnormal c * 4^k * 2^-24 (k = its 2-bit position in the 16-bit lane), so one
+// AND places two codes; hi = 8 rint(y / 8), lo = rint((y - hi) 256) / 256, each scaled by 4^-k, so every
+// product with a code is an integer multiple of 2^-21 (hi) or 2^-32 (lo) and a token's 128 products stay below
+// 2^24 such units.  e4m3 form (kind::f8f6f4, K = 32 per MMA): a code in the two low bits of a byte is c * 2^-9,
+// two bits up c * 2^-7; the integer Y = y 2^9 is written as six balanced base-16 digits d_t (|d_t| <= 8, exact
+// in e4m3), one column per digit plane, so each plane's sum is a small integer multiple of 2^-9 and the score
+// is 2^(-sigma - 2) sum_t 16^t S_t (Horner in float32).  Either way the float32 accumulation of Q.K is exact
+// in any order, and
+//   score = kf * sum_g scale_g * S_g + sum_g zero_g * zf_g,
 //   o_rot[ch] = 2^(24 - 2k - tau) * (O_hi + O_lo)[ch] + sum_t p_t zero_t,g(ch),
 // with weights p * scale * 2^tau split into fp16 hi + lo (22 significant bits) and a lazily rescaled base-2
 // online softmax (the reference grows only when a score exceeds it by more than 2^LAZY).
