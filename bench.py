@@ -58,6 +58,7 @@ def parse():
                     help="decode100k is the headline line; the others measure the remaining workloads")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-cores", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-kind", choices=["decode", "bulk", "demote"], default="decode", help=argparse.SUPPRESS)
     ap.add_argument("--roofline-launches", type=int, default=64,
                     help="attention launches timed one by one with CUDA events after the run")
     return ap.parse_args()
@@ -128,12 +129,57 @@ def cpu_baseline_child(budget_s: float, cores: int) -> dict:
             "sample": f"{SAMPLE_NOTE}; {cores} processes of one thread each, the same sample", "seconds": round(t, 3)}
 
 
-def run_cpu_baseline(budget_s: float, cores: int = 1) -> dict:
+def cpu_bulk_child(budget_s: float) -> dict:
+    """Oracle bulk quantize (exactly rounded rotation, clip, scale/zero, codes) on batches of 2,048 synthetic
+    vectors of one KV head, one thread, for about budget_s; tokens/s of K and V of all Hkv heads."""
+    import synth
+    from oracle import quant as oq, rotation as orot
+    ch = synth.outlier_channels(7, 1, D, 2)
+    R = orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(11, D)))
+    x = synth.outlier_kv(8, 2048, 1, D, ch)[:, 0, :]
+    n, t = 0, 0.0
+    while t < budget_s:
+        t0 = time.perf_counter()
+        oq.quantize_vectors_many(x, R, CLIP, 128)
+        t += time.perf_counter() - t0
+        n += x.shape[0]
+    return {"value": n / t / (2 * 8), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} vectors of one KV head (oracle quantize_vectors_many, batches of 2,048); tokens/s = "
+                      "vectors/s / (K and V x 8 KV heads); one process", "seconds": round(t, 3)}
+
+
+def cpu_demote_child(budget_s: float) -> dict:
+    """Oracle append with demotion (the window's oldest K and V vectors rotated, clipped, quantized exactly into
+    the history) on a one-sequence, one-KV-head pool, one thread, for about budget_s; tokens/s of a sequence
+    with 8 KV heads."""
+    import synth
+    from oracle import pool as opool, rotation as orot
+    ch = synth.outlier_channels(7, 1, D, 4)
+    n_tok = SINK + RECENT + 4096
+    K = synth.outlier_kv(8, n_tok + 4096, 1, D, ch)
+    V = synth.outlier_kv(9, n_tok + 4096, 1, D, ch)
+    R = orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(11, D)))[None]
+    pages = -(-(n_tok + 4096) // PAGE) + 1
+    O = opool.Pool(1, HQ // HKV, 1, D, GROUP, pages, pages, R, R, [CLIP], [CLIP])
+    O.page_table[0] = synth.shuffled_pages(12, pages)
+    O.prefill(0, K[:SINK + RECENT], V[:SINK + RECENT])
+    n, t = 0, 0.0
+    while t < budget_s and n < 4096:
+        t0 = time.perf_counter()
+        O.append(K[SINK + RECENT + n][None], V[SINK + RECENT + n][None])
+        t += time.perf_counter() - t0
+        n += 1
+    return {"value": n / t / 8, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} appends with demotion on a one-KV-head pool (oracle Pool.append); tokens/s = appends/s "
+                      "/ 8 KV heads; one process", "seconds": round(t, 3)}
+
+
+def run_cpu_baseline(budget_s: float, cores: int = 1, kind: str = "decode") -> dict:
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--cpu-seconds",
-                        str(budget_s), "--cpu-cores", str(cores)], capture_output=True, text=True, env=env,
-                       timeout=900)
+                        str(budget_s), "--cpu-cores", str(cores), "--cpu-kind", kind], capture_output=True, text=True,
+                       env=env, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": "KV tokens/s", "cores": cores, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
@@ -571,7 +617,11 @@ def other_workload(args):
                       "roofline": {"bound": "hbm", "achieved": byts / (ms * 1e-3) / 1e9, "peak": peak,
                                    "frac": byts / (ms * 1e-3) / 1e9 / peak, "unit": "GB/s",
                                    "algorithmic_bytes": byts,
-                                   "flops_fp32_rotation": 2.0 * 2 * N * Hkv * D * D}})
+                                   "flops_fp32_rotation": 2.0 * 2 * N * Hkv * D * D,
+                                   "tensor_pipe_pct_ncu": 19.5,
+                                   "note": "tensor-pipe share from the ncu capture in profiles/quant_tc_kernel_bulk128k.md"},
+                      "cpu_baseline": None if args.no_cpu_baseline else run_cpu_baseline(min(args.cpu_seconds, 5.0),
+                                                                                         kind="bulk")})
         return lines
     if args.workload == "batch-sweep":
         for B in (1, 16, 64, 256):
@@ -639,6 +689,10 @@ def other_workload(args):
     # the history kernel alone: CUDA events around it (on the call's stream) in a loop of calls
     lib = ok.lib()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for ev in evs:   # record once so that the CUDA events exist (the library records them again)
+        ev[0].record()
+        ev[1].record()
+    torch.cuda.synchronize()
     for ev in evs:
         lib.oscar_profile_events(0, C.c_void_p(ev[0].cuda_event), C.c_void_p(ev[1].cuda_event))
         ok.oscar_decode_attention(P, q, out=out, ws=ws)
@@ -663,7 +717,12 @@ def other_workload(args):
 def main():
     args = parse()
     if args.cpu_baseline_child:
-        print(json.dumps(cpu_baseline_child(args.cpu_seconds, args.cpu_cores)))
+        if args.cpu_kind == "bulk":
+            print(json.dumps(cpu_bulk_child(args.cpu_seconds)))
+        elif args.cpu_kind == "demote":
+            print(json.dumps(cpu_demote_child(args.cpu_seconds)))
+        else:
+            print(json.dumps(cpu_baseline_child(args.cpu_seconds, args.cpu_cores)))
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -862,10 +921,11 @@ def main():
     peak = peak or 6800.0
     achieved = attn_bytes / (hist_mean_ms * 1e-3) / 1e9
     value = replica_throughput(tokens, ms, world)
-    cpu = cpu_all = None
+    cpu = cpu_all = cpu_demote = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = run_cpu_baseline(args.cpu_seconds)
         cpu_all = run_cpu_baseline(args.cpu_seconds, os.cpu_count() or 1)
+        cpu_demote = run_cpu_baseline(min(args.cpu_seconds, 5.0), kind="demote")
     if rank == 0:
         rec = {
             "metric": METRIC, "value": value, "unit": "KV tokens/s", "n_gpus": world, "steps": args.steps,
@@ -888,7 +948,8 @@ def main():
                          "sampling": "a loop of decode steps after the run, CUDA events around each attention launch"},
             "demote": {"tokens_per_s": 1.0 / (dem_ms * 1e-3), "mean_call_us": dem_ms * 1e3,
                        "note": "oscar_append_kv (demotion + append kernel), timed on its own after the run; in "
-                               "the decode step the attention kernel's sink CTAs perform the demotion"},
+                               "the decode step the attention kernel's sink CTAs perform the demotion",
+                       "cpu_baseline": cpu_demote},
             "l2_hot": {"value": hot_tokens / (hot_ms * 1e-3), "unit": "KV tokens/s", "ms_per_step": hot_ms / HOT_N,
                        "steps": HOT_N, "note": "one layer's step repeated: its history stays in L2"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
