@@ -57,6 +57,17 @@ def test_edge_lengths():
     helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
 
 
+@pytest.mark.parametrize("G,g", [(4, 32), (8, 64), (1, 32)])
+def test_edge_lengths_group_sizes(G, g):
+    """Groups of 32 and 64 (the tensor-memory kernel): empty histories, one history token, tiles whose
+    second page is empty or partial, ragged last pages, sequences that end a CTA's range mid-page."""
+    lens = [1, 64, 321, 384, 385, 449, 513, 577, 1000, 2000, 3333]
+    O, P, q = _setup(lens, 2 * G, 2, g, 700 + 10 * G + g)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+    assert P.err() == 0
+
+
 @pytest.mark.parametrize("G,g", [(1, 32), (2, 64), (8, 32), (4, 64)])
 def test_gqa_ratios_and_group_sizes(G, g):
     Hkv = 2
@@ -89,7 +100,7 @@ def test_decode_after_appends():
     helpers.assert_pools_equal(O, P)
 
 
-@pytest.mark.parametrize("G,g", [(4, 128), (8, 128), (2, 32)])
+@pytest.mark.parametrize("G,g", [(4, 128), (8, 128), (2, 32), (8, 32), (1, 64)])
 def test_decode_step_matches_oracle_and_separate_calls(G, g):
     """oscar_decode_step gives the oracle's result at every step and, up to float32 rounding, what
     oscar_append_kv followed by oscar_decode_attention gives (for group 128 the step's attention runs
