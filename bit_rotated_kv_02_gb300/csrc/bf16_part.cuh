@@ -66,7 +66,7 @@ struct BfSmem {
 constexpr int DEMOTE_SCRATCH = (D + 2 * 4 * 32 * 4) * 4 + D / 4 + 16 + 16;
 
 // ---------------------------------------------------------------------------------------------
-// Decode-step demotion, run by BF16 CTAs once their chunk is done (the history CTAs take far longer):
+// Decode-step demotion, run by BF16 CTAs before their chunk:
 // the sink CTA (chunk 0) demotes the window's oldest K vector, the first window CTA (chunk 1) its V
 // vector (slot recent_start, unchanged until the merge).  The vector is rotated, clipped and quantized
 // exactly as the demotion kernel does (four warps, 32 rows of R each in two batches of 16; any summation
@@ -231,6 +231,13 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
   const int n = (chunk == 0) ? slen : max(0, min(64, rl - (chunk - 1) * 64));
   for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  // the demotion first: its R rows are read while the history CTAs are still starting, and the CTA's own
+  // chunk then ends about when a chunk without a demotion would have
+  if (a.step && chunk < 2) {
+    bool wait_qrot = false;
+    const float *qr = chunk == 0 ? qrot_rows(b, kvh, sm, wait_qrot) : nullptr;
+    demote_role<G>(a, scratch, b, kvh, seg, st, chunk, qr, wait_qrot);
+  }
   const uint16_t *kb = chunk == 0 ? p.sink_k + ((size_t)b * p.Hkv + kvh) * SINK * D
                                   : p.recent_k + ((size_t)b * p.Hkv + kvh) * RECENT * D;
   const uint16_t *vb = chunk == 0 ? p.sink_v + ((size_t)b * p.Hkv + kvh) * SINK * D
@@ -335,11 +342,6 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
     }
     slot[h * PART_STRIDE + tid] = O;
     if (tid == 0) { slot[h * PART_STRIDE + D] = M; slot[h * PART_STRIDE + D + 1] = L; }
-  }
-  if (a.step && chunk < 2) {
-    bool wait_qrot = false;
-    const float *qr = chunk == 0 ? qrot_rows(b, kvh, sm, wait_qrot) : nullptr;
-    demote_role<G>(a, scratch, b, kvh, seg, st, chunk, qr, wait_qrot);
   }
 }
 
