@@ -512,6 +512,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
   if (n_pages > 0) {
     if (warp == W_PROD) {
       // ---------------- producer: pages and Q.K operand images ----------------
+      const uint64_t stream_pol = l2_evict_first();
       int b = s_b0, kvh = s_kvh0, local = s_local0, np = s_np0, hl = s_hl0;
       long long done = 0;
       int j = 0, sigma = -1, cur_seg = -1, pt_base = -1, pt_b = -1, ptv = -1;
@@ -550,7 +551,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         if (b != pt_b || local < pt_base || local + cnt > pt_base + 32) {
           pt_b = b;
           pt_base = local;
-          ptv = local + lane < np ? p.page_table[(size_t)b * p.max_pages + local + lane] : -1;
+          ptv = local + lane < np ? ld_hint(p.page_table + (size_t)b * p.max_pages + local + lane, l2_evict_last()) : -1;
         }
         int pp = __shfl_sync(FULL, ptv, (local - pt_base + lane) & 31);
         int ntk = 0;
@@ -577,12 +578,12 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           uint8_t *dst = sm.stage(stage) + lane * C::PAGE_BYTES;
           const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
           const int mb = PAGE * C::META;
-          bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar.full + stage);
-          bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar.full + stage);
-          bulk_g2s(dst + OFF_META, p.scale_k + row * NG, mb, bar.full + stage);
-          bulk_g2s(dst + OFF_META + mb, p.zero_k + row * NG, mb, bar.full + stage);
-          bulk_g2s(dst + OFF_META + 2 * mb, p.scale_v + row * NG, mb, bar.full + stage);
-          bulk_g2s(dst + OFF_META + 3 * mb, p.zero_v + row * NG, mb, bar.full + stage);
+          bulk_g2s_hint(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar.full + stage, stream_pol);
+          bulk_g2s_hint(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar.full + stage, stream_pol);
+          bulk_g2s_hint(dst + OFF_META, p.scale_k + row * NG, mb, bar.full + stage, stream_pol);
+          bulk_g2s_hint(dst + OFF_META + mb, p.zero_k + row * NG, mb, bar.full + stage, stream_pol);
+          bulk_g2s_hint(dst + OFF_META + 2 * mb, p.scale_v + row * NG, mb, bar.full + stage, stream_pol);
+          bulk_g2s_hint(dst + OFF_META + 3 * mb, p.zero_v + row * NG, mb, bar.full + stage, stream_pol);
         }
         done += cnt;
         local += cnt;
@@ -591,9 +592,9 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           local = 0;
           if (++kvh == p.Hkv) {
             kvh = 0;
-            do { ++b; } while (b < p.B && ((max(0, min(p.hist_len[b], p.max_pages * PAGE)) + PAGE - 1) / PAGE) == 0);
+            do { ++b; } while (b < p.B && ((max(0, min(split::hist_len_of(p, b), p.max_pages * PAGE)) + PAGE - 1) / PAGE) == 0);
             if (b < p.B) {
-              hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+              hl = max(0, min(split::hist_len_of(p, b), p.max_pages * PAGE));
               np = (hl + PAGE - 1) / PAGE;
             }
           }

@@ -590,6 +590,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     // time (lane i holds entry pt_base + i of sequence b; every KV head of a sequence shares them), so
     // that most stages issue their copies without a round trip of their own.  hist_len is read once per
     // sequence.
+    const uint64_t stream_pol = l2_evict_first();
     int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
     int np = sm.np0, hl = sm.hl0;
     int stage = 0, it = 0;
@@ -609,7 +610,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
       if (cnt > 0 && (b != pt_b || local < pt_base || local + cnt > pt_base + 32)) {
         pt_b = b;
         pt_base = local;
-        ptv = local + lane < np ? p.page_table[(size_t)b * p.max_pages + local + lane] : -1;
+        ptv = local + lane < np ? ld_hint(p.page_table + (size_t)b * p.max_pages + local + lane, l2_evict_last()) : -1;
       }
       int pp = __shfl_sync(FULL, ptv, (local - pt_base + lane) & 31), ntk = 0;
       if (lane >= cnt) pp = -1;
@@ -634,12 +635,12 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
           mbar_arrive_expect_tx(bar, (uint32_t)PAGE_BYTES);
           uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
           const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
-          bulk_g2s(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar);
-          bulk_g2s(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar);
-          bulk_g2s(dst + OFF_KS, p.scale_k + row, 128, bar);
-          bulk_g2s(dst + OFF_KZ, p.zero_k + row, 128, bar);
-          bulk_g2s(dst + OFF_VS, p.scale_v + row, 128, bar);
-          bulk_g2s(dst + OFF_VZ, p.zero_v + row, 128, bar);
+          bulk_g2s_hint(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar, stream_pol);
+          bulk_g2s_hint(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar, stream_pol);
+          bulk_g2s_hint(dst + OFF_KS, p.scale_k + row, 128, bar, stream_pol);
+          bulk_g2s_hint(dst + OFF_KZ, p.zero_k + row, 128, bar, stream_pol);
+          bulk_g2s_hint(dst + OFF_VS, p.scale_v + row, 128, bar, stream_pol);
+          bulk_g2s_hint(dst + OFF_VZ, p.zero_v + row, 128, bar, stream_pol);
         } else {
           mbar_arrive(bar);
         }
@@ -660,7 +661,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
           do { ++b; } while (b < p.B && npages_of(p, b) == 0);
           if (b < p.B) {
             np = npages_of(p, b);
-            hl = max(0, min(p.hist_len[b], p.max_pages * PAGE));
+            hl = max(0, min(split::hist_len_of(p, b), p.max_pages * PAGE));
           }
         }
       }

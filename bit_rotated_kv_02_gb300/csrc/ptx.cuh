@@ -58,6 +58,32 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
                : "memory");
 }
 
+// L2 eviction-priority policies (createpolicy) for cache-hinted loads and bulk copies: the history pages
+// stream through once per step (evict first), the page tables and counters are read again by the next step
+// of the same pool (evict last), so that the dependent reads at the start of a step hit in L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 0f3F800000;\n" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 0f3F800000;\n" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ int ld_hint(const int *ptr, uint64_t pol) {
+  int v;
+  asm volatile("ld.global.L2::cache_hint.s32 %0, [%1], %2;\n" : "=r"(v) : "l"(ptr), "l"(pol) : "memory");
+  return v;
+}
+
 // Three-input float32 min / max (NaN inputs are ignored), max of absolute values, saturating FMA.
 __device__ __forceinline__ float min3f(float a, float b, float c) {
   float d;

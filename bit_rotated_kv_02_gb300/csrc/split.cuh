@@ -4,12 +4,16 @@
 #pragma once
 
 #include "oscar_internal.cuh"
+#include "ptx.cuh"
 
 namespace oscar {
 namespace split {
 
+// hist_len[b], kept in L2 between steps (evict last)
+__device__ __forceinline__ int hist_len_of(const PoolArgs &p, int b) { return ld_hint(p.hist_len + b, l2_evict_last()); }
+
 __device__ __forceinline__ int npages_of(const PoolArgs &p, int b) {
-  int hl = p.hist_len[b];
+  int hl = hist_len_of(p, b);
   hl = max(0, min(hl, p.max_pages * PAGE));
   return (hl + PAGE - 1) / PAGE;
 }
@@ -54,7 +58,7 @@ static __device__ void locate_range(const PoolArgs &p, int n_hist, int cta, long
   const int lane = threadIdx.x & 31;
   b0 = 0; kvh0 = 0; local0 = 0; np0 = 0; hl0 = 0;
   if (p.B <= 32) {
-    const int hl = lane < p.B ? max(0, min(p.hist_len[lane], p.max_pages * PAGE)) : 0;
+    const int hl = lane < p.B ? max(0, min(hist_len_of(p, lane), p.max_pages * PAGE)) : 0;
     const int np = (hl + PAGE - 1) / PAGE;
     const long long v = (long long)np * p.Hkv;
     long long inc = v;
@@ -88,7 +92,7 @@ static __device__ void locate_range(const PoolArgs &p, int n_hist, int cta, long
   if (n > 0) {
     locate(p, lo, b0, kvh0, local0, total);
     np0 = npages_of(p, b0);
-    hl0 = max(0, min(p.hist_len[b0], p.max_pages * PAGE));
+    hl0 = max(0, min(hist_len_of(p, b0), p.max_pages * PAGE));
   }
 }
 
