@@ -68,6 +68,7 @@ def test_dyadic_tier_bit_exact():
         for clip in ((1.0, 1.0), (0.9, 0.75)):
             gc, gs, gz, st = run_gpu(xb, R32, clip, g)
             assert check_rows(xb, R32, clip, g, gc, gs, gz) == 0
+            assert st[2] == 0, "a result could not be proven correctly rounded"
 
 
 @pytest.mark.parametrize("g", [32, 64, 128])
@@ -85,8 +86,9 @@ def test_production_rotation_ragged(g):
 def test_single_row_and_empty():
     R32 = helpers.oracle_rotations(3, 1)
     xb = synth.outlier_kv(4, 1, 1, 128, synth.outlier_channels(4, 1, 128, 4))
-    gc, gs, gz, _ = run_gpu(xb, R32, (0.9,), 128)
+    gc, gs, gz, st = run_gpu(xb, R32, (0.9,), 128)
     check_rows(xb, R32, (0.9,), 128, gc, gs, gz)
+    assert st[2] == 0
     empty = torch.zeros((0, 1, 128), dtype=torch.bfloat16, device="cuda")
     ok.oscar_quantize_kv(empty, torch.from_numpy(R32).cuda(), torch.ones(1, device="cuda"), 128)
 
