@@ -93,6 +93,9 @@ struct Cfg {
   static constexpr int NQG = QK8 ? NQG8 : NCG;                          // S columns per softmax warpgroup
   static constexpr int NQ = QK8 ? ((SG * NQG8 + 15) / 16) * 16 : N;     // MMA N of Q.K
   static constexpr int AKC = QK8 ? 32 : 64;                             // TMEM columns of one K operand
+  // fp16 Q.K with several groups: one MMA of N = 2G per 16-channel step into the columns of that step's group
+  // (S column g 2G + 2h + term), so that no step multiplies the zero rows of the other groups' columns
+  static constexpr bool QKG = !QK8 && NG > 1;
   static constexpr int BQ_FACTORS = ((G + G * NG) * 4 + 15) / 16 * 16;  // kf[G], zf[G][NG]
   static constexpr int BQ_IMG = QK8 ? NQ * 128 : N * 256;               // [NQ][128] e4m3 / [N][128] fp16
   static constexpr int BQ_BYTES = BQ_IMG + BQ_FACTORS;
@@ -129,6 +132,7 @@ struct Cfg {
   static_assert(STAGE_BYTES % 16 == 0 && OFF_RING % 16 == 0, "bulk copy alignment");
   static_assert(TM_USED <= 512 && GH * NG * 2 <= NCG && (!QK8 || GH * NG * QT <= NQG), "tensor memory and columns");
   static_assert(!BW_MN || (GH * NG * 2 == NCG && NCG % 8 == 0), "MN-major weights: every column of a 16-byte chunk written");
+  static_assert(!QKG || (2 * G * NG == N && 2 * G % 16 == 0 && 2 * GH % 8 == 0 && NQG == 2 * GH * NG), "per-group Q.K");
   static_assert(SMEM <= 232448, "shared memory per block");
 };
 // Column (and Q.K image row) of (head h, group g, term t): warpgroup h / GH owns the block of NCG columns
@@ -251,17 +255,23 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 // N (a multiple of 8) consecutive fp32 columns of this warp's 32 TMEM lanes, in chunks of 8.
+// Loads issued without waiting (tcgen05_wait_ld() before the registers are used).
 template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+__device__ __forceinline__ void tmem_ld_cols_async(uint32_t taddr, uint32_t *r) {
   static_assert(N % 8 == 0, "columns in chunks of 8");
-  uint32_t r[N];
 #pragma unroll
   for (int c = 0; c < N; c += 8)
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                  : "=r"(r[c + 0]), "=r"(r[c + 1]), "=r"(r[c + 2]), "=r"(r[c + 3]), "=r"(r[c + 4]), "=r"(r[c + 5]),
                    "=r"(r[c + 6]), "=r"(r[c + 7])
                  : "r"(taddr + c));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tcgen05_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+  uint32_t r[N];
+  tmem_ld_cols_async<N>(taddr, r);
+  tcgen05_wait_ld();
 #pragma unroll
   for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -428,9 +438,10 @@ __global__ void __launch_bounds__(256) qrot_kernel(PoolArgs p, const uint16_t *q
     for (int i = tid; i < C::N * (D / 2); i += 256) {
       const int n = i / (D / 2), p2 = 2 * (i % (D / 2));
       uint32_t word = 0;
-      const int sgi = n / C::NCG, loc = n % C::NCG;  // row n = col_of(h, g, term)
-      if (loc < C::GH * NG * 2) {
-        const int h = sgi * C::GH + loc / (2 * NG), g = (loc / 2) % NG, term = loc & 1;
+      const int sgi = n / C::NCG, loc = n % C::NCG;  // row n = col_of(h, g, term), or g 2G + 2h + term (QKG)
+      if (C::QKG || loc < C::GH * NG * 2) {
+        const int h = C::QKG ? (n % (2 * G)) / 2 : sgi * C::GH + loc / (2 * NG);
+        const int g = C::QKG ? n / (2 * G) : (loc / 2) % NG, term = n & 1;
         const float s2 = pow2i(s_sig[h]);
         float v[2];
 #pragma unroll
@@ -637,6 +648,7 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
       if (lane == 0) {
         // the e4m3 formats of kind::f8f6f4 and the f16 formats of kind::f16 share the descriptor value 0
         constexpr uint32_t ID_QK = idesc_f16(TILE, C::NQ, false), ID_PV = idesc_f16(TILE, C::N, true, C::BW_MN);
+        constexpr uint32_t ID_QKG = idesc_f16(TILE, 2 * G, false);
         constexpr int NS = C::NSQ;
         int sigma = -1, nq = 0, j = 0;
         int sig_of[NS];
@@ -662,6 +674,15 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // K = 32 e4m3 per MMA: 32 bytes of the operand rows
               mma_tmem_a_f8(d, a + 8 * kk, desc_sw128(bq + kk * 32, 16, 1024), ID_QK, kk > 0 ? 1u : 0u);
+          } else if constexpr (C::QKG) {
+            constexpr int KPG = 8 / NG;  // 16-channel steps per group
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const int g = kk / KPG;
+              mma_tmem_a(d + 2 * G * g, a + 8 * kk,
+                         desc_sw128(bq + (kk >> 2) * (C::N * 128) + g * (2 * G / 8) * 1024 + (kk & 3) * 32, 16, 1024),
+                         ID_QKG, (kk % KPG) > 0 ? 1u : 0u);
+            }
           } else {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
@@ -924,7 +945,18 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         tc_fence_after();
         constexpr int NQG = C::NQG;
         float s[NQG];
-        tmem_ld_cols<NQG>(tmem + lane_addr + C::TM_S + C::NQ * (j % C::NSQ) + sg * NQG, s);
+        if constexpr (C::QKG) {  // group g's columns of this warpgroup's heads: g 2G + 2 (sg GH) ...
+          uint32_t sr[NQG];
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            tmem_ld_cols_async<2 * GH>(tmem + lane_addr + C::TM_S + C::NQ * (j % C::NSQ) + 2 * G * g + 2 * GH * sg,
+                                       sr + 2 * GH * g);
+          tcgen05_wait_ld();
+#pragma unroll
+          for (int c = 0; c < NQG; ++c) s[c] = __uint_as_float(sr[c]);
+        } else {
+          tmem_ld_cols<NQG>(tmem + lane_addr + C::TM_S + C::NQ * (j % C::NSQ) + sg * NQG, s);
+        }
         float sc[GH];
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
@@ -937,6 +969,8 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
               sum = st[C::QT - 1];
 #pragma unroll
               for (int t = C::QT - 2; t >= 0; --t) sum = fmaf(sum, 16.f, st[t]);
+            } else if constexpr (C::QKG) {
+              sum = s[2 * GH * g + 2 * h] + s[2 * GH * g + 2 * h + 1];
             } else {
               sum = s[(h * NG + g) * 2] + s[(h * NG + g) * 2 + 1];
             }
