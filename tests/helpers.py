@@ -27,12 +27,31 @@ def oracle_rotations(seed: int, Hkv: int, d: int = 128):
     return np.stack([orot.to_f32(orot.rotation_from_gaussian(synth.gaussian_matrix(seed + h, d))) for h in range(Hkv)])
 
 
+def oracle_covariance_rotations(seed: int, Hq: int, Hkv: int, n_tokens: int = 512, d: int = 128):
+    """Per-head float32 (R_k, R_v) from the oracle's covariance mode: U = the eigenvectors of C_k = sum Q^T Q
+    over the group's query heads and of C_v = sum (S V)^T (S V), on seeded calibration-style activations."""
+    G = Hq // Hkv
+    ch = synth.outlier_channels(seed, Hkv, d, 4)
+    Q = synth.bf16_bits_to_f32(synth.calib_samples(seed + 1, n_tokens, Hq, d, ch, heads_per_channel_set=G))
+    K = synth.bf16_bits_to_f32(synth.calib_samples(seed + 2, n_tokens, Hkv, d, ch))
+    V = synth.bf16_bits_to_f32(synth.calib_samples(seed + 3, n_tokens, Hkv, d, ch))
+    Rk = np.stack([orot.to_f32(orot.rotation_from_covariance(orot.covariance_k(Q[:, h * G:(h + 1) * G])))
+                   for h in range(Hkv)])
+    Rv = np.stack([orot.to_f32(orot.rotation_from_covariance(orot.covariance_v(Q[:, h * G:(h + 1) * G], K[:, h], V[:, h])))
+                   for h in range(Hkv)])
+    return Rk, Rv
+
+
 def make_pools(B, Hq, Hkv, g, pages_per_seq, seed, clip_k=None, clip_v=None, extra_pages=0, codebook_k=None,
-               codebook_v=None):
-    """(oracle Pool, device Pool) with identical rotations, clips, codebooks and shuffled page tables."""
+               codebook_v=None, rotation="haar"):
+    """(oracle Pool, device Pool) with identical rotations (Haar U, or the covariance mode's eigenvectors),
+    clips, codebooks and shuffled page tables."""
     import bit_rotated_kv_02_gb300 as ok
-    Rk = oracle_rotations(seed, Hkv)
-    Rv = oracle_rotations(seed + 1000, Hkv)
+    if rotation == "covariance":
+        Rk, Rv = oracle_covariance_rotations(seed, Hq, Hkv)
+    else:
+        Rk = oracle_rotations(seed, Hkv)
+        Rv = oracle_rotations(seed + 1000, Hkv)
     clip_k = np.full(Hkv, 0.9, np.float32) if clip_k is None else np.asarray(clip_k, np.float32)
     clip_v = np.full(Hkv, 0.9, np.float32) if clip_v is None else np.asarray(clip_v, np.float32)
     max_pages = max(max(pages_per_seq) + extra_pages, 1)

@@ -23,11 +23,11 @@ def _built():
     __graft_entry__.build()
 
 
-def _setup(lens, Hq, Hkv, g, seed, clip=None, heads=None, check_pool=True, extra_pages=0):
+def _setup(lens, Hq, Hkv, g, seed, clip=None, heads=None, check_pool=True, extra_pages=0, rotation="haar"):
     B = len(lens)
     pages = [max(0, -(-(L - 320) // 64)) for L in lens]
     clip_k, clip_v = (None, None) if clip is None else clip
-    O, P = helpers.make_pools(B, Hq, Hkv, g, pages, seed, clip_k, clip_v, extra_pages=extra_pages)
+    O, P = helpers.make_pools(B, Hq, Hkv, g, pages, seed, clip_k, clip_v, extra_pages=extra_pages, rotation=rotation)
     ch = synth.outlier_channels(seed, Hkv, 128, 4)
     for b, L in enumerate(lens):
         K = synth.outlier_kv(seed + 10 + b, L, Hkv, 128, ch)
@@ -136,6 +136,19 @@ def test_100k_context_sampled_heads():
     wl = synth.DECODE_100K
     heads = [0, 5]
     O, P, q = _setup(list(wl.context), wl.num_q_heads, wl.num_kv_heads, wl.group_size, wl.seed, heads=heads)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q)).cpu().numpy()
+    qh = [h for kv in heads for h in range(kv * wl.group, (kv + 1) * wl.group)]
+    ref = O.decode(q, heads=qh)
+    helpers.assert_attention_close(out[:, qh], ref[:, qh])
+
+
+def test_100k_context_covariance_rotations_sampled_head():
+    """The same shapes with the rotations of the covariance mode (eigenvectors of the calibration covariances
+    Q^T Q and (S V)^T (S V), as the 100k workload specifies), KV head 3 rebuilt by the oracle."""
+    wl = synth.DECODE_100K
+    heads = [3]
+    O, P, q = _setup(list(wl.context), wl.num_q_heads, wl.num_kv_heads, wl.group_size, wl.seed + 1, heads=heads,
+                     rotation="covariance")
     out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q)).cpu().numpy()
     qh = [h for kv in heads for h in range(kv * wl.group, (kv + 1) * wl.group)]
     ref = O.decode(q, heads=qh)
