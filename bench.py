@@ -766,7 +766,7 @@ def main():
     NL = args.layers
     DEM_N = 200  # appends timed on their own after the run
     HOT_N, HOT_W = 500, 20  # the L2-hot steps (layer 0 only) after the run
-    total = args.warmup + args.steps + args.e2e_steps + DEM_N + max(50, args.roofline_launches)
+    total = args.warmup + args.steps + args.e2e_steps + max(1, args.e2e_steps // 4) + DEM_N + max(50, args.roofline_launches)
     per_layer = -(-total // NL)
     layers = setup_layers(NL, per_layer + HOT_N + HOT_W + 8)
     dev = torch.device("cuda")
@@ -823,33 +823,43 @@ def main():
         if P.err() != 0:
             raise RuntimeError(f"device error flags {P.err():#x}")
 
-    # end to end through the public API: pinned host inputs copied in, result copied out, every step.
-    # The step's inputs (q, k_new, v_new) sit in one pinned buffer and go over in one copy; the calls
-    # take 16-byte-aligned views of the device copy.
+    # End to end through the public API with the step's inputs (q, k_new, v_new) in pinned host memory and its
+    # result read back into pinned host memory, every step.  Main figure: the host buffers are passed to the
+    # call itself, whose kernels read the inputs from and write the result to host memory over the host link
+    # (no separate copy; the calls stay back to back on the stream).  Second figure: one explicit copy of the
+    # inputs in and one of the result out per step around a call on device buffers.
     nq, nk = HQ * D, HKV * D
     hin = torch.empty(nq + 2 * nk, dtype=torch.bfloat16).pin_memory()
     hin[:nq].copy_(qs[0].reshape(-1).cpu()); hin[nq:nq + nk].copy_(kn[0].reshape(-1).cpu())
     hin[nq + nk:].copy_(vn[0].reshape(-1).cpu())
-    hq, hk, hv = hin[:nq], hin[nq:nq + nk], hin[nq + nk:]
+    hq, hk, hv = hin[:nq].view(1, HQ, D), hin[nq:nq + nk].view(1, HKV, D), hin[nq + nk:].view(1, HKV, D)
     hout = torch.empty((1, HQ, D), dtype=torch.float32).pin_memory()
     din = torch.empty_like(hin, device="cuda")
     dq, dk, dv = din[:nq].view(1, HQ, D), din[nq:nq + nk].view(1, HKV, D), din[nq + nk:].view(1, HKV, D)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_tokens = 0
     base = args.warmup + args.steps
-    e0.record()
-    for i in range(args.e2e_steps):
-        l = (base + i) % NL
-        din.copy_(hin, non_blocking=True)
-        ok.oscar_decode_step(layers[l], dk, dv, dq, out=outs[l], ws=ws)
-        hout.copy_(outs[l], non_blocking=True)
-        appended[l] += 1
-        e2e_tokens += L_CTX + appended[l]
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms)
+
+    def e2e_loop(explicit: bool, n: int, first: int):
+        tok = 0
+        e0.record()
+        for i in range(n):
+            l = (first + i) % NL
+            if explicit:
+                din.copy_(hin, non_blocking=True)
+                ok.oscar_decode_step(layers[l], dk, dv, dq, out=outs[l], ws=ws)
+                hout.copy_(outs[l], non_blocking=True)
+            else:
+                ok.oscar_decode_step(layers[l], hk, hv, hq, out=hout, ws=ws)
+            appended[l] += 1
+            tok += L_CTX + appended[l]
+        e1.record()
+        torch.cuda.synchronize()
+        return tok, max_over_ranks(e0.elapsed_time(e1))
+
+    e2e_tokens, e2e_ms = e2e_loop(False, args.e2e_steps, base)
+    e2x_steps = max(1, args.e2e_steps // 4)
+    e2x_tokens, e2x_ms = e2e_loop(True, e2x_steps, base + args.e2e_steps)
     # the demotion + append kernel on its own (oscar_append_kv: one token per step, window full)
     e0.record()
     for i in range(DEM_N):
@@ -868,7 +878,7 @@ def main():
             e.record()
     torch.cuda.synchronize()
     rl_tokens = 0
-    base = args.warmup + args.steps + args.e2e_steps
+    base = args.warmup + args.steps + args.e2e_steps + e2x_steps
     for i in range(RL):
         rl_tokens += step(base + i, evs[i])
     torch.cuda.synchronize()
@@ -954,7 +964,12 @@ def main():
                        "steps": HOT_N, "note": "one layer's step repeated: its history stays in L2"},
             "e2e": {"value": replica_throughput(e2e_tokens, e2e_ms, world), "unit": "KV tokens/s",
                     "h2d_bytes_per_step": hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2,
-                    "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps},
+                    "d2h_bytes_per_step": hout.numel() * 4, "steps": args.e2e_steps,
+                    "transfer": "the call's kernels read q, k_new, v_new from pinned host memory and write the "
+                                "output to pinned host memory over the host link",
+                    "explicit_copies": {"value": replica_throughput(e2x_tokens, e2x_ms, world), "steps": e2x_steps,
+                                        "transfer": "one host-to-device copy of the inputs and one device-to-host "
+                                                    "copy of the output per step, around a call on device buffers"}},
             "gpu_launches": args.steps * 3,   # q rotation, attention (history + BF16 CTAs + demotion), merge
             "clocks": clk,
             "cpu_baseline": cpu,

@@ -46,9 +46,11 @@ def _s(stream):
     return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def _dev(t, dtype, name):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+def _dev(t, dtype, name, host_ok=False):
+    """Check a tensor argument: a contiguous CUDA tensor of `dtype` (or, where host_ok, a page-locked host
+    tensor, which the kernels read or write in place over the host link)."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise TypeError(f"{name} must be a CUDA tensor" + (" or a pinned host tensor" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -152,6 +154,7 @@ class Pool:
     def __init__(self, batch, num_q_heads, num_kv_heads, group_size, num_pages, max_pages, R_k, R_v, clip_k, clip_v,
                  device="cuda", head_dim=HEAD_DIM, codebook_k=None, codebook_v=None):
         dev = torch.device(device)
+        self.device = dev
         self.B, self.Hq, self.Hkv, self.d, self.g = batch, num_q_heads, num_kv_heads, head_dim, group_size
         self.ng = head_dim // group_size
         self.num_pages, self.max_pages = num_pages, max_pages
@@ -249,10 +252,11 @@ def oscar_decode_step(pool: Pool, k_new, v_new, q, out=None, softmax_scale=None,
     """One decode step (append k_new/v_new bf16 [B][Hkv][128], demote, attention of q bf16 [B][Hq][128]):
     what oscar_append_kv then oscar_decode_attention give, in fewer launches.  Returns fp32 out."""
     for t, n in ((k_new, "k_new"), (v_new, "v_new"), (q, "q")):
-        _dev(t, torch.bfloat16, n)
-    out = torch.empty(q.shape, dtype=torch.float32, device=q.device) if out is None else out
+        _dev(t, torch.bfloat16, n, host_ok=True)
+    out = torch.empty(q.shape, dtype=torch.float32, device=q.device, pin_memory=not q.is_cuda) if out is None else out
+    _dev(out, torch.float32, "out", host_ok=True)
     if ws is None:
-        ws = torch.empty(oscar_decode_workspace_size(pool, 0), dtype=torch.uint8, device=q.device)
+        ws = torch.empty(oscar_decode_workspace_size(pool, 0), dtype=torch.uint8, device=pool.device)
     scale = 1.0 / math.sqrt(pool.d) if softmax_scale is None else float(softmax_scale)
     _lib.check(lib().oscar_decode_step(pool.ref, _p(k_new), _p(v_new), _p(q), _p(out), scale, _p(ws), ws.numel(),
                                        _s(stream)), "oscar_decode_step")

@@ -301,6 +301,30 @@ oscar_status_t oscar_demote(const oscar_pool *pool, const int32_t *mask, oscar_s
                      "demote");
 }
 
+// The per-call inputs and outputs (q, k_new, v_new, out) are read and written by the kernels themselves: each
+// must be device (or managed) memory, or page-locked host memory mapped into the device's address space at
+// the same address, which the kernels then read and write over the host link.  Anything else (pageable
+// host memory, a bad pointer) is refused here, before any launch.
+static bool device_accessible(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return at.devicePointer == p;
+    default: return false;
+  }
+}
+static oscar_status_t check_io(const void *p, const char *name) {
+  if (!device_accessible(p))
+    return fail(OSCAR_ERR_INVALID_ARG, "%s is neither device memory nor page-locked host memory mapped at the same "
+                "address", name);
+  return OSCAR_OK;
+}
+
 oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, const oscar_bf16 *v_new,
                                oscar_stream_t stream) {
   PoolArgs a;
@@ -309,6 +333,7 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
   if (k_new == nullptr || v_new == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "k_new/v_new NULL");
   if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 7u)
     return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 8-byte aligned");
+  if ((st = check_io(k_new, "k_new")) != OSCAR_OK || (st = check_io(v_new, "v_new")) != OSCAR_OK) return st;
   return cuda_status(launch_demote(a, nullptr, 2, k_new, v_new, static_cast<cudaStream_t>(stream)), "append_kv");
 }
 
@@ -362,6 +387,7 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   if (path != Path::CORE && (reinterpret_cast<uintptr_t>(q) & 15u))
     return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(ws) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "ws must be 16-byte aligned");
+  if ((st = check_io(q, "q")) != OSCAR_OK || (st = check_io(out, "out")) != OSCAR_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   float *w = static_cast<float *>(ws);
   switch (path) {
@@ -384,6 +410,9 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
     return fail(OSCAR_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   if (q == nullptr || out == nullptr) return fail(OSCAR_ERR_INVALID_ARG, "q/out NULL");
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
+  if ((st = check_io(k_new, "k_new")) != OSCAR_OK || (st = check_io(v_new, "v_new")) != OSCAR_OK ||
+      (st = check_io(q, "q")) != OSCAR_OK || (st = check_io(out, "out")) != OSCAR_OK)
+    return st;
   const Path path = decode_path(a);
   if (path == Path::CORE) {
     if ((st = oscar_append_kv(pool, k_new, v_new, stream)) != OSCAR_OK) return st;

@@ -253,6 +253,11 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
  * KV-cache serving).
  *   q       bf16 [batch][Hq][d]; query head h reads KV head h / (Hq/Hkv)
  *   out     fp32 [batch][Hq][d]
+ *           q and out (and k_new, v_new of the calls that take them) are read and written by the kernels
+ *           themselves: device (or managed) memory, or page-locked host memory mapped into the device's
+ *           address space at the same address (cudaHostAlloc under unified addressing), which the kernels
+ *           then access over the host link with no separate copy.  Other pointers (pageable host memory)
+ *           are refused with OSCAR_ERR_INVALID_ARG before any launch.
  *   softmax_scale   > 0 (usually 1/sqrt(d))
  *   num_splits      history split factor per (sequence, KV head) for pools with a codebook and group
  *                   size 32/64; 0 = choose to fill the GPU.  Every other pool balances the history

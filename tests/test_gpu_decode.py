@@ -130,6 +130,41 @@ def test_decode_step_matches_oracle_and_separate_calls(G, g):
     assert P.err() == 0 and P2.err() == 0
 
 
+@pytest.mark.parametrize("g", [128, 32])
+def test_decode_step_with_pinned_host_inputs_and_output(g):
+    """q, k_new, v_new and out in page-locked host memory: the step's kernels read and write them in place over
+    the host link (no separate copy) and give what the call with device buffers gives, pool bytes included; a
+    pageable host buffer is refused on the host before any launch."""
+    import ctypes as C
+    seed, Hkv, Hq = 660 + g, 2, 8
+    O, P, q = _setup([330, 1100], Hq, Hkv, g, seed, extra_pages=2)
+    _, P2, _ = _setup([330, 1100], Hq, Hkv, g, seed, extra_pages=2)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for t in range(6):
+        kn = synth.outlier_kv(seed + 2000 + t, 2, Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, 2, Hkv, 128, ch)
+        qt = synth.outlier_q(seed + 4000 + t, 2, Hq, Hkv, 128, ch)
+        O.append(kn, vn)
+        kd, vd, qd = helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn), helpers.to_dev_bf16(qt)
+        out_dev = ok.oscar_decode_step(P, kd, vd, qd)
+        kh, vh, qh = kd.cpu().pin_memory(), vd.cpu().pin_memory(), qd.cpu().pin_memory()
+        outh = torch.full(tuple(out_dev.shape), float("nan"), dtype=torch.float32).pin_memory()
+        ok.oscar_decode_step(P2, kh, vh, qh, out=outh)
+        torch.cuda.synchronize()
+        torch.testing.assert_close(outh, out_dev.cpu(), rtol=1e-6, atol=1e-6)
+        helpers.assert_attention_close(outh.numpy(), O.decode(qt))
+    helpers.assert_pools_equal(O, P2)
+    assert P2.err() == 0
+    lib = ok.lib()
+    ws = torch.empty(ok.oscar_decode_workspace_size(P2, 0), dtype=torch.uint8, device="cuda")
+    pageable = qd.cpu()
+    assert not pageable.is_pinned()
+    st = lib.oscar_decode_step(P2.ref, C.c_void_p(kd.data_ptr()), C.c_void_p(vd.data_ptr()),
+                               C.c_void_p(pageable.data_ptr()), C.c_void_p(out_dev.data_ptr()), 0.088,
+                               C.c_void_p(ws.data_ptr()), ws.numel(), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 1 and b"page-locked" in lib.oscar_last_error_string()
+
+
 def test_100k_context_sampled_heads():
     """Qwen3-8B layer shapes at 100k context: 99,680 history tokens on a shuffled page table (partial
     last page); the oracle rebuilds KV heads 0 and 5 and checks their 8 query heads."""
