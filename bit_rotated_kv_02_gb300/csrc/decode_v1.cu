@@ -63,8 +63,12 @@ struct Args {
   const float *qrot;   // [B][Hq][D] (qrot_kernel)
   const uint16_t *q;   // [B][Hq][D] bf16
   float sm_log2;       // softmax_scale * log2(e)
-  int n_hist;          // history CTAs (block indices n_bf .. n_bf + n_hist - 1)
-  int n_bf;            // BF16 CTAs (block indices 0 .. n_bf - 1)
+  int n_hist;          // history CTAs
+  int n_bf;            // BF16 CTAs
+  // block order: BF16 CTAs first (they and the history CTAs fit in one wave), or, when the BF16 CTAs
+  // outnumber a quarter of the resident slots (large batches), the history CTAs first, so that they start at
+  // once and the BF16 CTAs run in the remaining slots alongside them instead of in waves before them
+  int hist_first;
   float *part;         // partial slots [*][G][PART_STRIDE]
   const uint32_t *frag;  // per (sequence, KV head): the consumers' query fragments (qrot_kernel)
   // decode-step form: the pool counters still hold the state before the step (the merge kernel that
@@ -714,12 +718,14 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   // history pages, the window slots the BF16 CTAs read, q) is unchanged until the merge that follows.
   if (!a.step) pdl_wait();
   pdl_trigger();
-  if ((int)blockIdx.x < a.n_bf)
-    part::bf16_role<G>(a, sm, (int)blockIdx.x, sm.ring[0], [&](int b, int kvh, Smem<G> &, bool &wait) {
+  const int bid = (int)blockIdx.x;
+  const bool is_bf = a.hist_first ? bid >= a.n_hist : bid < a.n_bf;
+  if (is_bf)
+    part::bf16_role<G>(a, sm, a.hist_first ? bid - a.n_hist : bid, sm.ring[0], [&](int b, int kvh, Smem<G> &, bool &wait) {
       wait = true;  // q_rot is written by the query rotation that precedes this kernel
       return a.qrot + ((size_t)b * a.p.Hq + kvh * G) * D;
     });
-  else hist_role<G, CB>(a, sm, (int)blockIdx.x - a.n_bf);
+  else hist_role<G, CB>(a, sm, a.hist_first ? bid : bid - a.n_bf);
   // every thread has waited for the query rotation before the grid completes: the merge's wait (and the
   // next step's query rotation, which overwrites the fragments) then follows it as well
   if (a.step) pdl_wait();
@@ -985,6 +991,10 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.n_hist = v1_hist_ctas(p);
   const int nbf = p.B * p.Hkv * 5;
   a.n_bf = nbf;
+  {
+    const int slots = has_codebook(p) ? resident_ctas_for<true>(G) : resident_ctas_for<false>(G);
+    a.hist_first = nbf > slots / 4 ? 1 : 0;
+  }
   const int smem = (int)sizeof(v1::Smem<G>);
   auto attn = has_codebook(p) ? v1::attn_kernel<G, true> : v1::attn_kernel<G, false>;
   cudaError_t e = cudaFuncSetAttribute(attn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
