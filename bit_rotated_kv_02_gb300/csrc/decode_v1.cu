@@ -749,16 +749,18 @@ constexpr int RV_LD = D + 4;  // padded row stride of the shared copy of R_v
 constexpr int PMAX = 96;      // partial slots staged in shared memory per round
 constexpr uint32_t PART_BYTES = PART_STRIDE * sizeof(float);
 constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX * PART_BYTES;
+// hpc query heads per CTA (grid G / hpc x Hkv x B): large grids merge several heads of a (sequence, KV head)
+// in one CTA, one after the other, with one copy of R_v and one location of the partials.
 template <int G>
 __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
-                                                   const uint16_t *k_new, const uint16_t *v_new) {
+                                                   const uint16_t *k_new, const uint16_t *v_new, int hpc) {
   extern __shared__ float4 rvs4[];  // R_v of this KV head (row stride RV_LD floats), then the staged slots
   float *pst = reinterpret_cast<float *>(rvs4 + D * (RV_LD / 4));
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
   __shared__ float pw[PMAX], s_stat[2];
   __shared__ long long s_pref, s_total;
   __shared__ int s_last_all;
-  const int h = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
+  const int kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
   const bool step = k_new != nullptr;
@@ -776,20 +778,22 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   }
   StepState st{};
   if (step) st = step_state(p, b);
-  // the partials' location (pool counters, unchanged until the grid's last arrival advances them)
+  // the partials' location (pool counters, unchanged until the grid's last arrival advances them): the
+  // history pages of all sequences and of the sequences before b, from one round of independent loads
   if (warp == 0) {
-    long long total;
-    int bb, kk, ll;
-    locate(p, 0, bb, kk, ll, total);
-    long long run = 0;
-    for (int base = 0; base < b; base += 32) {
-      const int x = base + lane;
-      long long v = (x < b) ? (long long)npages_of(p, x) * p.Hkv : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
-      run += v;
+    long long total = 0, pref = 0;
+#pragma unroll 8
+    for (int x = lane; x < p.B; x += 32) {
+      const long long v = (long long)npages_of(p, x) * p.Hkv;
+      total += v;
+      if (x < b) pref += v;
     }
-    if (lane == 0) { s_pref = run; s_total = total; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      total += __shfl_xor_sync(FULL, total, o);
+      pref += __shfl_xor_sync(FULL, pref, o);
+    }
+    if (lane == 0) { s_pref = pref; s_total = total; }
   }
   const int np = npages_of(p, b);
   __syncthreads();  // every counter read of this CTA is done
@@ -809,12 +813,6 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   const int nrot = nh + (step ? 1 : 0);  // rotated-space partials: history (+ the demoted token)
   const int nparts = nrot + 5;
   const size_t stride = (size_t)G * PART_STRIDE;
-  const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
-  const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride + (size_t)h * PART_STRIDE;
-  const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
-  auto slot = [&](int i) {
-    return i < nh ? hp + (size_t)i * stride : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
-  };
   __syncthreads();  // s_last_all
   // the grid's last arrival: every sequence's counters after the step (the first MT are read here, while
   // no CTA reads them any more, and kept in registers for the stores after the wait)
@@ -823,6 +821,14 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   if (last_all && tid < p.B) sa = step_state(p, tid);
   pdl_wait();
   pdl_trigger();
+  for (int hh = 0; hh < hpc; ++hh) {
+  const int h = blockIdx.x * hpc + hh;
+  const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
+  const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride + (size_t)h * PART_STRIDE;
+  const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
+  auto slot = [&](int i) {
+    return i < nh ? hp + (size_t)i * stride : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
+  };
   // The partial slots are staged in shared memory, PMAX per round, by 16-byte loads of every thread
   // (one round trip); warp 0 forms the round's maximum, the weights and their sum once, and the
   // threads (slice, channel) add the weighted outputs of every fourth slot.  Rounds combine with a
@@ -900,8 +906,10 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
                     (((Obs[0][ch] + Obs[1][ch]) + Obs[2][ch]) + Obs[3][ch]);
     out[((size_t)b * p.Hq + kvh * G + h) * D + ch] = L > 0.f ? o / L : 0.f;
   }
+  __syncthreads();  // the next head reuses Osl, Obs and Orot
+  }
   if (!step) return;
-  if (h == 0 && st.append && tid < 2 * (D / 4)) {  // the new token of KV head kvh (8-byte pieces of K and V)
+  if (blockIdx.x == 0 && st.append && tid < 2 * (D / 4)) {  // the new token of KV head kvh (8-byte pieces of K and V)
     const int kv = tid / (D / 4), j = tid % (D / 4);
     uint16_t *dst = st.to_sink
         ? (kv == 0 ? p.sink_k : p.sink_v) + (((size_t)b * p.Hkv + kvh) * SINK + st.slen) * D
@@ -1013,19 +1021,35 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(attn, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
-  return launch_pdl(v1::merge_kernel<G>, dim3(G, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p,
-                    (const float *)a.part, a.n_hist, out, k_new, v_new);
+  return launch_merge_v1(p, (const float *)a.part, a.n_hist, out, k_new, v_new, s);
 }
 
 // The merge of a decode launch whose partial slots follow this file's layout (history slots cta + segment
 // for n_hist history CTAs, then the BF16 and demoted-token slots); k_new != NULL: the decode-step form.
+// Query heads per merge CTA: one while the grid takes at most four waves of one CTA per SM (the waves after
+// the first run their copies of R_v and their counter reads behind the first), else the smallest power of
+// two that brings it within four waves, at most G.
+static int merge_heads_per_cta(const PoolArgs &p) {
+  static std::atomic<int> sms_cache[kMaxDevices];
+  const int sms = per_device(sms_cache, [](int dev) {
+    int n = 148;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n;
+  });
+  const int G = p.Hq / p.Hkv;
+  int hpc = 1;
+  while (hpc < G && (long long)(G / hpc) * p.Hkv * p.B > 4LL * sms) hpc *= 2;
+  return hpc;
+}
+
 cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
                             const uint16_t *v_new, cudaStream_t s) {
+  const int hpc = merge_heads_per_cta(p);
   auto go = [&](auto kernel) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v1::MERGE_SMEM);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kernel, dim3(p.Hq / p.Hkv, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p, part, n_hist, out,
-                      k_new, v_new);
+    return launch_pdl(kernel, dim3(p.Hq / p.Hkv / hpc, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p, part, n_hist,
+                      out, k_new, v_new, hpc);
   };
   switch (p.Hq / p.Hkv) {
     case 1: return go(v1::merge_kernel<1>);
