@@ -46,7 +46,6 @@ namespace v1 {
 using part::StepState;
 using part::step_state;
 using split::npages_of;
-using split::locate;
 using split::locate_range;
 
 constexpr int NSTAGE = 3;

@@ -18,37 +18,6 @@ __device__ __forceinline__ int npages_of(const PoolArgs &p, int b) {
   return (hl + PAGE - 1) / PAGE;
 }
 
-// Map a flattened page index to (b, kvh, local page) by a warp-cooperative scan over sequences.
-// Run by one full warp; results valid in every lane.  total receives the number of pages.
-static __device__ void locate(const PoolArgs &p, long long start, int &b0, int &kvh0, int &local0, long long &total) {
-  const int lane = threadIdx.x & 31;
-  long long run = 0;
-  b0 = -1; kvh0 = 0; local0 = 0;
-  for (int base = 0; base < p.B; base += 32) {
-    const int b = base + lane;
-    const long long v = (b < p.B) ? (long long)npages_of(p, b) * p.Hkv : 0;
-    long long inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(FULL, inc, o);
-      if (lane >= o) inc += t;
-    }
-    const long long excl = run + inc - v;
-    const unsigned hit = __ballot_sync(FULL, b < p.B && v > 0 && start >= excl && start < excl + v);
-    if (b0 < 0 && hit) {
-      const int src = __ffs(hit) - 1;
-      const long long e = __shfl_sync(FULL, excl, src);
-      const int bb = base + src;
-      const int np = npages_of(p, bb);
-      b0 = bb;
-      kvh0 = (int)((start - e) / np);
-      local0 = (int)((start - e) % np);
-    }
-    run += __shfl_sync(FULL, inc, 31);
-  }
-  total = run;
-}
-
 // This CTA's share of the flattened (sequence, KV head, page) space: pages [lo, lo + n) with
 // chunk = ceil(total / n_hist), lo = cta * chunk, and the position (b0, kvh0, local0) of page lo plus
 // the page count np0 and history length hl0 of sequence b0.  Run by one full warp; results valid in
@@ -84,15 +53,46 @@ static __device__ void locate_range(const PoolArgs &p, int n_hist, int cta, long
     }
     return;
   }
-  long long total;
-  locate(p, 0, b0, kvh0, local0, total);  // total only
+  // more than 32 sequences: lane l takes the block of sequences [l K, l K + K), K = ceil(B / 32); the block
+  // sums come from one round of independent loads, a warp scan orders the blocks, and the lane whose block
+  // holds page lo walks it
+  const int K = (p.B + 31) / 32, first = min(p.B, lane * K), last = min(p.B, first + K);
+  long long bsum = 0;
+#pragma unroll 8
+  for (int x = first; x < last; ++x) bsum += (long long)npages_of(p, x) * p.Hkv;
+  long long inc = bsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long t = __shfl_up_sync(FULL, inc, o);
+    if (lane >= o) inc += t;
+  }
+  const long long total = __shfl_sync(FULL, inc, 31);
   const long long chunk = (total + n_hist - 1) / n_hist;
   lo = (long long)cta * chunk;
   n = max(0ll, min(total, lo + chunk) - lo);
-  if (n > 0) {
-    locate(p, lo, b0, kvh0, local0, total);
-    np0 = npages_of(p, b0);
-    hl0 = max(0, min(hist_len_of(p, b0), p.max_pages * PAGE));
+  const long long excl = inc - bsum;
+  const unsigned hit = __ballot_sync(FULL, bsum > 0 && lo >= excl && lo < excl + bsum);
+  if (n > 0 && hit) {
+    const int src = __ffs(hit) - 1;
+    int bb = 0, kk = 0, ll = 0, np = 0, hl = 0;
+    if (lane == src) {
+      long long run = excl;
+      for (int x = first; x < last; ++x) {
+        const int hx = max(0, min(hist_len_of(p, x), p.max_pages * PAGE));
+        const int npx = (hx + PAGE - 1) / PAGE;
+        const long long v = (long long)npx * p.Hkv;
+        if (v > 0 && lo < run + v) {
+          bb = x; kk = (int)((lo - run) / npx); ll = (int)((lo - run) % npx); np = npx; hl = hx;
+          break;
+        }
+        run += v;
+      }
+    }
+    b0 = __shfl_sync(FULL, bb, src);
+    kvh0 = __shfl_sync(FULL, kk, src);
+    local0 = __shfl_sync(FULL, ll, src);
+    np0 = __shfl_sync(FULL, np, src);
+    hl0 = __shfl_sync(FULL, hl, src);
   }
 }
 
