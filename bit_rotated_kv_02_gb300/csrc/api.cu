@@ -318,8 +318,23 @@ static bool device_accessible(const void *p) {
     default: return false;
   }
 }
+// The last pointers this thread found reachable (decode loops pass the same buffers every step; the
+// attribute query costs host time comparable to a short step).  A freed and re-allocated pinned buffer keeps
+// its verdict only if the new allocation at that address is pinned too or the system lets the device reach
+// pageable memory (GB300 with its coherent host link does).
+static bool device_accessible_cached(const void *p) {
+  constexpr int N = 8;
+  static thread_local const void *seen[N] = {};
+  static thread_local int next = 0;
+  for (int i = 0; i < N; ++i)
+    if (seen[i] == p) return true;
+  if (!device_accessible(p)) return false;
+  seen[next] = p;
+  next = (next + 1) % N;
+  return true;
+}
 static oscar_status_t check_io(const void *p, const char *name) {
-  if (!device_accessible(p))
+  if (!device_accessible_cached(p))
     return fail(OSCAR_ERR_INVALID_ARG, "%s is neither device memory nor page-locked host memory mapped at the same "
                 "address", name);
   return OSCAR_OK;
@@ -355,12 +370,19 @@ static Path decode_path(const PoolArgs &a) {
   return uniform ? Path::TC : Path::CORE;
 }
 
+// Workspace bytes a call needs at least (min) or the size that enables everything (the group-128 path's
+// dynamic tail of the history split: oscar_decode_workspace_size reports it).
+static size_t ws_min(const PoolArgs &a, int num_splits);
 static size_t ws_need(const PoolArgs &a, int num_splits) {
   switch (decode_path(a)) {
     case Path::TC: return tc_ws_bytes(a);
-    case Path::V1: return v1_ws_bytes(a);
+    case Path::V1: return v1_ws_bytes(a, true);
     default: return decode_ws_bytes(a, num_splits == 0 ? auto_splits(a) : num_splits);
   }
+}
+
+static size_t ws_min(const PoolArgs &a, int num_splits) {
+  return decode_path(a) == Path::V1 ? v1_ws_bytes(a, false) : ws_need(a, num_splits);
 }
 
 oscar_status_t oscar_decode_workspace_size(const oscar_pool *pool, int32_t num_splits, size_t *bytes) {
@@ -382,7 +404,7 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   if (!(softmax_scale > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "softmax_scale must be > 0");
   if (num_splits < 0) return fail(OSCAR_ERR_INVALID_ARG, "num_splits < 0");
   const Path path = decode_path(a);
-  const size_t need = ws_need(a, num_splits);
+  const size_t need = ws_min(a, num_splits);
   if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   if (path != Path::CORE && (reinterpret_cast<uintptr_t>(q) & 15u))
     return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
@@ -392,7 +414,9 @@ oscar_status_t oscar_decode_attention(const oscar_pool *pool, const oscar_bf16 *
   float *w = static_cast<float *>(ws);
   switch (path) {
     case Path::TC: return cuda_status(launch_decode_tc(a, q, out, softmax_scale, w, s), "decode_attention");
-    case Path::V1: return cuda_status(launch_decode_v1(a, q, out, softmax_scale, w, s), "decode_attention");
+    case Path::V1:
+      return cuda_status(launch_decode_v1(a, q, out, softmax_scale, w, s, ws_bytes >= v1_ws_bytes(a, true)),
+                         "decode_attention");
     default:
       return cuda_status(launch_decode(a, q, out, softmax_scale, num_splits == 0 ? auto_splits(a) : num_splits, w, s),
                          "decode_attention");
@@ -418,7 +442,7 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
     if ((st = oscar_append_kv(pool, k_new, v_new, stream)) != OSCAR_OK) return st;
     return oscar_decode_attention(pool, q, out, softmax_scale, 0, ws, ws_bytes, stream);
   }
-  const size_t need = ws_need(a, 0);
+  const size_t need = ws_min(a, 0);
   if (ws == nullptr || ws_bytes < need) return fail(OSCAR_ERR_WORKSPACE, "workspace %zu < %zu bytes", ws_bytes, need);
   if (reinterpret_cast<uintptr_t>(q) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "q must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(ws) & 15u) return fail(OSCAR_ERR_INVALID_ARG, "ws must be 16-byte aligned");
@@ -426,7 +450,8 @@ oscar_status_t oscar_decode_step(const oscar_pool *pool, const oscar_bf16 *k_new
   if (path == Path::TC)
     return cuda_status(launch_decode_tc(a, q, out, softmax_scale, static_cast<float *>(ws), s, k_new, v_new),
                        "decode_step");
-  return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws), s),
+  return cuda_status(launch_step_v1(a, k_new, v_new, q, out, softmax_scale, static_cast<float *>(ws), s,
+                                    ws_bytes >= v1_ws_bytes(a, true)),
                      "decode_step");
 }
 
@@ -496,3 +521,11 @@ oscar_status_t oscar_bf16_decode_step(const oscar_bf16_cache *cache, const oscar
 }
 
 }  // extern "C"
+
+oscar_status_t oscar::decode_workspace_min(const oscar_pool *pool, size_t *bytes) {
+  PoolArgs a;
+  oscar_status_t st = check_pool(pool, a);
+  if (st != OSCAR_OK) return st;
+  *bytes = ws_min(a, 0);
+  return OSCAR_OK;
+}

@@ -510,7 +510,8 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
   if (warp == W_PROD) {
     long long lo, n;
     int b0, kvh0, local0, np0, hl0;
-    split::locate_range(p, a.n_hist, cta, lo, n, b0, kvh0, local0, np0, hl0);
+    split::Plan pl;
+    split::locate_range(p, a.n_hist, cta, false, lo, n, b0, kvh0, local0, np0, hl0, pl);
     if (lane == 0) { s_lo = lo; s_n = n; s_b0 = b0; s_kvh0 = kvh0; s_local0 = local0; s_np0 = np0; s_hl0 = hl0; }
   }
   if (warp == W_MMA) tmem_alloc(misc + M_TMEM, C::TM_COLS);

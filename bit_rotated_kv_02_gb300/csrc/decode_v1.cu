@@ -68,6 +68,10 @@ struct Args {
   // outnumber a quarter of the resident slots (large batches), the history CTAs first, so that they start at
   // once and the BF16 CTAs run in the remaining slots alongside them instead of in waves before them
   int hist_first;
+  // dynamic tail of the history split (split::plan_of): enabled when the workspace holds its partial slots;
+  // the chunk counter (zeroed by the query rotation) sits in the workspace after the partial slots
+  int dyn;
+  unsigned long long *dyn_ctr;
   float *part;         // partial slots [*][G][PART_STRIDE]
   const uint32_t *frag;  // per (sequence, KV head): the consumers' query fragments (qrot_kernel)
   // decode-step form: the pool counters still hold the state before the step (the merge kernel that
@@ -104,11 +108,12 @@ struct Smem {
   uint64_t full[NSTAGE][STAGE_PAGES], empty[NSTAGE][STAGE_PAGES];  // one pair per page slot
   uint64_t csync;                                                    // consumer-warp barrier
   int meta_seg[NSTAGE], meta_ntok[NSTAGE][STAGE_PAGES], meta_flags[NSTAGE];  // flags: 1 last, 2 abort
+  int meta_slot[NSTAGE];                                                      // partial slot of the stage
   float qr[G][D];  // BF16 CTAs: the queries
   float wm[CONSUMER_WARPS][G], wl[CONSUMER_WARPS][G], wz[CONSUMER_WARPS][G];
   float wo[CONSUMER_WARPS][G][D];
   float pbuf[CONSUMER_WARPS][G][16];
-  long long range_lo, range_n;
+  long long range_lo, range_n, n_dyn;
   int b0, kvh0, local0, np0, hl0;
 };
 
@@ -134,7 +139,7 @@ __host__ __device__ constexpr int frag_words() { return Smem<G>::NT * 18; }
 // starts only after the previous step's merge has completed.
 template <int G>
 __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q, float *qrot, uint32_t *frag,
-                                                   float sm_log2) {
+                                                   float sm_log2, unsigned long long *dyn_ctr) {
   constexpr int NT = Smem<G>::NT;
   __shared__ float qs[G][D];
   __shared__ float part[8][G][D];
@@ -155,6 +160,7 @@ __global__ void __launch_bounds__(512) qrot_kernel(PoolArgs p, const uint16_t *q
   }
   pdl_wait();  // the previous kernel on the stream (the last reader of q_rot and the fragments) has completed
   pdl_trigger();
+  if (dyn_ctr != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *dyn_ctr = 0;  // the split's chunk counter
 #pragma unroll
   for (int k = 0; k < QPT; ++k) {
     const int i = tid + 512 * k;
@@ -564,7 +570,9 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
   }
 }
 
-template <int G, bool CB>
+// DYN: the build of the kernel with the dynamic tail of the split (launched when the pool can be large enough
+// for it); without it the producer issues its static range only and the consumers flush on segment changes.
+template <int G, bool CB, bool DYN>
 __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int cta) {
   constexpr int NT = Smem<G>::NT;
   const PoolArgs &p = a.p;
@@ -575,101 +583,161 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     mbar_init(&sm.csync, CONSUMER_WARPS);
     mbar_fence_init();
   }
+  split::Plan pl{};
   if (warp == CONSUMER_WARPS) {  // the producer warp locates this CTA's range
     long long lo, n;
     int b0, kvh0, local0, np0, hl0;
-    locate_range(p, a.n_hist, cta, lo, n, b0, kvh0, local0, np0, hl0);
+    locate_range(p, a.n_hist, cta, DYN, lo, n, b0, kvh0, local0, np0, hl0, pl);
     if (lane == 0) {
       sm.range_lo = lo; sm.range_n = n; sm.b0 = b0; sm.kvh0 = kvh0; sm.local0 = local0; sm.np0 = np0; sm.hl0 = hl0;
+      sm.n_dyn = pl.n_dyn;
     }
   }
   __syncthreads();
   const long long n = sm.range_n;
-  if (n <= 0) return;
+  if (n <= 0 && (!DYN || sm.n_dyn == 0)) return;
 
   if (warp == CONSUMER_WARPS) {
     // ---------------- producer warp: up to STAGE_PAGES pages of one segment per stage ----------------
     // Lane i owns page i of a stage and issues its bulk copies.  The page-table entries are read 32 at a
     // time (lane i holds entry pt_base + i of sequence b; every KV head of a sequence shares them), so
     // that most stages issue their copies without a round trip of their own.  hist_len is read once per
-    // sequence.
+    // sequence.  A stage carries its partial slot (slot0 + segment: the static range's slot0 = cta, chunk
+    // k's dyn_slot0 + k); the consumers flush when it changes.
     const uint64_t stream_pol = l2_evict_first();
-    int b = sm.b0, kvh = sm.kvh0, local = sm.local0;
-    int np = sm.np0, hl = sm.hl0;
     int stage = 0, it = 0;
     uint32_t phase = 0;
-    long long done = 0;
     int pt_base = -1, pt_b = -1, ptv = -1;
-    while (done < n) {
-      bool abort = false;
-      if (it >= NSTAGE) {  // every page slot of the stage released by its consumer warp
-        bool okw = true;
-        if (lane < STAGE_PAGES) okw = mbar_wait_bounded(&sm.empty[stage][lane], phase ^ 1);
-        abort = !__all_sync(FULL, okw);
-        if (abort && lane == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
-      }
-      const int seg = b * p.Hkv + kvh;
-      const int cnt = abort ? 0 : (int)min((long long)STAGE_PAGES, min(n - done, (long long)(np - local)));
-      if (cnt > 0 && (b != pt_b || local < pt_base || local + cnt > pt_base + 32)) {
-        pt_b = b;
-        pt_base = local;
-        ptv = local + lane < np ? ld_hint(p.page_table + (size_t)b * p.max_pages + local + lane, l2_evict_last()) : -1;
-      }
-      int pp = __shfl_sync(FULL, ptv, (local - pt_base + lane) & 31), ntk = 0;
-      if (lane >= cnt) pp = -1;
-      if (lane < cnt) {
-        const int lp = local + lane;
-        ntk = min(PAGE, hl - lp * PAGE);
-        if (pp < 0 || pp >= p.num_pages) {
-          atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
-          pp = -1;
+    int last_seg = sm.b0 * p.Hkv + sm.kvh0, last_slot = -1;
+    bool abort = false;
+    // pages [start, start + cnt_all) from position (b, kvh, local); `final` marks the stage that ends the CTA
+    auto issue = [&](long long cnt_all, int b, int kvh, int local, int np, int hl, int slot0, bool final) {
+      long long done = 0;
+      while (done < cnt_all && !abort) {
+        if (it >= NSTAGE) {  // every page slot of the stage released by its consumer warp
+          bool okw = true;
+          if (lane < STAGE_PAGES) okw = mbar_wait_bounded(&sm.empty[stage][lane], phase ^ 1);
+          abort = !__all_sync(FULL, okw);
+          if (abort && lane == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
         }
-      }
-      const bool have = pp >= 0;
-      if (lane < STAGE_PAGES) sm.meta_ntok[stage][lane] = have ? ntk : 0;
-      if (lane == 0) {
-        sm.meta_seg[stage] = seg;
-        sm.meta_flags[stage] = (done + cnt >= n ? 1 : 0) | (abort ? 2 : 0);
-      }
-      __syncwarp();  // the stage's metadata is written before any of its slots can complete
-      if (lane < STAGE_PAGES) {
-        uint64_t *bar = &sm.full[stage][lane];
-        if (have) {
-          mbar_arrive_expect_tx(bar, (uint32_t)PAGE_BYTES);
-          uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
-          const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
-          bulk_g2s_hint(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar, stream_pol);
-          bulk_g2s_hint(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar, stream_pol);
-          bulk_g2s_hint(dst + OFF_KS, p.scale_k + row, 128, bar, stream_pol);
-          bulk_g2s_hint(dst + OFF_KZ, p.zero_k + row, 128, bar, stream_pol);
-          bulk_g2s_hint(dst + OFF_VS, p.scale_v + row, 128, bar, stream_pol);
-          bulk_g2s_hint(dst + OFF_VZ, p.zero_v + row, 128, bar, stream_pol);
-        } else {
-          mbar_arrive(bar);
+        const int seg = b * p.Hkv + kvh;
+        const int cnt = abort ? 0 : (int)min((long long)STAGE_PAGES, min(cnt_all - done, (long long)(np - local)));
+        if (cnt > 0 && (b != pt_b || local < pt_base || local + cnt > pt_base + 32)) {
+          pt_b = b;
+          pt_base = local;
+          ptv = local + lane < np ? ld_hint(p.page_table + (size_t)b * p.max_pages + local + lane, l2_evict_last()) : -1;
         }
-      }
-      if (abort) {
-        // wait (bounded) for the copies still in flight into stages the consumers may not read
-        if (lane < STAGE_PAGES)
-          for (int k = max(0, it - NSTAGE + 1); k < it; ++k)
-            mbar_wait_bounded(&sm.full[k % NSTAGE][lane], (uint32_t)((k / NSTAGE) & 1));
-        break;
-      }
-      done += cnt;
-      local += cnt;
-      if (local == np && done < n) {
-        local = 0;
-        if (++kvh == p.Hkv) {
-          kvh = 0;
-          do { ++b; } while (b < p.B && npages_of(p, b) == 0);
-          if (b < p.B) {
-            np = npages_of(p, b);
-            hl = max(0, min(split::hist_len_of(p, b), p.max_pages * PAGE));
+        int pp = __shfl_sync(FULL, ptv, (local - pt_base + lane) & 31), ntk = 0;
+        if (lane >= cnt) pp = -1;
+        if (lane < cnt) {
+          const int lp = local + lane;
+          ntk = min(PAGE, hl - lp * PAGE);
+          if (pp < 0 || pp >= p.num_pages) {
+            atomicOr(p.err, OSCAR_DEVERR_PAGE_INDEX);
+            pp = -1;
           }
         }
+        const bool have = pp >= 0;
+        if (lane < STAGE_PAGES) sm.meta_ntok[stage][lane] = have ? ntk : 0;
+        if (lane == 0) {
+          sm.meta_seg[stage] = seg;
+          if constexpr (DYN) sm.meta_slot[stage] = slot0 + seg;
+          sm.meta_flags[stage] = ((final && done + cnt >= cnt_all) ? 1 : 0) | (abort ? 2 : 0);
+        }
+        if constexpr (DYN) {
+          last_seg = seg;
+          last_slot = slot0 + seg;
+        }
+        __syncwarp();  // the stage's metadata is written before any of its slots can complete
+        if (lane < STAGE_PAGES) {
+          uint64_t *bar = &sm.full[stage][lane];
+          if (have) {
+            mbar_arrive_expect_tx(bar, (uint32_t)PAGE_BYTES);
+            uint8_t *dst = sm.ring[stage] + lane * PAGE_BYTES;
+            const size_t row = ((size_t)pp * p.Hkv + kvh) * PAGE;
+            bulk_g2s_hint(dst + OFF_KC, p.codes_k + row * (D / 4), 2048, bar, stream_pol);
+            bulk_g2s_hint(dst + OFF_VC, p.codes_v + row * (D / 4), 2048, bar, stream_pol);
+            bulk_g2s_hint(dst + OFF_KS, p.scale_k + row, 128, bar, stream_pol);
+            bulk_g2s_hint(dst + OFF_KZ, p.zero_k + row, 128, bar, stream_pol);
+            bulk_g2s_hint(dst + OFF_VS, p.scale_v + row, 128, bar, stream_pol);
+            bulk_g2s_hint(dst + OFF_VZ, p.zero_v + row, 128, bar, stream_pol);
+          } else {
+            mbar_arrive(bar);
+          }
+        }
+        if (abort) {
+          // wait (bounded) for the copies still in flight into stages the consumers may not read
+          if (lane < STAGE_PAGES)
+            for (int k = max(0, it - NSTAGE + 1); k < it; ++k)
+              mbar_wait_bounded(&sm.full[k % NSTAGE][lane], (uint32_t)((k / NSTAGE) & 1));
+          return;
+        }
+        done += cnt;
+        local += cnt;
+        if (local == np && done < cnt_all) {
+          local = 0;
+          if (++kvh == p.Hkv) {
+            kvh = 0;
+            do { ++b; } while (b < p.B && npages_of(p, b) == 0);
+            if (b < p.B) {
+              np = npages_of(p, b);
+              hl = max(0, min(split::hist_len_of(p, b), p.max_pages * PAGE));
+            }
+          }
+        }
+        ++it;
+        if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
       }
-      ++it;
-      if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
+    };
+    // the static range, then (dynamic tail) chunks while any are left; one call site of issue() keeps the
+    // producer's code small
+    const bool dyn = DYN && sm.n_dyn > 0;
+    const long long dyn_slot0 = (long long)a.n_hist + 7LL * p.B * p.Hkv;
+    bool static_done = n <= 0, waited = false;
+    while (!abort) {
+      long long cnt_all;
+      int b, kvh, local, np, hl, slot0;
+      bool final;
+      if (!static_done) {
+        static_done = true;
+        cnt_all = n; b = sm.b0; kvh = sm.kvh0; local = sm.local0; np = sm.np0; hl = sm.hl0; slot0 = cta;
+        final = !dyn;
+      } else {
+        if (!dyn) break;
+        if (!waited) {  // the chunk counter was zeroed by the query rotation, complete after this wait
+          pdl_wait();
+          waited = true;
+        }
+        long long k = 0;
+        if (lane == 0) k = (long long)atomicAdd(a.dyn_ctr, 1ull);
+        k = __shfl_sync(FULL, k, 0);
+        if (k >= pl.n_dyn) break;
+        const long long start = pl.static_pages + k * pl.dyn_pages;
+        cnt_all = min(pl.dyn_pages, pl.total - start);
+        split::locate_at(p, start, b, kvh, local, np, hl);
+        slot0 = (int)(dyn_slot0 + k);
+        final = false;
+      }
+      issue(cnt_all, b, kvh, local, np, hl, slot0, final);
+    }
+    if (DYN && dyn) {
+      if (!abort) {
+        // the terminal stage: no pages, the last slot (no flush), the end flag
+        if (it >= NSTAGE) {
+          bool okw = true;
+          if (lane < STAGE_PAGES) okw = mbar_wait_bounded(&sm.empty[stage][lane], phase ^ 1);
+          abort = !__all_sync(FULL, okw);
+          if (abort && lane == 0) atomicOr(p.err, OSCAR_DEVERR_TIMEOUT);
+        }
+        if (lane < STAGE_PAGES) sm.meta_ntok[stage][lane] = 0;
+        if (lane == 0) {
+          sm.meta_seg[stage] = last_seg;
+          sm.meta_slot[stage] = last_slot;
+          sm.meta_flags[stage] = 1 | (abort ? 2 : 0);
+        }
+        __syncwarp();
+        if (lane < STAGE_PAGES) mbar_arrive(&sm.full[stage][lane]);
+      }
     }
     return;
   }
@@ -679,7 +747,7 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
   uint32_t bq[NT][8][2];
   float kf[NT], zf[NT];
   // the first segment's query setup needs no pages: it overlaps the first bulk copies
-  int cur = sm.b0 * p.Hkv + sm.kvh0, stage = 0;
+  int cur = sm.b0 * p.Hkv + sm.kvh0, cur_slot = -1, stage = 0;
   ws.csync_par = 0;
   Levels lv{};
   setup_segment<G, CB>(a, sm.b0, sm.kvh0, bq, kf, zf, lv);
@@ -692,8 +760,18 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     const int flags = sm.meta_flags[stage];
     if (flags & 2) break;  // producer aborted
     const int seg = sm.meta_seg[stage];
-    if (seg != cur) {
-      if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
+    if constexpr (DYN) {
+      const int slot = sm.meta_slot[stage];
+      if (slot != cur_slot) {
+        if (cur_slot >= 0) flush(a, sm, ws, a.part + (size_t)cur_slot * G * PART_STRIDE);
+        cur_slot = slot;
+        if (seg != cur) {
+          cur = seg;
+          setup_segment<G, CB>(a, seg / p.Hkv, seg % p.Hkv, bq, kf, zf, lv);
+        }
+      }
+    } else if (seg != cur) {
+      flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
       cur = seg;
       setup_segment<G, CB>(a, seg / p.Hkv, seg % p.Hkv, bq, kf, zf, lv);
     }
@@ -705,10 +783,14 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
     if (flags & 1) break;
     if (++stage == NSTAGE) { stage = 0; phase ^= 1; }
   }
-  if (cur >= 0) flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
+  if constexpr (DYN) {
+    if (cur_slot >= 0) flush(a, sm, ws, a.part + (size_t)cur_slot * G * PART_STRIDE);
+  } else {
+    flush(a, sm, ws, a.part + ((size_t)cta + cur) * G * PART_STRIDE);
+  }
 }
 
-template <int G, bool CB>
+template <int G, bool CB, bool DYN>
 __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem<G> &sm = *reinterpret_cast<Smem<G> *>(smem_raw);
@@ -724,7 +806,7 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
       wait = true;  // q_rot is written by the query rotation that precedes this kernel
       return a.qrot + ((size_t)b * a.p.Hq + kvh * G) * D;
     });
-  else hist_role<G, CB>(a, sm, a.hist_first ? bid : bid - a.n_bf);
+  else hist_role<G, CB, DYN>(a, sm, a.hist_first ? bid : bid - a.n_bf);
   // every thread has waited for the query rotation before the grid completes: the merge's wait (and the
   // next step's query rotation, which overwrites the fragments) then follows it as well
   if (a.step) pdl_wait();
@@ -752,7 +834,7 @@ constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX *
 // in one CTA, one after the other, with one copy of R_v and one location of the partials.
 template <int G>
 __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
-                                                   const uint16_t *k_new, const uint16_t *v_new, int hpc) {
+                                                   const uint16_t *k_new, const uint16_t *v_new, int hpc, int dyn) {
   extern __shared__ float4 rvs4[];  // R_v of this KV head (row stride RV_LD floats), then the staged slots
   float *pst = reinterpret_cast<float *>(rvs4 + D * (RV_LD / 4));
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
@@ -800,16 +882,28 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
     __threadfence();
     s_last_all = atomicAdd(p.sync, 1) == (int)(gridDim.x * gridDim.y * gridDim.z) - 1;
   }
-  int nh = 0, i0 = 0;
+  // the segment's pages [start, end): the static ranges' slots i0 + seg .. (nh of them), then the dynamic
+  // chunks' slots dyn_slot0 + k0 + seg .. (nd of them)
+  int nh = 0, i0 = 0, nd = 0;
+  long long k0 = 0;
   if (np > 0) {
-    const long long chunk = (s_total + n_hist - 1) / n_hist;
+    const split::Plan pl = split::plan_of(s_total, n_hist, dyn != 0);
     const long long start = s_pref + (long long)kvh * np, end = start + np;
-    i0 = (int)(start / chunk);
-    nh = (int)((end - 1) / chunk) - i0 + 1;
+    const long long send = min(end, pl.static_pages);
+    if (start < send) {
+      i0 = (int)(start / pl.chunk);
+      nh = (int)((send - 1) / pl.chunk) - i0 + 1;
+    }
+    if (end > pl.static_pages) {
+      k0 = (max(start, pl.static_pages) - pl.static_pages) / pl.dyn_pages;
+      nd = (int)((end - 1 - pl.static_pages) / pl.dyn_pages - k0 + 1);
+    }
   }
-  // (the debug build checks the located history slots against the workspace's n_hist + B * Hkv)
+  const long long dyn_slot0 = (long long)n_hist + 7LL * p.B * p.Hkv;
+  // (the debug build checks the located slots against the workspace's slot ranges)
   if (!OSCAR_DCHECK(nh == 0 || ((long long)i0 + seg + nh <= (long long)n_hist + p.B * p.Hkv && i0 >= 0), p.err)) nh = 0;
-  const int nrot = nh + (step ? 1 : 0);  // rotated-space partials: history (+ the demoted token)
+  if (!OSCAR_DCHECK(nd == 0 || (k0 + nd <= split::max_dyn_chunks(n_hist) && k0 >= 0), p.err)) nd = 0;
+  const int nrot = nh + nd + (step ? 1 : 0);  // rotated-space partials: history (+ the demoted token)
   const int nparts = nrot + 5;
   const size_t stride = (size_t)G * PART_STRIDE;
   __syncthreads();  // s_last_all
@@ -825,8 +919,11 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
   const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride + (size_t)h * PART_STRIDE;
   const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
+  const float *yp = part + ((size_t)dyn_slot0 + (size_t)k0 + seg) * stride + (size_t)h * PART_STRIDE;
   auto slot = [&](int i) {
-    return i < nh ? hp + (size_t)i * stride : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
+    return i < nh ? hp + (size_t)i * stride
+           : i < nh + nd ? yp + (size_t)(i - nh) * stride
+           : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
   };
   // The partial slots are staged in shared memory, PMAX per round, by 16-byte loads of every thread
   // (one round trip); warp 0 forms the round's maximum, the weights and their sum once, and the
@@ -944,8 +1041,8 @@ static int resident_ctas() {
     int sms = 148, occ = 1;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int smem = (int)sizeof(v1::Smem<G>);
-    cudaFuncSetAttribute(v1::attn_kernel<G, CB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v1::attn_kernel<G, CB>, v1::THREADS, smem) != cudaSuccess ||
+    cudaFuncSetAttribute(v1::attn_kernel<G, CB, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, v1::attn_kernel<G, CB, false>, v1::THREADS, smem) != cudaSuccess ||
         occ < 1)
       occ = 1;
     return sms * occ;
@@ -975,18 +1072,24 @@ int v1_hist_ctas(const PoolArgs &p) {
   return (int)(n < 1 ? 1 : n);
 }
 
-size_t v1_ws_bytes(const PoolArgs &p) {
+// Partial slots: history (CTA index + segment index), 5 BF16 and one demoted-token slot per segment, then
+// (dynamic tail) chunk index + segment index.
+static size_t v1_slots(const PoolArgs &p, bool dyn) {
+  const int nh = v1_hist_ctas(p);
+  return (size_t)nh + (size_t)p.B * p.Hkv * 7 + (dyn ? (size_t)split::max_dyn_chunks(nh) + (size_t)p.B * p.Hkv : 0);
+}
+size_t v1_ws_bytes(const PoolArgs &p, bool dyn) {
   const int G = p.Hq / p.Hkv;
-  // history slots (CTA index + segment index), 5 BF16 slots and one demoted-token slot per segment
-  const size_t slots = (size_t)v1_hist_ctas(p) + (size_t)p.B * p.Hkv * 7;
   const size_t frag = (size_t)p.B * p.Hkv * (G > 4 ? 36 : 18) * 32 * sizeof(uint32_t);
-  return (size_t)p.B * p.Hq * D * sizeof(float) + frag + slots * G * PART_STRIDE * sizeof(float);
+  return (size_t)p.B * p.Hq * D * sizeof(float) + frag + v1_slots(p, dyn) * G * PART_STRIDE * sizeof(float) +
+         (dyn ? 16 : 0);
 }
 
 // Workspace: [q_rot][query fragments][partial slots].  k_new != NULL: the decode-step form.
 template <int G>
 static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
-                               cudaStream_t s, const uint16_t *k_new = nullptr, const uint16_t *v_new = nullptr) {
+                               cudaStream_t s, bool dyn, const uint16_t *k_new = nullptr,
+                               const uint16_t *v_new = nullptr) {
   v1::Args a;
   a.p = p;
   a.q = q;
@@ -996,6 +1099,10 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.part = reinterpret_cast<float *>(frag + (size_t)p.B * p.Hkv * v1::frag_words<G>() * 32);
   a.sm_log2 = sm_scale * 1.4426950408889634f;
   a.n_hist = v1_hist_ctas(p);
+  // the dynamic tail only where the pool can hold 64 history pages per history CTA (split::plan_of)
+  dyn = dyn && (long long)p.B * p.Hkv * p.max_pages >= 64LL * a.n_hist;
+  a.dyn = dyn ? 1 : 0;
+  a.dyn_ctr = dyn ? reinterpret_cast<unsigned long long *>(a.part + v1_slots(p, true) * G * PART_STRIDE) : nullptr;
   const int nbf = p.B * p.Hkv * 5;
   a.n_bf = nbf;
   {
@@ -1003,7 +1110,8 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
     a.hist_first = nbf > slots / 4 ? 1 : 0;
   }
   const int smem = (int)sizeof(v1::Smem<G>);
-  auto attn = has_codebook(p) ? v1::attn_kernel<G, true> : v1::attn_kernel<G, false>;
+  auto attn = has_codebook(p) ? (dyn ? v1::attn_kernel<G, true, true> : v1::attn_kernel<G, true, false>)
+                              : (dyn ? v1::attn_kernel<G, false, true> : v1::attn_kernel<G, false, false>);
   cudaError_t e = cudaFuncSetAttribute(attn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   a.step = k_new != nullptr;
@@ -1014,13 +1122,13 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   if ((e = cudaFuncSetAttribute(v1::merge_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)v1::MERGE_SMEM)) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2)) !=
+  if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2, a.dyn_ctr)) !=
       cudaSuccess)
     return e;
   profile_begin(OSCAR_PROFILE_HISTORY, s);
   if ((e = launch_pdl(attn, dim3(a.n_hist + nbf), dim3(v1::THREADS), smem, s, a)) != cudaSuccess) return e;
   profile_end(OSCAR_PROFILE_HISTORY, s);
-  return launch_merge_v1(p, (const float *)a.part, a.n_hist, out, k_new, v_new, s);
+  return launch_merge_v1(p, (const float *)a.part, a.n_hist, out, k_new, v_new, s, dyn);
 }
 
 // The merge of a decode launch whose partial slots follow this file's layout (history slots cta + segment
@@ -1042,13 +1150,13 @@ static int merge_heads_per_cta(const PoolArgs &p) {
 }
 
 cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
-                            const uint16_t *v_new, cudaStream_t s) {
+                            const uint16_t *v_new, cudaStream_t s, bool dyn) {
   const int hpc = merge_heads_per_cta(p);
   auto go = [&](auto kernel) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v1::MERGE_SMEM);
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, dim3(p.Hq / p.Hkv / hpc, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p, part, n_hist,
-                      out, k_new, v_new, hpc);
+                      out, k_new, v_new, hpc, dyn ? 1 : 0);
   };
   switch (p.Hq / p.Hkv) {
     case 1: return go(v1::merge_kernel<1>);
@@ -1060,23 +1168,23 @@ cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, fl
 }
 
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool dyn) {
   switch (p.Hq / p.Hkv) {
-    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s);
-    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s);
-    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s);
-    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s);
+    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s, dyn);
+    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s, dyn);
+    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s, dyn);
+    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s, dyn);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
-                           float *out, float sm_scale, float *ws, cudaStream_t s) {
+                           float *out, float sm_scale, float *ws, cudaStream_t s, bool dyn) {
   switch (p.Hq / p.Hkv) {
-    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s, k_new, v_new);
-    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s, k_new, v_new);
-    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s, k_new, v_new);
-    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s, k_new, v_new);
+    case 1: return launch_v1_g<1>(p, q, out, sm_scale, ws, s, dyn, k_new, v_new);
+    case 2: return launch_v1_g<2>(p, q, out, sm_scale, ws, s, dyn, k_new, v_new);
+    case 4: return launch_v1_g<4>(p, q, out, sm_scale, ws, s, dyn, k_new, v_new);
+    case 8: return launch_v1_g<8>(p, q, out, sm_scale, ws, s, dyn, k_new, v_new);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -89,18 +89,24 @@ cudaError_t launch_decode(const PoolArgs &p, const uint16_t *q, float *out, floa
                           cudaStream_t s);
 
 // decode_v1.cu (tensor-core path, group size 128)
-size_t v1_ws_bytes(const PoolArgs &p);
+// Workspace bytes: dyn = false the minimum, dyn = true with the dynamic tail of the history split (its
+// partial slots and chunk counter); a launch with dyn uses that tail.
+size_t v1_ws_bytes(const PoolArgs &p, bool dyn);
 cudaError_t launch_decode_v1(const PoolArgs &p, const uint16_t *q, float *out, float sm_scale, float *ws,
-                             cudaStream_t s);
+                             cudaStream_t s, bool dyn);
 // The decode step for group size 128: the query rotation, the attention kernel and the merge, which
 // performs the demotion and the append.
 cudaError_t launch_step_v1(const PoolArgs &p, const uint16_t *k_new, const uint16_t *v_new, const uint16_t *q,
-                           float *out, float sm_scale, float *ws, cudaStream_t s);
+                           float *out, float sm_scale, float *ws, cudaStream_t s, bool dyn);
 
 // The merge kernel of decode_v1.cu (LSE merge, o . R_v^T, normalisation; k_new != NULL: the decode-step form
 // with the append and the counter update) over partial slots in its layout.
+// The smallest decode workspace a call on this pool accepts (api.cu; validates the pool).
+oscar_status_t decode_workspace_min(const oscar_pool *pool, size_t *bytes);
+
+// dyn: the history partials include the dynamic tail's (decode_v1.cu's attention with dyn).
 cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
-                            const uint16_t *v_new, cudaStream_t s);
+                            const uint16_t *v_new, cudaStream_t s, bool dyn = false);
 
 // decode_tc.cu (tcgen05 path, uniform levels, group sizes 32, 64, 128): history CTAs (one per SM), workspace
 // bytes, and the launch (query rotation + operand images, history, BF16 + demotion, merge); k_new != NULL:

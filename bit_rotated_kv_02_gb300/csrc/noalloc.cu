@@ -59,7 +59,7 @@ extern "C" oscar_status_t oscar_decode_attention_noalloc(const oscar_pool *pool,
                                                          float softmax_scale, oscar_stream_t stream) {
   char msg[256];
   size_t need = 0;
-  oscar_status_t st = oscar_decode_workspace_size(pool, 0, &need);  // validates the pool
+  oscar_status_t st = oscar::decode_workspace_min(pool, &need);  // validates the pool
   if (st != OSCAR_OK) return st;
   if (need > OSCAR_NOALLOC_SCRATCH_BYTES) {
     snprintf(msg, sizeof msg,

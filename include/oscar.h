@@ -262,8 +262,11 @@ oscar_status_t oscar_append_kv(const oscar_pool *pool, const oscar_bf16 *k_new, 
  *   num_splits      history split factor per (sequence, KV head) for pools with a codebook and group
  *                   size 32/64; 0 = choose to fill the GPU.  Every other pool balances the history
  *                   pages of all (sequence, KV head) pairs over a GPU-filling grid itself and ignores it.
- *   ws, ws_bytes    workspace of at least oscar_decode_workspace_size() bytes (same pool shape and
- *                   num_splits), 16-byte aligned
+ *   ws, ws_bytes    workspace, 16-byte aligned: oscar_decode_workspace_size() bytes (same pool shape and
+ *                   num_splits) enable every part of the decode; a smaller one down to the pool's minimum
+ *                   is accepted (group size 128 then splits the history statically, without the dynamic
+ *                   tail in which CTAs that finish early take the remaining pages), less is refused with
+ *                   OSCAR_ERR_WORKSPACE
  * out[b][h] = sum over all pool tokens of softmax(score) * value, with score = q·k*scale for sink
  * and recent tokens and (q·R_k)·k_rot*scale for history tokens, whose values enter as v_rot·R_v^T.
  * Kernels: uniform pools of group size 128 run the warp-MMA history kernel, uniform pools of group

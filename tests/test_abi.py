@@ -57,9 +57,12 @@ def test_decode_rejects_missing_workspace(lib):
     n = C.c_size_t(0)
     assert lib.oscar_decode_workspace_size(C.byref(p), 4, C.byref(n)) == 0 and n.value > 0
     assert lib.oscar_decode_attention(C.byref(p), FAKE, FAKE, 0.088, 4, None, 0, None) == 3
-    assert lib.oscar_decode_attention(C.byref(p), FAKE, FAKE, 0.088, 4, FAKE, n.value - 1, None) == 3
+    assert lib.oscar_decode_attention(C.byref(p), FAKE, FAKE, 0.088, 4, FAKE, 4096, None) == 3
     assert lib.oscar_decode_attention(C.byref(p), FAKE, FAKE, -1.0, 4, FAKE, n.value, None) == 1
     assert lib.oscar_decode_attention(C.byref(p), None, FAKE, 0.088, 4, FAKE, n.value, None) == 1
+    # q and out must be memory the kernels can reach: a bad pointer is refused on the host
+    assert lib.oscar_decode_attention(C.byref(p), FAKE, FAKE, 0.088, 4, FAKE, n.value, None) == 1
+    assert b"page-locked" in lib.oscar_last_error_string()
 
 
 def test_quantize_validation(lib):
