@@ -550,6 +550,11 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
         if (j >= C::RING && !warp_wait(bar.empty + stage, ((j / C::RING) - 1) & 1, p, misc)) { ok = false; break; }
         const int seg = b * p.Hkv + kvh;
         const int cnt = (int)min(2ll, min(n_pages - done, (long long)(np - local)));
+        if (cnt <= 0) {  // counters inconsistent with the range (changed during the launch): stop; the other
+          if (lane == 0) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);  // roles end at their bounded waits
+          ok = false;
+          break;
+        }
         int flags = 0;
         const bool new_seg = seg != cur_seg;
         if (new_seg) {

@@ -622,6 +622,10 @@ __device__ __forceinline__ void hist_role(const Args &a, Smem<G> &sm, const int 
         }
         const int seg = b * p.Hkv + kvh;
         const int cnt = abort ? 0 : (int)min((long long)STAGE_PAGES, min(cnt_all - done, (long long)(np - local)));
+        if (cnt <= 0 && !abort) {  // counters inconsistent with the range (changed during the launch): stop
+          abort = true;
+          if (lane == 0) atomicOr(p.err, OSCAR_DEVERR_COUNTERS);
+        }
         if (cnt > 0 && (b != pt_b || local < pt_base || local + cnt > pt_base + 32)) {
           pt_b = b;
           pt_base = local;
