@@ -65,7 +65,7 @@ struct Args {
   int n_hist;          // history CTAs
   int n_bf;            // BF16 CTAs
   // block order: BF16 CTAs first (they and the history CTAs fit in one wave), or, when the BF16 CTAs
-  // outnumber a quarter of the resident slots (large batches), the history CTAs first, so that they start at
+  // outnumber a sixth of the resident slots (large batches), the history CTAs first, so that they start at
   // once and the BF16 CTAs run in the remaining slots alongside them instead of in waves before them
   int hist_first;
   // dynamic tail of the history split (split::plan_of): enabled when the workspace holds its partial slots;
@@ -832,33 +832,43 @@ __global__ void __launch_bounds__(THREADS, G <= 4 ? 3 : 2) attn_kernel(Args a) {
 constexpr int MT = 512;
 constexpr int RV_LD = D + 4;  // padded row stride of the shared copy of R_v
 constexpr int PMAX = 96;      // partial slots staged in shared memory per round
+constexpr int PMAX_WIDE = 48; // the same in the wide build (two CTAs per SM)
 constexpr uint32_t PART_BYTES = PART_STRIDE * sizeof(float);
-constexpr size_t MERGE_SMEM = (size_t)D * RV_LD * sizeof(float) + (size_t)PMAX * PART_BYTES;
+__host__ __device__ constexpr size_t merge_smem(bool wide) {
+  return (size_t)D * RV_LD * sizeof(float) + (size_t)(wide ? PMAX_WIDE : PMAX) * PART_BYTES;
+}
 // hpc query heads per CTA (grid G / hpc x Hkv x B): large grids merge several heads of a (sequence, KV head)
-// in one CTA, one after the other, with one copy of R_v and one location of the partials.
-template <int G>
-__global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
+// in one CTA, one after the other, with one copy of R_v and one location of the partials; their partials
+// are staged together (one round trip) when they fit.  WIDE: the build for those grids, with a smaller
+// staging buffer so that two CTAs share an SM.
+template <int G, bool WIDE>
+__global__ void __launch_bounds__(MT, WIDE ? 2 : 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
                                                    const uint16_t *k_new, const uint16_t *v_new, int hpc, int dyn) {
+  constexpr int PM = WIDE ? PMAX_WIDE : PMAX;
   extern __shared__ float4 rvs4[];  // R_v of this KV head (row stride RV_LD floats), then the staged slots
   float *pst = reinterpret_cast<float *>(rvs4 + D * (RV_LD / 4));
   __shared__ float Osl[4][D], Obs[4][D], Orot[D];
-  __shared__ float pw[PMAX], s_stat[2];
+  __shared__ float pw[PM], s_stat[2];
   __shared__ long long s_pref, s_total;
   __shared__ int s_last_all;
   const int kvh = blockIdx.y, b = blockIdx.z, seg = b * p.Hkv + kvh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ch = tid & (D - 1), sl = tid >> 7;
   const bool step = k_new != nullptr;
-  // R_v rows into shared memory (coalesced 16-byte loads)
+  // R_v rows into shared memory (coalesced 16-byte loads; the wide build in two batches, for its registers)
   {
     const float4 *R4 = reinterpret_cast<const float4 *>(p.R_v + (size_t)kvh * D * D);
-    float4 rv[8];
+    constexpr int NB = WIDE ? 4 : 8;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) rv[k] = R4[tid + MT * k];
+    for (int k0 = 0; k0 < 8; k0 += NB) {
+      float4 rv[NB];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int i = tid + MT * k;
-      rvs4[(i / (D / 4)) * (RV_LD / 4) + i % (D / 4)] = rv[k];
+      for (int k = 0; k < NB; ++k) rv[k] = R4[tid + MT * (k0 + k)];
+#pragma unroll
+      for (int k = 0; k < NB; ++k) {
+        const int i = tid + MT * (k0 + k);
+        rvs4[(i / (D / 4)) * (RV_LD / 4) + i % (D / 4)] = rv[k];
+      }
     }
   }
   StepState st{};
@@ -918,52 +928,69 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
   if (last_all && tid < p.B) sa = step_state(p, tid);
   pdl_wait();
   pdl_trigger();
-  for (int hh = 0; hh < hpc; ++hh) {
-  const int h = blockIdx.x * hpc + hh;
-  const float *hp = part + ((size_t)i0 + seg) * stride + (size_t)h * PART_STRIDE;
-  const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride + (size_t)h * PART_STRIDE;
-  const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride + (size_t)h * PART_STRIDE;
-  const float *yp = part + ((size_t)dyn_slot0 + (size_t)k0 + seg) * stride + (size_t)h * PART_STRIDE;
+  // slot i of the segment (every head's values), i < nparts: history, dynamic chunks, demoted token, BF16
+  const float *hp = part + ((size_t)i0 + seg) * stride;
+  const float *dp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv * 6 + seg) * stride;
+  const float *bp = part + ((size_t)n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5) * stride;
+  const float *yp = part + ((size_t)dyn_slot0 + (size_t)k0 + seg) * stride;
   auto slot = [&](int i) {
     return i < nh ? hp + (size_t)i * stride
            : i < nh + nd ? yp + (size_t)(i - nh) * stride
            : i < nrot ? dp : bp + (size_t)(i - nrot) * stride;
   };
-  // The partial slots are staged in shared memory, PMAX per round, by 16-byte loads of every thread
-  // (one round trip); warp 0 forms the round's maximum, the weights and their sum once, and the
-  // threads (slice, channel) add the weighted outputs of every fourth slot.  Rounds combine with a
-  // running maximum.
-  float M = -INFINITY, L = 0.f, acc = 0.f, accb = 0.f;
-  constexpr int V4 = PART_STRIDE / 4;  // float4 per staged slot
-  for (int r0 = 0; r0 < nparts; r0 += PMAX) {
-    const int n = min(PMAX, nparts - r0);
-    {
-      constexpr int PER = (PMAX * V4 + MT - 1) / MT;
-      float4 v[PER];
+  // Staging: n entries into shared memory by 16-byte loads of every thread (one round trip); entry e holds
+  // the PART_STRIDE floats of query head blockIdx.x * hpc + hh of slot i, (hh, i) = at(e).
+  constexpr int V4 = PART_STRIDE / 4;  // float4 per staged entry
+  auto stage = [&](int n, auto at) {
+    constexpr int PER = (PM * V4 + MT - 1) / MT;
+    float4 v[PER];
 #pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int e = tid + MT * k;
-        if (e < n * V4) v[k] = reinterpret_cast<const float4 *>(slot(r0 + e / V4))[e % V4];
-      }
-#pragma unroll
-      for (int k = 0; k < PER; ++k) {
-        const int e = tid + MT * k;
-        if (e < n * V4) reinterpret_cast<float4 *>(pst)[e] = v[k];
+    for (int k = 0; k < PER; ++k) {
+      const int e = tid + MT * k;
+      if (e < n * V4) {
+        const int2 hi = at(e / V4);
+        v[k] = reinterpret_cast<const float4 *>(slot(hi.y) + (size_t)(blockIdx.x * hpc + hi.x) * PART_STRIDE)[e % V4];
       }
     }
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int e = tid + MT * k;
+      if (e < n * V4) reinterpret_cast<float4 *>(pst)[e] = v[k];
+    }
+  };
+  // every head's partials in one round when they fit (entry hh * nparts + i)
+  const bool together = hpc > 1 && nparts * hpc <= PM;
+  if (together) {
+    stage(nparts * hpc, [&](int e) { return make_int2(e / nparts, e % nparts); });
     __syncthreads();
+  }
+  for (int hh = 0; hh < hpc; ++hh) {
+  const int h = blockIdx.x * hpc + hh;
+  // Rounds of PM staged slots (one round when staged together above); warp 0 forms the round's maximum,
+  // the weights and their sum once, and the threads (slice, channel) add the weighted outputs of every
+  // fourth slot.  Rounds combine with a running maximum.
+  float M = -INFINITY, L = 0.f, acc = 0.f, accb = 0.f;
+  for (int r0 = 0; r0 < nparts; r0 += PM) {
+    const int n = min(PM, nparts - r0);
+    const float *ps = pst;
+    if (together) {
+      ps = pst + (size_t)hh * nparts * PART_STRIDE;
+    } else {
+      stage(n, [&](int e) { return make_int2(hh, r0 + e); });
+      __syncthreads();
+    }
     if (warp == 0) {
       float mr = -INFINITY;
-      for (int i = lane; i < n; i += 32) mr = fmaxf(mr, pst[(size_t)i * PART_STRIDE + D]);
+      for (int i = lane; i < n; i += 32) mr = fmaxf(mr, ps[(size_t)i * PART_STRIDE + D]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(FULL, mr, o));
       const float Mn = fmaxf(M, mr);
       float lr = 0.f;
       for (int i = lane; i < n; i += 32) {
-        const float m = pst[(size_t)i * PART_STRIDE + D];
+        const float m = ps[(size_t)i * PART_STRIDE + D];
         const float w = m == -INFINITY ? 0.f : exp2f(m - Mn);
         pw[i] = w;
-        lr = fmaf(w, pst[(size_t)i * PART_STRIDE + D + 1], lr);
+        lr = fmaf(w, ps[(size_t)i * PART_STRIDE + D + 1], lr);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) lr += __shfl_xor_sync(FULL, lr, o);
@@ -977,7 +1004,7 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
     accb *= f;
     M = Mn;
     for (int i = sl; i < n; i += 4) {  // rotated-space partials and BF16 partials (original space) apart
-      const float w = pw[i], o = pst[(size_t)i * PART_STRIDE + ch];
+      const float w = pw[i], o = ps[(size_t)i * PART_STRIDE + ch];
       if (r0 + i < nrot) acc = fmaf(w, o, acc);
       else accb = fmaf(w, o, accb);
     }
@@ -1037,7 +1064,10 @@ __global__ void __launch_bounds__(MT, 1) merge_kernel(PoolArgs p, const float *p
 
 // ---------------------------------------------------------------------------------------------
 // Grid of the attention kernel: BF16 CTAs (5 per sequence and KV head) first, then history CTAs
-// sized so that both fit in one wave of resident CTAs (history CTAs get at least 3/4 of it).
+// sized so that both fit in one wave of resident CTAs (history CTAs get at least 5/6 of it; when the BF16
+// CTAs outnumber the rest they run in waves in the remaining sixth, alongside the history CTAs: measured
+// on the 32k batch sweep, a quarter left the history CTAs too few slots and an eighth gained nothing more).
+constexpr int BF_SHARE = 6;
 template <int G, bool CB>
 static int resident_ctas() {
   static std::atomic<int> slots[kMaxDevices];
@@ -1069,7 +1099,7 @@ static bool has_codebook(const PoolArgs &p) { return p.cb_k != nullptr || p.cb_v
 int v1_hist_ctas(const PoolArgs &p) {
   const int slots = has_codebook(p) ? resident_ctas_for<true>(p.Hq / p.Hkv) : resident_ctas_for<false>(p.Hq / p.Hkv);
   const long long nbf = (long long)p.B * p.Hkv * 5;
-  long long n = slots - (nbf < slots / 4 ? nbf : slots / 4);
+  long long n = slots - (nbf < slots / BF_SHARE ? nbf : slots / BF_SHARE);
   if (n > 1000) n = 1000;
   const long long cap = (long long)p.B * p.Hkv * p.max_pages;
   if (cap < n) n = cap;
@@ -1111,7 +1141,7 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.n_bf = nbf;
   {
     const int slots = has_codebook(p) ? resident_ctas_for<true>(G) : resident_ctas_for<false>(G);
-    a.hist_first = nbf > slots / 4 ? 1 : 0;
+    a.hist_first = nbf > slots / BF_SHARE ? 1 : 0;
   }
   const int smem = (int)sizeof(v1::Smem<G>);
   auto attn = has_codebook(p) ? (dyn ? v1::attn_kernel<G, true, true> : v1::attn_kernel<G, true, false>)
@@ -1123,9 +1153,6 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
   a.v_new = v_new;
   // Step form: the attention reads only state the step leaves unchanged and its BF16 CTAs perform the
   // demotion (overlapping the history CTAs); the merge performs the append and the counter update.
-  if ((e = cudaFuncSetAttribute(v1::merge_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)v1::MERGE_SMEM)) != cudaSuccess)
-    return e;
   if ((e = launch_pdl(v1::qrot_kernel<G>, dim3(p.B * p.Hkv), dim3(512), 0, s, p, q, ws, frag, a.sm_log2, a.dyn_ctr)) !=
       cudaSuccess)
     return e;
@@ -1156,17 +1183,19 @@ static int merge_heads_per_cta(const PoolArgs &p) {
 cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
                             const uint16_t *v_new, cudaStream_t s, bool dyn) {
   const int hpc = merge_heads_per_cta(p);
+  const bool wide = hpc > 1;
+  const size_t smem = v1::merge_smem(wide);
   auto go = [&](auto kernel) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)v1::MERGE_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kernel, dim3(p.Hq / p.Hkv / hpc, p.Hkv, p.B), dim3(v1::MT), v1::MERGE_SMEM, s, p, part, n_hist,
-                      out, k_new, v_new, hpc, dyn ? 1 : 0);
+    return launch_pdl(kernel, dim3(p.Hq / p.Hkv / hpc, p.Hkv, p.B), dim3(v1::MT), smem, s, p, part, n_hist, out,
+                      k_new, v_new, hpc, dyn ? 1 : 0);
   };
   switch (p.Hq / p.Hkv) {
-    case 1: return go(v1::merge_kernel<1>);
-    case 2: return go(v1::merge_kernel<2>);
-    case 4: return go(v1::merge_kernel<4>);
-    case 8: return go(v1::merge_kernel<8>);
+    case 1: return go(v1::merge_kernel<1, false>);
+    case 2: return wide ? go(v1::merge_kernel<2, true>) : go(v1::merge_kernel<2, false>);
+    case 4: return wide ? go(v1::merge_kernel<4, true>) : go(v1::merge_kernel<4, false>);
+    case 8: return wide ? go(v1::merge_kernel<8, true>) : go(v1::merge_kernel<8, false>);
     default: return cudaErrorInvalidValue;
   }
 }
