@@ -488,12 +488,20 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
     const bool live_h = ALL_LIVE || 4 * nt + t < G;
     const float kf = kf_[nt], zf = zf_[nt];
     (void)h;
+    // score of row j = 2 mt + e: (S hi + S lo) * ks * kf + kz * zf, both rows of a tile in one paired op
     float sc[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int mt = j >> 1, e = j & 1;
-      const float v = fmaf((S[mt][nt][2 * e] + S[mt][nt][2 * e + 1]) * ks[j], kf, kz[j] * zf);
-      sc[j] = j < nvalid ? v : -INFINITY;
+    for (int mt = 0; mt < 4; ++mt) {
+      const float2 x = make_float2(S[mt][nt][0] + S[mt][nt][1], S[mt][nt][2] + S[mt][nt][3]);
+      const float2 v = ffma2(fmul2(x, make_float2(ks[2 * mt], ks[2 * mt + 1])), make_float2(kf, kf),
+                             fmul2(make_float2(kz[2 * mt], kz[2 * mt + 1]), make_float2(zf, zf)));
+      sc[2 * mt] = v.x;
+      sc[2 * mt + 1] = v.y;
+    }
+    if (nvalid < 8) {  // a partial page: rows past its last token
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j >= nvalid) sc[j] = -INFINITY;
     }
     // lazy rescaling: the head's maximum is formed across lanes only when some row exceeds the
     // reference by more than 2^LAZY (a warp vote on the lane maxima decides)
@@ -515,25 +523,32 @@ __device__ __forceinline__ void page_pass(const uint8_t *pb, int ntok, WarpState
     }
     // p * 2^tau = exp2(score - (m - tau)); l and the zero-point sum take p itself
     const float mref = ws.m2[nt] - (float)ws.tau;
-    float lsum = 0.f, zsum = 0.f;
+    float2 lsum = make_float2(0.f, 0.f), zsum = make_float2(0.f, 0.f);
     float wv[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float pr = fast_exp2(sc[j] - mref);  // 0 for rows past ntok (score -inf)
-      lsum += pr;
-      zsum = fmaf(pr, vz[j], zsum);
-      wv[j] = live_h ? pr * vs[j] : 0.f;
+    for (int mt = 0; mt < 4; ++mt) {
+      const float2 d = fsub2(make_float2(sc[2 * mt], sc[2 * mt + 1]), make_float2(mref, mref));
+      const float2 pr = make_float2(fast_exp2(d.x), fast_exp2(d.y));  // 0 for rows past ntok (score -inf)
+      lsum = fadd2(lsum, pr);
+      zsum = ffma2(pr, make_float2(vz[2 * mt], vz[2 * mt + 1]), zsum);
+      const float2 w = fmul2(pr, make_float2(vs[2 * mt], vs[2 * mt + 1]));
+      wv[2 * mt] = live_h ? w.x : 0.f;
+      wv[2 * mt + 1] = live_h ? w.y : 0.f;
     }
-    ws.l[nt] = fmaf(lsum, untau, ws.l[nt]);
-    ws.oz[nt] = fmaf(zsum, untau, ws.oz[nt]);
+    ws.l[nt] = fmaf(lsum.x + lsum.y, untau, ws.l[nt]);
+    ws.oz[nt] = fmaf(zsum.x + zsum.y, untau, ws.oz[nt]);
 #pragma unroll
     for (int pl = 0; pl < (CB ? 3 : 1); ++pl) {
       uint32_t wp[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float w = CB ? wv[j] * lv.dv[pl] : wv[j];
-        const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
-        wp[j] = pack_half2(hi, w - hi);                                      // (hi, lo)
+      for (int mt = 0; mt < 4; ++mt) {
+        float2 w = make_float2(wv[2 * mt], wv[2 * mt + 1]);
+        if (CB) w = fmul2(w, make_float2(lv.dv[pl], lv.dv[pl]));
+        const float2 hi = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xffffe000u),   // w to 11
+                                      __uint_as_float(__float_as_uint(w.y) & 0xffffe000u));  // significant bits
+        const float2 lo = fsub2(w, hi);
+        wp[2 * mt] = pack_half2(hi.x, lo.x);  // (hi, lo)
+        wp[2 * mt + 1] = pack_half2(hi.y, lo.y);
       }
 #pragma unroll
       for (int mt = 0; mt < 4; ++mt) {

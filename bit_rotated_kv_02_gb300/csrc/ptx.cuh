@@ -114,6 +114,41 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Paired float32 arithmetic (add / sub / mul / fma .rn.f32x2: two IEEE operations in one instruction on
+// a 64-bit register pair; each lane rounds exactly as the scalar operation does).
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, R;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n add.rn.f32x2 R, A, B;\n"
+      " mov.b64 {%0, %1}, R;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, R;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n sub.rn.f32x2 R, A, B;\n"
+      " mov.b64 {%0, %1}, R;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, R;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n mul.rn.f32x2 R, A, B;\n"
+      " mov.b64 {%0, %1}, R;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 A, B, C, R;\n mov.b64 A, {%2, %3};\n mov.b64 B, {%4, %5};\n mov.b64 C, {%6, %7};\n"
+      " fma.rn.f32x2 R, A, B, C;\n mov.b64 {%0, %1}, R;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 // Two floats -> fp16x2 (round to nearest even): low half = lo.
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
