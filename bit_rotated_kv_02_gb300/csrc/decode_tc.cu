@@ -964,24 +964,39 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
           tmem_ld_cols<NQG>(tmem + lane_addr + C::TM_S + C::NQ * (j % C::NSQ) + sg * NQG, s);
         }
         float sc[GH];
+        auto code_sum = [&](int h, int g) {  // head h's code sum of group g
+          if constexpr (C::QK8) {  // sum_t 16^t S_t by Horner (exact until the last two steps)
+            const float *st = s + (h * NG + g) * C::QT;
+            float sum = st[C::QT - 1];
+#pragma unroll
+            for (int t = C::QT - 2; t >= 0; --t) sum = fmaf(sum, 16.f, st[t]);
+            return sum;
+          } else if constexpr (C::QKG) {
+            return s[2 * GH * g + 2 * h] + s[2 * GH * g + 2 * h + 1];
+          } else {
+            return s[(h * NG + g) * 2] + s[(h * NG + g) * 2 + 1];
+          }
+        };
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
-          float acc = 0.f, zacc = 0.f;
+          float acc, zacc;
+          if constexpr (NG % 2 == 0) {  // groups in pairs: paired float32 products and sums
+            float2 a2 = make_float2(0.f, 0.f), z2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            float sum;
-            if constexpr (C::QK8) {  // sum_t 16^t S_t by Horner (exact until the last two steps)
-              const float *st = s + (h * NG + g) * C::QT;
-              sum = st[C::QT - 1];
-#pragma unroll
-              for (int t = C::QT - 2; t >= 0; --t) sum = fmaf(sum, 16.f, st[t]);
-            } else if constexpr (C::QKG) {
-              sum = s[2 * GH * g + 2 * h] + s[2 * GH * g + 2 * h + 1];
-            } else {
-              sum = s[(h * NG + g) * 2] + s[(h * NG + g) * 2 + 1];
+            for (int g = 0; g < NG; g += 2) {
+              a2 = ffma2(make_float2(code_sum(h, g), code_sum(h, g + 1)), make_float2(ks[g], ks[g + 1]), a2);
+              z2 = ffma2(make_float2(kz[g], kz[g + 1]), make_float2(zf[h][g], zf[h][g + 1]), z2);
             }
-            acc = fmaf(sum, ks[g], acc);
-            zacc = fmaf(kz[g], zf[h][g], zacc);
+            acc = a2.x + a2.y;
+            zacc = z2.x + z2.y;
+          } else {
+            acc = 0.f;
+            zacc = 0.f;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              acc = fmaf(code_sum(h, g), ks[g], acc);
+              zacc = fmaf(kz[g], zf[h][g], zacc);
+            }
           }
           sc[h] = valid ? fmaf(acc, kf[h], zacc) : -INFINITY;
         }
@@ -1065,17 +1080,36 @@ __global__ void __maxnreg__((Cfg<G, NG>::MAXREG)) hist_kernel(HArgs a) {
 #pragma unroll
         for (int g = 0; g < NG; ++g) vsu[g] = vs[g] * ut;
         uint32_t wp[GH * NG];  // (hi, lo) of head h, group g as one fp16x2: columns (h NG + g) 2 and + 1
+        auto split = [](float w) {  // w to 11 significant bits (hi) and the rest (lo), one packed conversion
+          const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);
+          const __half2 hl = __floats2half2_rn(hi, w - hi);
+          return *reinterpret_cast<const uint32_t *>(&hl);
+        };
 #pragma unroll
         for (int h = 0; h < GH; ++h) {
           const float pr = sc[h] == -INFINITY ? 0.f : fast_exp2(sc[h] - mref[h]);  // 0 past the tile's tokens
           lpart[h] += pr;
+          if constexpr (NG % 2 == 0) {  // groups in pairs: paired float32 products, sums and hi/lo splits
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            ozp[h][g] = fmaf(pr, vz[g], ozp[h][g]);
-            const float w = pr * vsu[g];
-            const float hi = __uint_as_float(__float_as_uint(w) & 0xffffe000u);  // w to 11 significant bits
-            const __half2 hl = __floats2half2_rn(hi, w - hi);  // one packed conversion for the pair
-            wp[h * NG + g] = *reinterpret_cast<const uint32_t *>(&hl);
+            for (int g = 0; g < NG; g += 2) {
+              const float2 prp = make_float2(pr, pr);
+              const float2 oz = ffma2(prp, make_float2(vz[g], vz[g + 1]), make_float2(ozp[h][g], ozp[h][g + 1]));
+              ozp[h][g] = oz.x;
+              ozp[h][g + 1] = oz.y;
+              const float2 w = fmul2(prp, make_float2(vsu[g], vsu[g + 1]));
+              const float2 hi = make_float2(__uint_as_float(__float_as_uint(w.x) & 0xffffe000u),
+                                            __uint_as_float(__float_as_uint(w.y) & 0xffffe000u));
+              const float2 lo = fsub2(w, hi);
+              const __half2 h0 = __floats2half2_rn(hi.x, lo.x), h1 = __floats2half2_rn(hi.y, lo.y);
+              wp[h * NG + g] = *reinterpret_cast<const uint32_t *>(&h0);
+              wp[h * NG + g + 1] = *reinterpret_cast<const uint32_t *>(&h1);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              ozp[h][g] = fmaf(pr, vz[g], ozp[h][g]);
+              wp[h * NG + g] = split(pr * vsu[g]);
+            }
           }
         }
         if constexpr (C::BW_MN) {
