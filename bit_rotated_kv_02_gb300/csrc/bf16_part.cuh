@@ -58,7 +58,7 @@ __device__ __forceinline__ StepState step_state(const PoolArgs &p, int b) {
 // v_new); demotion scratch is separate (DEMOTE_SCRATCH bytes).
 template <int G>
 struct BfSmem {
-  float qr[G][D];
+  alignas(16) float qr[D][G];  // the queries, channel-major (a channel's G values adjacent, read in 8-byte pairs)
   float wm[BF_WARPS][G], wl[BF_WARPS][G];
   float wo[BF_WARPS][G][D];
   float pbuf[BF_WARPS][G][16];
@@ -229,7 +229,7 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
   }
   slen = max(0, min(slen, SINK)); rs = max(0, min(rs, RECENT - 1)); rl = max(0, min(rl, RECENT));
   const int n = (chunk == 0) ? slen : max(0, min(64, rl - (chunk - 1) * 64));
-  for (int i = tid; i < G * D; i += 128) sm.qr[i / D][i % D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
+  for (int i = tid; i < G * D; i += 128) sm.qr[i % D][i / D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
   // the demotion first: its R rows are read while the history CTAs are still starting, and the CTA's own
   // chunk then ends about when a chunk without a demotion would have
@@ -253,6 +253,7 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
   // the products of two bf16 values are exact in float32; their sum carries its rounding errors
   // (TwoSum), so that the score is the exact dot product rounded about once: logits of several
   // hundred with two tokens sharing the weight need that accuracy
+  // (heads in pairs on paired float32 operations, each lane rounding as the scalar TwoSum does)
   float dot[G], cmp[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) dot[h] = cmp[h] = 0.f;
@@ -261,22 +262,39 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
     uint4 w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = kr[i];
+    constexpr int GP = G / 2;  // head pairs
+    float2 d2[GP > 0 ? GP : 1], c2[GP > 0 ? GP : 1];
+#pragma unroll
+    for (int k = 0; k < GP; ++k) d2[k] = c2[k] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float kv = bf16_to_f32((ws[e >> 1] >> (16 * (e & 1))) & 0xffffu);
-        const int c = hf * 64 + 8 * i + e;
+        const float *qc = sm.qr[hf * 64 + 8 * i + e];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pr = kv * sm.qr[h][c];
+        for (int k = 0; k < GP; ++k) {
+          const float2 q2 = *reinterpret_cast<const float2 *>(qc + 2 * k);
+          const float2 pr = fmul2(make_float2(kv, kv), q2);  // exact: products of two bf16 values
+          const float2 s = fadd2(d2[k], pr), bp = fsub2(s, d2[k]);
+          const float2 er = fadd2(fsub2(d2[k], fsub2(s, bp)), fsub2(pr, bp));
+          d2[k] = s;
+          c2[k] = fadd2(c2[k], er);
+        }
+        if constexpr (G % 2 == 1) {
+          const float pr = kv * qc[G - 1];
           float t, e2;
-          two_sum_f32(dot[h], pr, t, e2);
-          dot[h] = t;
-          cmp[h] += e2;
+          two_sum_f32(dot[G - 1], pr, t, e2);
+          dot[G - 1] = t;
+          cmp[G - 1] += e2;
         }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < GP; ++k) {
+      dot[2 * k] = d2[k].x; dot[2 * k + 1] = d2[k].y;
+      cmp[2 * k] = c2[k].x; cmp[2 * k + 1] = c2[k].y;
     }
   }
   float m2[G], l[G], o[G][4];

@@ -1172,6 +1172,9 @@ struct BSmem {
   alignas(16) uint8_t scratch[part::DEMOTE_SCRATCH];
   alignas(16) float qrot[G][D];
 };
+static_assert(offsetof(BSmem<2>, bf.qr) % 16 == 0 && offsetof(BSmem<4>, bf.qr) % 16 == 0 &&
+                  offsetof(BSmem<8>, bf.qr) % 16 == 0,
+              "query pairs are read with 8-byte loads");
 
 template <int G>
 __global__ void __launch_bounds__(128, 4) bf16_kernel(BArgs a) {
@@ -1193,7 +1196,7 @@ __global__ void __launch_bounds__(128, 4) bf16_kernel(BArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
 #pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.bf.qr[h][i0 + i], rv[i], acc[h]);
+        for (int h = 0; h < G; ++h) acc[h] = fmaf(sm.bf.qr[i0 + i][h], rv[i], acc[h]);
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) sm.qrot[h][c] = acc[h];

@@ -109,13 +109,15 @@ struct Smem {
   uint64_t csync;                                                    // consumer-warp barrier
   int meta_seg[NSTAGE], meta_ntok[NSTAGE][STAGE_PAGES], meta_flags[NSTAGE];  // flags: 1 last, 2 abort
   int meta_slot[NSTAGE];                                                      // partial slot of the stage
-  float qr[G][D];  // BF16 CTAs: the queries
+  alignas(16) float qr[D][G];  // BF16 CTAs: the queries, channel-major (read in 8-byte pairs)
   float wm[CONSUMER_WARPS][G], wl[CONSUMER_WARPS][G], wz[CONSUMER_WARPS][G];
   float wo[CONSUMER_WARPS][G][D];
   float pbuf[CONSUMER_WARPS][G][16];
   long long range_lo, range_n, n_dyn;
   int b0, kvh0, local0, np0, hl0;
 };
+static_assert(offsetof(Smem<2>, qr) % 16 == 0 && offsetof(Smem<4>, qr) % 16 == 0 && offsetof(Smem<8>, qr) % 16 == 0,
+              "query pairs are read with 8-byte loads");
 
 // Query fragments of one (sequence, KV head) as the history consumers use them: per MMA lane, the B
 // operands bq[nt][j][hb] (NT * 16 words) and the score factors kf[nt], zf[nt] of the lane's accumulator
