@@ -327,16 +327,25 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
     const int t2 = 16 * warp + j;
     vv[j] = t2 < n ? reinterpret_cast<const uint2 *>(vrow(t2))[lane] : make_uint2(0, 0);
   }
+  // (channel pairs on paired float32 FMAs)
+  float2 ov[G][2];
+#pragma unroll
+  for (int h = 0; h < G; ++h) ov[h][0] = ov[h][1] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const float v[4] = {bf16_to_f32(vv[j].x & 0xffffu), bf16_to_f32(vv[j].x >> 16), bf16_to_f32(vv[j].y & 0xffffu),
-                        bf16_to_f32(vv[j].y >> 16)};
+    const float2 v01 = make_float2(bf16_to_f32(vv[j].x & 0xffffu), bf16_to_f32(vv[j].x >> 16));
+    const float2 v23 = make_float2(bf16_to_f32(vv[j].y & 0xffffu), bf16_to_f32(vv[j].y >> 16));
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float pj = sm.pbuf[warp][h][j];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) o[h][k] = fmaf(pj, v[k], o[h][k]);
+      ov[h][0] = ffma2(make_float2(pj, pj), v01, ov[h][0]);
+      ov[h][1] = ffma2(make_float2(pj, pj), v23, ov[h][1]);
     }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    o[h][0] = ov[h][0].x; o[h][1] = ov[h][0].y;
+    o[h][2] = ov[h][1].x; o[h][3] = ov[h][1].y;
   }
 #pragma unroll
   for (int h = 0; h < G; ++h) {
