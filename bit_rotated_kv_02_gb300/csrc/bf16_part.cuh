@@ -27,6 +27,7 @@ struct StepState {
   bool demote;    // the oldest window token moves to history position hist_len
   bool append;    // the new token is stored
   bool to_sink;   // ... into the sink (else into the window)
+  int page;       // the page-table entry of history row hl (read when the window is full)
   int slen, hl, rs, rl;        // before
   int nslen, nhl, nrs, nrl;    // after
 };
@@ -38,9 +39,10 @@ __device__ __forceinline__ StepState step_state(const PoolArgs &p, int b) {
   const bool want = st.ok && st.rl == RECENT;
   st.want = want;
   st.demote = false;
+  st.page = -1;
   if (want && st.hl / PAGE < p.max_pages) {
-    const int page = p.page_table[(size_t)b * p.max_pages + st.hl / PAGE];
-    st.demote = page >= 0 && page < p.num_pages;
+    st.page = p.page_table[(size_t)b * p.max_pages + st.hl / PAGE];
+    st.demote = st.page >= 0 && st.page < p.num_pages;
   }
   st.append = st.ok && !(want && !st.demote);
   st.nslen = st.slen; st.nhl = st.hl; st.nrs = st.rs; st.nrl = st.rl;
@@ -97,6 +99,13 @@ __device__ __noinline__ void demote_role(const A &a, uint8_t *scratch, int b, in
   uint16_t *dsz = reinterpret_cast<uint16_t *>(dcode + D / 4);      // scale[4], zero[4] (one per group)
   const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
   const float *cb = kv == 0 ? p.cb_k : p.cb_v;
+  // this warp's first 16 rows of R are requested with the vector (they do not depend on it)
+  float4 rrow[16];
+  {
+    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)(32 * warp) * (D / 4) + lane;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) rrow[i] = R4[i * (D / 4)];
+  }
   if (warp == 0) {
     const uint2 xw = reinterpret_cast<const uint2 *>((kv == 0 ? p.recent_k : p.recent_v) +
                                                      (((size_t)b * p.Hkv + kvh) * RECENT + st.rs) * D)[lane];
@@ -110,10 +119,11 @@ __device__ __noinline__ void demote_role(const A &a, uint8_t *scratch, int b, in
 #pragma unroll 1
   for (int bt = 0; bt < 2; ++bt) {
     const int r0 = 32 * warp + 16 * bt;
-    const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)r0 * (D / 4) + lane;
-    float4 rrow[16];
+    if (bt == 1) {
+      const float4 *R4 = reinterpret_cast<const float4 *>(Rw) + (size_t)r0 * (D / 4) + lane;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) rrow[i] = R4[i * (D / 4)];
+      for (int i = 0; i < 16; ++i) rrow[i] = R4[i * (D / 4)];
+    }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float xi = xs[r0 + i], ax = fabsf(xi);
@@ -141,8 +151,8 @@ __device__ __noinline__ void demote_role(const A &a, uint8_t *scratch, int b, in
                        cb != nullptr ? cb + 4 * kvh : nullptr);
   }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
-  if (tid < D / 4) {  // the demoted codes, scale and zero into history row hist_len
-    const int page = p.page_table[(size_t)b * p.max_pages + st.hl / PAGE];
+  if (tid < D / 4) {  // the demoted codes, scale and zero into history row hist_len (its page: step_state's)
+    const int page = st.page;
     const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + st.hl % PAGE;
     if (OSCAR_DCHECK(page >= 0 && page < p.num_pages, p.err)) {
     (kv == 0 ? p.codes_k : p.codes_v)[row * (D / 4) + tid] = dcode[tid];
@@ -214,6 +224,14 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
   if (!OSCAR_DCHECK(seg < p.B * p.Hkv, p.err)) return;
   float *slot = a.part + ((size_t)a.n_hist + (size_t)p.B * p.Hkv + (size_t)seg * 5 + chunk) * G * PART_STRIDE;
   if (warp >= BF_WARPS) return;
+  // the queries are requested first (they do not depend on the counters)
+  constexpr int QPT = (G * D + 127) / 128;
+  uint16_t qv[QPT];
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = tid + 128 * k;
+    qv[k] = i < G * D ? a.q[((size_t)b * p.Hq + kvh * G) * D + i] : 0;
+  }
   int slen, rs, rl;
   int new_at = -1;  // step form: the chunk-local index of the new token (read from k_new / v_new)
   StepState st{};
@@ -229,7 +247,11 @@ __device__ __forceinline__ void bf16_role(const A &a, SM &sm, int idx, uint8_t *
   }
   slen = max(0, min(slen, SINK)); rs = max(0, min(rs, RECENT - 1)); rl = max(0, min(rl, RECENT));
   const int n = (chunk == 0) ? slen : max(0, min(64, rl - (chunk - 1) * 64));
-  for (int i = tid; i < G * D; i += 128) sm.qr[i % D][i / D] = bf16_to_f32(a.q[((size_t)b * p.Hq + kvh * G) * D + i]);
+#pragma unroll
+  for (int k = 0; k < QPT; ++k) {
+    const int i = tid + 128 * k;
+    if (i < G * D) sm.qr[i % D][i / D] = bf16_to_f32(qv[k]);
+  }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
   // the demotion first: its R rows are read while the history CTAs are still starting, and the CTA's own
   // chunk then ends about when a chunk without a demotion would have
