@@ -72,6 +72,39 @@ def test_batches_above_32_uneven_contexts(B):
     assert P.err() == 0 and int(P.sync.abs().sum()) == 0
 
 
+def test_one_long_sequence_among_many_short():
+    """40 sequences, one with a 60k-token context and 39 short ones: the merge grid then merges four query
+    heads per CTA, and the long sequence's segments hold more partials (about 52) than one staging round
+    of the wide merge (48), so the merge stages them head by head in two rounds; attention, then decode
+    steps."""
+    seed, B, Hq, Hkv = 960, 40, 32, 8
+    g = synth.rng(seed)
+    lens = [int(x) for x in g.integers(300, 400, size=B)]
+    lens[5] = 60_000
+    steps = 3
+    O, P = helpers.make_pools(B, Hq, Hkv, 128, [_pages(L, steps) for L in lens], seed)
+    ch = synth.outlier_channels(seed, Hkv, 128, 4)
+    for b, L in enumerate(lens):
+        K = synth.outlier_kv(seed + 10 + b, L, Hkv, 128, ch)
+        V = synth.outlier_kv(seed + 500 + b, L, Hkv, 128, ch)
+        O.prefill(b, K, V)
+        ok.oscar_prefill_pool(P, b, helpers.to_dev_bf16(K), helpers.to_dev_bf16(V))
+    torch.cuda.synchronize()
+    q = synth.outlier_q(seed + 7, B, Hq, Hkv, 128, ch)
+    out = ok.oscar_decode_attention(P, helpers.to_dev_bf16(q))
+    helpers.assert_attention_close(out.cpu().numpy(), O.decode(q))
+    for t in range(steps):
+        kn = synth.outlier_kv(seed + 2000 + t, B, Hkv, 128, ch)
+        vn = synth.outlier_kv(seed + 3000 + t, B, Hkv, 128, ch)
+        qt = synth.outlier_q(seed + 4000 + t, B, Hq, Hkv, 128, ch)
+        O.append(kn, vn)
+        out = ok.oscar_decode_step(P, helpers.to_dev_bf16(kn), helpers.to_dev_bf16(vn), helpers.to_dev_bf16(qt))
+        helpers.assert_attention_close(out.cpu().numpy(), O.decode(qt))
+    torch.cuda.synchronize()
+    helpers.assert_pools_equal(O, P)
+    assert P.err() == 0 and int(P.sync.abs().sum()) == 0
+
+
 def _fill_sampled(O, P, lens, sampled, seed, ch, Hkv, heads=None):
     """Prefill: sampled sequences from seeded host draws (both pools), the rest from GPU draws."""
     gen = torch.Generator(device="cuda")
