@@ -1181,26 +1181,28 @@ static cudaError_t launch_v1_g(const PoolArgs &p, const uint16_t *q, float *out,
 
 // The merge of a decode launch whose partial slots follow this file's layout (history slots cta + segment
 // for n_hist history CTAs, then the BF16 and demoted-token slots); k_new != NULL: the decode-step form.
-// Query heads per merge CTA: one while the grid takes at most four waves of one CTA per SM (the waves after
-// the first run their copies of R_v and their counter reads behind the first), else the smallest power of
-// two that brings it within four waves, at most G.
-static int merge_heads_per_cta(const PoolArgs &p) {
+// Merge grid: grids of more CTAs than SMs run the wide build (two CTAs per SM); query heads per CTA: the
+// smallest power of two (at most G) that brings the grid within one wave of it, or, past G, as many waves as
+// it takes.
+static int merge_sms(const PoolArgs &) {
   static std::atomic<int> sms_cache[kMaxDevices];
-  const int sms = per_device(sms_cache, [](int dev) {
+  return per_device(sms_cache, [](int dev) {
     int n = 148;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     return n;
   });
-  const int G = p.Hq / p.Hkv;
+}
+static int merge_heads_per_cta(const PoolArgs &p) {
+  const int sms = merge_sms(p), G = p.Hq / p.Hkv;
   int hpc = 1;
-  while (hpc < G && (long long)(G / hpc) * p.Hkv * p.B > 4LL * sms) hpc *= 2;
+  while (hpc < G && (long long)(G / hpc) * p.Hkv * p.B > 2LL * sms) hpc *= 2;
   return hpc;
 }
 
 cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, float *out, const uint16_t *k_new,
                             const uint16_t *v_new, cudaStream_t s, bool dyn) {
   const int hpc = merge_heads_per_cta(p);
-  const bool wide = hpc > 1;
+  const bool wide = (long long)(p.Hq / p.Hkv / hpc) * p.Hkv * p.B > merge_sms(p);
   const size_t smem = v1::merge_smem(wide);
   auto go = [&](auto kernel) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1209,7 +1211,7 @@ cudaError_t launch_merge_v1(const PoolArgs &p, const float *part, int n_hist, fl
                       k_new, v_new, hpc, dyn ? 1 : 0);
   };
   switch (p.Hq / p.Hkv) {
-    case 1: return go(v1::merge_kernel<1, false>);
+    case 1: return wide ? go(v1::merge_kernel<1, true>) : go(v1::merge_kernel<1, false>);
     case 2: return wide ? go(v1::merge_kernel<2, true>) : go(v1::merge_kernel<2, false>);
     case 4: return wide ? go(v1::merge_kernel<4, true>) : go(v1::merge_kernel<4, false>);
     case 8: return wide ? go(v1::merge_kernel<8, true>) : go(v1::merge_kernel<8, false>);
