@@ -856,8 +856,8 @@ __host__ __device__ constexpr size_t merge_smem(bool wide) {
 }
 // hpc query heads per CTA (grid G / hpc x Hkv x B): large grids merge several heads of a (sequence, KV head)
 // in one CTA, one after the other, with one copy of R_v and one location of the partials; their partials
-// are staged together (one round trip) when they fit.  WIDE: the build for those grids, with a smaller
-// staging buffer so that two CTAs share an SM.
+// are staged together (one round trip) when they fit.  WIDE: the build for grids of more CTAs than SMs, with
+// a smaller staging buffer so that two CTAs share an SM.
 template <int G, bool WIDE>
 __global__ void __launch_bounds__(MT, WIDE ? 2 : 1) merge_kernel(PoolArgs p, const float *part, int n_hist, float *out,
                                                    const uint16_t *k_new, const uint16_t *v_new, int hpc, int dyn) {
