@@ -65,7 +65,7 @@ struct BfSmem {
   float wo[BF_WARPS][G][D];
   float pbuf[BF_WARPS][G][16];
 };
-constexpr int DEMOTE_SCRATCH = (D + 2 * 4 * 32 * 4) * 4 + D / 4 + 16 + 16;
+constexpr int DEMOTE_SCRATCH = (D + 2 * 4 * 32 * 4) * 4 + D / 4 + 16 + 64 + 16;
 
 // ---------------------------------------------------------------------------------------------
 // Decode-step demotion, run by BF16 CTAs before their chunk:
@@ -97,6 +97,7 @@ __device__ __noinline__ void demote_role(const A &a, uint8_t *scratch, int b, in
   float *psab = pacc + 4 * 32 * 4;
   uint8_t *dcode = reinterpret_cast<uint8_t *>(psab + 4 * 32 * 4);  // [D / 4]
   uint16_t *dsz = reinterpret_cast<uint16_t *>(dcode + D / 4);      // scale[4], zero[4] (one per group)
+  float *red = reinterpret_cast<float *>(dsz + 8);                  // [16]: the quantizer's group extremes
   const float *Rw = (kv == 0 ? p.R_k : p.R_v) + (size_t)kvh * D * D;
   const float *cb = kv == 0 ? p.cb_k : p.cb_v;
   // this warp's first 16 rows of R are requested with the vector (they do not depend on it)
@@ -140,15 +141,13 @@ __device__ __noinline__ void demote_role(const A &a, uint8_t *scratch, int b, in
 #pragma unroll
   for (int k = 0; k < 4; ++k) { pacc[(warp * 32 + lane) * 4 + k] = acc[k]; psab[(warp * 32 + lane) * 4 + k] = sab[k]; }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
-  if (warp == 0) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc[k] = (pacc[lane * 4 + k] + pacc[(32 + lane) * 4 + k]) + (pacc[(64 + lane) * 4 + k] + pacc[(96 + lane) * 4 + k]);
-      sab[k] = (psab[lane * 4 + k] + psab[(32 + lane) * 4 + k]) + (psab[(64 + lane) * 4 + k] + psab[(96 + lane) * 4 + k]);
-    }
+  {  // thread e quantizes element e (its four warps' partial sums, added as one warp would)
+    const int k = tid & 3, l = tid >> 2;
+    const float a = (pacc[l * 4 + k] + pacc[(32 + l) * 4 + k]) + (pacc[(64 + l) * 4 + k] + pacc[(96 + l) * 4 + k]);
+    const float sb = (psab[l * 4 + k] + psab[(32 + l) * 4 + k]) + (psab[(64 + l) * 4 + k] + psab[(96 + l) * 4 + k]);
     QuantStats qst{0, 0, 0};
-    quantize_from_dots(xs, Rw, Rw, D, acc, sab, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcode, dsz, dsz + 4, qst,
-                       cb != nullptr ? cb + 4 * kvh : nullptr);
+    quantize_from_dots_cta(xs, Rw, Rw, D, a, sb, (kv == 0 ? p.clip_k : p.clip_v)[kvh], p.g, dcode, dsz, dsz + 4, qst,
+                           cb != nullptr ? cb + 4 * kvh : nullptr, red, 1);
   }
   asm volatile("bar.sync 1, 128;\n" ::: "memory");
   if (tid < D / 4) {  // the demoted codes, scale and zero into history row hist_len (its page: step_state's)

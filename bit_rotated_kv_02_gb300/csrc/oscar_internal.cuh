@@ -363,6 +363,106 @@ __device__ inline void quantize_from_dots(const float *xs, const float *R, const
   }
 }
 
+// Named barrier `bar` over 128 threads, and the OR of a predicate over them.
+__device__ __forceinline__ void bar_sync128(int bar) { asm volatile("bar.sync %0, 128;\n" ::"r"(bar) : "memory"); }
+__device__ __forceinline__ bool bar_or128(int bar, bool v) {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+               : "=r"(r)
+               : "r"((uint32_t)v), "r"(bar)
+               : "memory");
+  return r != 0;
+}
+
+// quantize_from_dots on the first 128 threads of a CTA (four warps, named barrier `bar`), one element per
+// thread (element e = thread e): the same intervals, decisions and results, with a chain a quarter as long.
+// A group's extremes combine its warps through `red` (shared memory, 16 floats); the Dot2 and exact
+// evaluations run warp by warp over each warp's own flagged elements.
+__device__ inline void quantize_from_dots_cta(const float *xs, const float *R, const float *R2, int ld2, float acc,
+                                              float sab, float clip, int g, uint8_t *codes_out, uint16_t *scale_out,
+                                              uint16_t *zero_out, QuantStats &st, const float *cb, float *red, int bar) {
+  const int e = threadIdx.x & 127, lane = e & 31, warp = e >> 5;
+  const int wpg = g / 32;              // warps per group (1, 2 or 4)
+  const int gw0 = (warp / wpg) * wpg;  // the first warp of this thread's group
+  // gamma_128 = 7.6294e-6; 8e-6 also covers the rounding of sab itself; 1e-37 covers underflow.
+  const float E = __fadd_ru(__fmul_ru(sab, 8.0e-6f), 1e-37f);
+  float lo = __fsub_rd(acc, E), hi = __fadd_ru(acc, E);
+  // minima of a, b and maxima of c, d over the group
+  auto group4 = [&](float &a, float &b, float &c, float &d) {
+    for (int off = 16; off > 0; off >>= 1) {
+      a = fminf(a, __shfl_xor_sync(FULL, a, off));
+      b = fminf(b, __shfl_xor_sync(FULL, b, off));
+      c = fmaxf(c, __shfl_xor_sync(FULL, c, off));
+      d = fmaxf(d, __shfl_xor_sync(FULL, d, off));
+    }
+    if (wpg > 1) {
+      bar_sync128(bar);  // every earlier read of red is done
+      if (lane == 0) {
+        red[4 * warp + 0] = a; red[4 * warp + 1] = b; red[4 * warp + 2] = c; red[4 * warp + 3] = d;
+      }
+      bar_sync128(bar);
+      for (int w = gw0; w < gw0 + wpg; ++w) {
+        a = fminf(a, red[4 * w + 0]); b = fminf(b, red[4 * w + 1]);
+        c = fmaxf(c, red[4 * w + 2]); d = fmaxf(d, red[4 * w + 3]);
+      }
+    }
+  };
+  float mn_lo = lo, mn_hi = hi, mx_lo = lo, mx_hi = hi;
+  group4(mn_lo, mn_hi, mx_lo, mx_hi);
+  uint16_t z = zero_of(clip, mn_lo), s = scale_of(clip, mn_hi, mx_lo);
+  bool uz = z != zero_of(clip, mn_hi), us = s != scale_of(clip, mn_lo, mx_hi);
+  if ((uz || us) && (e & (g - 1)) == 0) ++st.exact_groups;
+  bool unproven = false;
+  // candidates for the extremes: only elements whose interval reaches the group's extreme
+  const bool cmin = (uz || us) && lo <= mn_hi, cmax = us && hi >= mx_lo, cand = cmin || cmax;
+  int done = -1;  // highest tier already applied to the element
+  auto evaluate = [&](bool flag, int tier) {
+    uint32_t mine = __ballot_sync(FULL, flag && done < tier);
+    while (mine != 0) {
+      const int src = __ffs(mine) - 1;
+      mine &= mine - 1;
+      float2 iv;
+      if (tier == 0) iv = dot2_interval_xs(xs, R2, ld2, 32 * warp + src);
+      else iv.x = iv.y = exact_rot_elem(xs, R, 32 * warp + src, unproven);
+      if (lane == src) { lo = iv.x; hi = iv.y; done = tier; }
+      ++st.exact_elems;
+    }
+  };
+  for (int tier = 0; tier < 2; ++tier) {
+    if (!bar_or128(bar, uz || us)) break;
+    evaluate(cand, tier);
+    float a0 = cmin ? lo : INFINITY, a1 = cmin ? hi : INFINITY, b0 = cmax ? lo : -INFINITY, b1 = cmax ? hi : -INFINITY;
+    group4(a0, a1, b0, b1);
+    if (uz) {
+      const uint16_t z1 = zero_of(clip, a0);
+      if (z1 == zero_of(clip, a1) || tier == 1) { z = z1; uz = false; }
+    }
+    if (us) {
+      const uint16_t s1 = scale_of(clip, a1, b0);
+      if (s1 == scale_of(clip, a0, b1) || tier == 1) { s = s1; us = false; }
+    }
+  }
+  const float zf = bf16_to_f32(z), sf = bf16_to_f32(s);
+  const bool valid = sf != 0.0f && isfinite(sf);
+  const float3 mids = cb != nullptr ? level_midpoints(cb) : make_float3(0.f, 0.f, 0.f);
+  auto code_at = [&](float x) { return cb != nullptr ? code_of_levels(x, zf, sf, valid, mids) : code_of(x, zf, sf, valid); };
+  int code = 0;
+  for (int tier = 0; tier < 3; ++tier) {
+    code = code_at(lo);
+    const bool need = code != code_at(hi);
+    if (tier == 2 || !__any_sync(FULL, need)) break;
+    evaluate(need, tier);
+  }
+  if (__any_sync(FULL, unproven) && lane == 0) ++st.unproven;
+  const int c1 = __shfl_down_sync(FULL, code, 1), c2 = __shfl_down_sync(FULL, code, 2),
+            c3 = __shfl_down_sync(FULL, code, 3);
+  if ((lane & 3) == 0) codes_out[e >> 2] = (uint8_t)(code | (c1 << 2) | (c2 << 4) | (c3 << 6));
+  if ((e & (g - 1)) == 0) {
+    scale_out[e / g] = s;
+    zero_out[e / g] = z;
+  }
+}
+
 // Load one bf16 head vector (128 values, 8-byte aligned) into the warp's shared float32 buffer.
 __device__ __forceinline__ void load_vec_to_smem(const uint16_t *x, float *xs) {
   const int lane = threadIdx.x & 31;

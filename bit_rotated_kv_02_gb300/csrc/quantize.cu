@@ -30,6 +30,7 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
   __shared__ float xs[D];
   __shared__ float pacc[DEMOTE_WARPS][32][4], psab[DEMOTE_WARPS][32][4];
   __shared__ int s_ok;
+  __shared__ float qred[16];       // the quantizer's group extremes
   extern __shared__ float4 rs4[];  // this CTA's R, row stride RS_LD floats, for the Dot2 tier
   pdl_wait();
   pdl_trigger();
@@ -98,23 +99,19 @@ __global__ void __launch_bounds__(256, 1) demote_append_kernel(PoolArgs p, const
 #pragma unroll
     for (int k = 0; k < 4; ++k) { pacc[warp][lane][k] = acc[k]; psab[warp][lane][k] = sab[k]; }
     __syncthreads();
-    if (warp == 0) {
+    if (threadIdx.x < D) {  // thread e quantizes element e (the warps' partial sums in the order one warp adds them)
+      const int k = threadIdx.x & 3, l = threadIdx.x >> 2;
+      float a8 = 0.f, s8 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float a8 = 0.f, s8 = 0.f;
-#pragma unroll
-        for (int w = 0; w < DEMOTE_WARPS; ++w) { a8 += pacc[w][lane][k]; s8 += psab[w][lane][k]; }
-        acc[k] = a8;
-        sab[k] = s8;
-      }
+      for (int w = 0; w < DEMOTE_WARPS; ++w) { a8 += pacc[w][l][k]; s8 += psab[w][l][k]; }
       const float clip = (kv == 0 ? p.clip_k : p.clip_v)[kvh];
       const size_t row = ((size_t)page * p.Hkv + kvh) * PAGE + (hl % PAGE);
       QuantStats st{0, 0, 0};
       const float *cb = kv == 0 ? p.cb_k : p.cb_v;
-      quantize_from_dots(xs, Rw, reinterpret_cast<const float *>(rs4), RS_LD, acc, sab, clip, p.g,
-                         (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
-                         (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
-                         st, cb != nullptr ? cb + 4 * kvh : nullptr);
+      quantize_from_dots_cta(xs, Rw, reinterpret_cast<const float *>(rs4), RS_LD, a8, s8, clip, p.g,
+                             (kv == 0 ? p.codes_k : p.codes_v) + row * (D / 4),
+                             (kv == 0 ? p.scale_k : p.scale_v) + row * p.ng, (kv == 0 ? p.zero_k : p.zero_v) + row * p.ng,
+                             st, cb != nullptr ? cb + 4 * kvh : nullptr, qred, 1);
     }
   }
   __syncthreads();  // the demoted slot is read before the append may overwrite it
